@@ -1,0 +1,445 @@
+"""Benchmark of the GB300 sparse-MoE block (one JSON line on rank 0).
+
+Metric: MoE-block tokens/s at the serving configurations T = 1 (decode),
+T = 32 (speculative verify, 8 sequences x 4 draft tokens) and T = 2048
+(prefill chunk); H = 2048, 256 experts top-8, I = Is = 512, int8 group-128
+weights with bf16 scales, bf16 activations.  The headline `value` is the
+workload named by --workload (default: verify T=32); the other two are in
+`workloads`.
+
+Timing protocol:
+  * weights and inputs are resident in HBM before timing starts;
+  * L2 stays cold across steps: R rotating weight banks (each a relabelled
+    copy of the seeded weights with its experts permuted, so the same math
+    reads different memory) and R distinct inputs; the bytes one lap of the
+    banks touches exceed L2 (129 MB) many times over;
+  * each step is one CUDA-graph replay of moe_block_forward; W warm-up steps,
+    then exactly K timed steps between CUDA events, barrier + synchronize on
+    both sides, max over ranks;
+  * a second timed pass runs the profiled entry point (events between the
+    block's kernels) to give the dominant kernel's average duration;
+  * e2e: moe_block_forward_host with pinned host x/out, copies inside;
+  * cpu_baseline: the fp64 oracle on this host's cores, on a bounded sample.
+Multi-GPU: replicas only (the block has no exchange step); each rank runs
+the same workload on its own GPU and `value` sums the ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+WORKLOAD_T = {"decode": 1, "verify": 32, "prefill": 2048}
+LABEL = {"decode": "decode_T1", "verify": "verify_T32", "prefill": "prefill_T2048"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "src": "fallback"}
+
+
+# --------------------------------------------------------------- clocks
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- workloads
+
+def algorithmic_bytes(d: W.Dims, T: int, n_active: int):
+    """Bytes the method must touch: each distinct routed expert's int8
+    weights + scales once, the shared expert, router + gate rows, x in, out."""
+    return ((n_active + (1 if d.Is else 0)) * d.expert_bytes + d.router_bytes +
+            2 * 2 * T * d.H)
+
+
+def gateup_bytes(d: W.Dims, T: int, n_active: int):
+    H, I, Is, G = d.H, d.I, d.Is, d.G
+    per = 2 * I * H + 2 * 2 * I * (H // G)
+    sh = 2 * Is * H + 2 * 2 * Is * (H // G) if Is else 0
+    return n_active * per + sh + 2 * T * H + 2 * (T * 8 * I + T * Is)
+
+
+def algorithmic_flops(d: W.Dims, T: int):
+    H, I, Is = d.H, d.I, d.Is
+    return 2 * T * (8 * 3 * I * H + 3 * Is * H + 256 * H + H)
+
+
+class Bench:
+    def __init__(self, name, moe, torch, dev, banks, seed_base=0):
+        self.name = name
+        self.moe, self.torch, self.dev = moe, torch, dev
+        wl = W.WORKLOADS[name]
+        self.d = wl.dims
+        self.T = T = WORKLOAD_T[name]
+        self.R = banks
+        host_w = W.make_weights(self.d, wl.seed)
+        self.host_w = host_w
+        base = {k: self._up(v) for k, v in host_w.items()}
+        # R banks: bank r relabels experts by a seeded permutation
+        self.banks, self.keep = [], []
+        for r in range(banks):
+            perm = torch.from_numpy(W.expert_permutation(256, wl.seed, r)).to(dev)
+            w = dict(base)
+            if r > 0:
+                for k in ("w_router", "w13_q", "w13_s", "w2_q", "w2_s"):
+                    w[k] = base[k].index_select(0, perm).contiguous()
+            self.keep.append(w)
+            self.banks.append(moe.weights_struct(w))
+        # R inputs
+        self.x_host, self.x = [], []
+        for r in range(banks):
+            x, _ = W.make_x(self.d, T, wl.seed * 1000 + r, wl.skew_tokens, host_w["w_router"])
+            self.x_host.append(x)
+            self.x.append(self._up(x))
+        self.dims = moe.Dims.make(self.d.H, self.d.I, self.d.Is)
+        self.ws_bytes = moe.moe_workspace_bytes(self.dims, T)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.out = torch.empty((T, self.d.H), dtype=torch.int16, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.nk = moe.moe_block_kernel_count(self.dims, T)
+        self.kernel_names = [moe.moe_block_kernel_name(self.dims, T, i) for i in range(self.nk)]
+        # routing of each input (bank 0 computes the same ids up to relabelling)
+        ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
+        self.n_active = []
+        for r in range(banks):
+            moe.moe_block_forward(self.dims, self.banks[0], self.x[r], T, self.out, ids, None,
+                                  None, None, self.ws, self.ws_bytes)
+            self.n_active.append(len(np.unique(ids.cpu().numpy())))
+        torch.cuda.synchronize()
+        assert moe.moe_read_status(self.ws) == 0
+
+    def _up(self, a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return self.torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
+    def step(self, r, events=None):
+        if events is None:
+            self.moe.moe_block_forward(self.dims, self.banks[r], self.x[r], self.T, self.out, None,
+                                       None, None, None, self.ws, self.ws_bytes, self.stream)
+        else:
+            self.moe.moe_block_forward_profiled(self.dims, self.banks[r], self.x[r], self.T,
+                                                self.out, self.ws, self.ws_bytes, events,
+                                                self.stream)
+
+    def graphs(self, profiled_steps=0):
+        torch = self.torch
+        gs = []
+        with torch.cuda.stream(self.stream):
+            for r in range(self.R):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    self.step(r)
+                gs.append(g)
+        self.plain = gs
+        self.prof = []
+        self.prof_events = []
+        with torch.cuda.stream(self.stream):
+            for i in range(profiled_steps):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(self.nk + 1)]
+                for e in ev:  # creates the underlying cudaEvent_t before capture
+                    e.record(self.stream)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    self.step(i % self.R, ev)
+                self.prof.append(g)
+                self.prof_events.append(ev)
+
+    def run(self, steps, warmup, barrier, clocks_index):
+        torch = self.torch
+        self.graphs(profiled_steps=steps)
+        s = self.stream
+        for i in range(warmup):
+            self.plain[i % self.R].replay()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with Clocks(clocks_index) as clk:
+            torch.cuda.synchronize()
+            barrier()
+            t_wall = time.perf_counter()
+            e0.record(s)
+            for i in range(steps):
+                self.plain[i % self.R].replay()
+            e1.record(s)
+            torch.cuda.synchronize()
+            t_wall = time.perf_counter() - t_wall
+            barrier()
+            ms = e0.elapsed_time(e1) / steps
+            # profiled pass: same steps, events between kernels
+            for i in range(min(warmup, len(self.prof))):
+                self.prof[i].replay()
+            torch.cuda.synchronize()
+            for g in self.prof:
+                g.replay()
+            torch.cuda.synchronize()
+        per_kernel = np.zeros(self.nk)
+        for ev in self.prof_events:
+            for k in range(self.nk):
+                per_kernel[k] += ev[k].elapsed_time(ev[k + 1])
+        per_kernel /= max(1, len(self.prof_events))
+        assert self.moe.moe_read_status(self.ws) == 0
+        return ms, t_wall, per_kernel, clk.summary()
+
+    def e2e(self, steps, warmup):
+        """Whole call through the host entry point: H2D of x, block, D2H."""
+        torch = self.torch
+        xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in self.x_host]
+        oh = torch.empty((self.T, self.d.H), dtype=torch.int16).pin_memory()
+        for i in range(warmup):
+            self.moe.moe_block_forward_host(self.dims, self.banks[i % self.R], xh[i % self.R],
+                                            self.T, oh, self.ws, self.ws_bytes, self.stream)
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for i in range(steps):
+            self.moe.moe_block_forward_host(self.dims, self.banks[i % self.R], xh[i % self.R],
+                                            self.T, oh, self.ws, self.ws_bytes, self.stream)
+        t = time.perf_counter() - t
+        return t / steps, 2 * self.T * self.d.H, 2 * self.T * self.d.H
+
+
+def _oracle_inputs(name: str, n: int):
+    wl = W.WORKLOADS[name]
+    w = W.make_weights(wl.dims, wl.seed)
+    T = WORKLOAD_T[name]
+    x, _ = W.make_x(wl.dims, max(n, T), wl.seed * 1000, wl.skew_tokens if n <= T else 0,
+                    w["w_router"])
+    return wl.dims, w, x
+
+
+def oracle_steps(name: str, steps: int, warmup: int, budget_s: float | None = None):
+    """The oracle as it stands on this host's cores.  One step = `cores`
+    tokens of the workload's recipe through A1..A7 (fp64, one token per
+    thread).  With a budget, the number of steps is cut to fit it."""
+    import oracle
+    cores = os.cpu_count() or 1
+    dims, w, x = _oracle_inputs(name, cores)
+    toks = np.arange(cores, dtype=np.int32)
+
+    def one():
+        oracle.block_forward(dims.as_dict(), w, x, tokens=toks, nthreads=cores)
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    done = 0
+    while done < steps:
+        one()
+        done += 1
+        if budget_s is not None and time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    T = WORKLOAD_T[name]
+    return {"value": done * cores / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "%d steps x %d tokens drawn like the %s batch (T=%d) through the fp64 "
+                      "oracle, %d threads, %.1f s" % (done, cores, LABEL[name], T, cores, dt)}
+
+
+def cpu_baseline(name: str, budget_s: float = 10.0):
+    return oracle_steps(name, steps=1000, warmup=1, budget_s=budget_s)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOAD_T), default="verify")
+    ap.add_argument("--only", action="store_true", help="time only --workload")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        # the oracle is the reference arm: rank 0 only, host cores
+        if rank != 0:
+            return
+        cb = oracle_steps(args.workload, args.steps, args.warmup, budget_s=240.0)
+        T = WORKLOAD_T[args.workload]
+        line = {"impl": "reference", "metric": "moe_block_tokens_per_s", "value": cb["value"],
+                "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * (os.cpu_count() or 1) / cb["value"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": LABEL[args.workload], "T": T,
+                                                "H": 2048, "I": 512, "Is": 512, "E": 256,
+                                                "K": 8, "G": 128},
+                "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    import sparse_moe_decode_gb300 as moe
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_all(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pk = peaks()
+    order = [args.workload] + ([] if args.only else
+                               [n for n in ("decode", "verify", "prefill") if n != args.workload])
+    results = {}
+    head = None
+    for name in order:
+        T = WORKLOAD_T[name]
+        banks = 16 if T <= 32 else 2
+        b = Bench(name, moe, torch, dev, banks)
+        ms, wall, per_kernel, clk = b.run(args.steps, args.warmup, barrier, local)
+        ms = max_all(ms)
+        d = b.d
+        n_act = float(np.mean(b.n_active))
+        bytes_step = algorithmic_bytes(d, T, n_act)
+        gbs = bytes_step / (ms * 1e-3) / 1e9
+        flops = algorithmic_flops(d, T)
+        tfs = flops / (ms * 1e-3) / 1e12
+        t_hbm = bytes_step / (pk["hbm_gbs"] * 1e9)
+        t_tc = flops / (pk["bf16_tflops"] * 1e12)
+        k_dom = int(np.argmax(per_kernel))
+        r = {
+            "tokens_per_s": world * T / (ms * 1e-3), "ms_per_step": ms,
+            "T": T, "n_active_experts": n_act, "algorithmic_bytes": bytes_step,
+            "achieved_gbs": gbs, "frac_hbm_measured": gbs / pk["hbm_gbs"],
+            "frac_hbm_8000": gbs / 8000.0, "tflops": tfs,
+            "frac_bf16_peak": tfs / pk["bf16_tflops"],
+            "frac_roofline_time": max(t_hbm, t_tc) / (ms * 1e-3),
+            "kernels_ms": {n: float(v) for n, v in zip(b.kernel_names, per_kernel)},
+            "dominant_kernel": b.kernel_names[k_dom], "wall_s": wall, "clocks": clk,
+            "banks": banks,
+        }
+        if name == args.workload:
+            kb = gateup_bytes(d, T, n_act) if b.kernel_names[k_dom] == "gateup_swiglu" else None
+            r["_kernel"] = (b.kernel_names[k_dom], per_kernel[k_dom], kb)
+            e2e_s, bi, bo = b.e2e(args.steps, args.warmup)
+            e2e_s = max_all(e2e_s)
+            r["e2e"] = {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                        "d2h_bytes_per_step": bo}
+            r["gpu_launches"] = args.steps * b.nk
+            head = r
+        results[LABEL[name]] = r
+        del b
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        return
+    kname, kms, kbytes = head.pop("_kernel")
+    if kbytes is None:  # fall back to the block's bytes for another dominant kernel
+        kbytes = head["algorithmic_bytes"]
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+            "peak_src": pk["src"] + " (copy, burst)", "kernel_ms": kms,
+            "algorithmic_bytes_per_launch": kbytes}
+    cb = cpu_baseline(args.workload, budget_s=args.cpu_budget) if world == 1 or rank == 0 else None
+    line = {
+        "metric": "moe_block_tokens_per_s", "value": head["tokens_per_s"], "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8*bf16->f32", "data": "synthetic",
+        "config": {"workload": LABEL[args.workload], "T": head["T"], "H": 2048, "I": 512,
+                   "Is": 512, "E": 256, "K": 8, "G": 128, "parallelism": "replicas" if world > 1
+                   else "single", "l2": "cold: %d rotating weight banks (expert-permuted copies) "
+                   "and %d inputs, larger than L2" % (head["banks"], head["banks"])},
+        "roofline": roof, "cpu_baseline": cb, "e2e": head.pop("e2e"),
+        "gpu_launches": head.pop("gpu_launches"), "clocks": head["clocks"],
+        "workloads": results,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,363 @@
+// api.cu -- the extern "C" entry points of libmoe_gb300.so: argument checks,
+// workspace carving, and the order of kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "moe_gb300.h"
+
+namespace moe {
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status check_dims(const moe_dims *d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->num_experts != kE || d->top_k != kK || d->group != kG) return MOE_ERR_UNSUPPORTED;
+  if (d->hidden <= 0 || d->hidden % kG || d->hidden > kMaxH) return MOE_ERR_UNSUPPORTED;
+  if (d->expert_inter <= 0 || d->expert_inter % kG || d->expert_inter > kMaxI)
+    return MOE_ERR_UNSUPPORTED;
+  if (d->shared_inter < 0 || d->shared_inter % kG || d->shared_inter > kMaxI)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_weights(const moe_dims *d, const moe_weights *w, bool router, bool experts) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (router && (!w->w_router || !aligned(w->w_router, 16))) return MOE_ERR_INVALID_ARG;
+  if (experts) {
+    const void *p[4] = {w->w13_q, w->w13_s, w->w2_q, w->w2_s};
+    for (const void *q : p)
+      if (!q || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+  }
+  if (d->shared_inter > 0) {
+    if (router && (!w->w_shared_gate || !aligned(w->w_shared_gate, 16)))
+      return MOE_ERR_INVALID_ARG;
+    if (experts) {
+      const void *p[4] = {w->ws13_q, w->ws13_s, w->ws2_q, w->ws2_s};
+      for (const void *q : p)
+        if (!q || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  return MOE_OK;
+}
+
+bool ptr_ok(const void *p) { return p != nullptr && aligned(p, 16); }
+bool opt_ok(const void *p) { return p == nullptr || aligned(p, 16); }
+
+size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Workspace carving for a call with T tokens; offsets are 256-byte aligned
+// and grow monotonically with T, so a workspace sized for T_max serves every
+// T <= T_max.
+struct Layout {
+  size_t status, logits, gate_logit, ids, weights, sgate;
+  size_t counts, offsets, active, perm, slot_of;
+  size_t h_routed, h_shared, y, xstage, ostage, total;
+};
+
+Layout layout(const moe_dims *d, int T) {
+  Layout L{};
+  const size_t H = d->hidden, I = d->expert_inter, Is = d->shared_inter;
+  const size_t t = static_cast<size_t>(T);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += up256(bytes); return at; };
+  L.status = take(256);
+  L.logits = take(4 * t * kE);
+  L.gate_logit = take(4 * t);
+  L.ids = take(4 * t * kK);
+  L.weights = take(4 * t * kK);
+  L.sgate = take(4 * t);
+  L.counts = take(4 * kE);
+  L.offsets = take(4 * (kE + 1));
+  L.active = take(4 * (kE + 1));
+  L.perm = take(4 * t * kK);
+  L.slot_of = take(4 * t * kK);
+  L.h_routed = take(2 * t * kK * I);
+  L.h_shared = take(2 * t * (Is ? Is : 1));
+  L.y = take(4 * t * (kK + 1) * H);
+  L.xstage = take(2 * t * H);
+  L.ostage = take(2 * t * H);
+  L.total = o;
+  return L;
+}
+
+template <typename P>
+P *at(void *ws, size_t off) {
+  return reinterpret_cast<P *>(static_cast<uint8_t *>(ws) + off);
+}
+
+Lists lists_in(void *ws, const Layout &L) {
+  return Lists{at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.perm),
+               at<int32_t>(ws, L.slot_of), at<int32_t>(ws, L.active)};
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                  \
+  do {                                                 \
+    cudaError_t e_ = (expr);                           \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA;        \
+  } while (0)
+
+moe_status check_ws(const moe_dims *d, int T, const void *ws, size_t ws_bytes, Layout &L) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  L = layout(d, T);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// Kernel sequence of moe_block_forward (decode/verify route).
+const char *const kStageNames[] = {"router_gemv", "select_top8", "expert_lists",
+                                   "gateup_swiglu", "down", "combine"};
+constexpr int kStages = 6;
+
+// Records `ev[i]` after kernel i-1 when profiling (ev[0] before the first).
+struct Rec {
+  cudaEvent_t const *ev;
+  cudaStream_t s;
+  int i = 0;
+  cudaError_t operator()() { return ev ? cudaEventRecord(ev[i++], s) : cudaSuccess; }
+};
+
+// The decode/verify path: router -> select -> lists -> gate|up -> down -> combine.
+moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const moe_bf16 *x,
+                                int T, moe_bf16 *out, int32_t *ids_out, float *weights_out,
+                                float *logits_out, float *gate_logit_out, void *ws,
+                                const Layout &L, cudaStream_t s,
+                                cudaEvent_t const *events = nullptr) {
+  const int H = d->hidden, I = d->expert_inter, Is = d->shared_inter;
+  Rec rec{events, s};
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  float *logits = logits_out ? logits_out : at<float>(ws, L.logits);
+  float *glog = gate_logit_out ? gate_logit_out : at<float>(ws, L.gate_logit);
+  int32_t *ids = ids_out ? ids_out : at<int32_t>(ws, L.ids);
+  float *wts = weights_out ? weights_out : at<float>(ws, L.weights);
+  float *sg = at<float>(ws, L.sgate);
+  const moe_bf16 *wg = Is > 0 ? w->w_shared_gate : nullptr;
+  MOE_TRY(rec());
+  MOE_TRY(launch_router_gemv(x, T, H, w->w_router, wg, logits, wg ? glog : nullptr, s));
+  MOE_TRY(rec());
+  MOE_TRY(launch_select(logits, T, kE, wg ? glog : nullptr, ids, wts, wg ? sg : nullptr, status, s));
+  MOE_TRY(rec());
+  const Lists lists = lists_in(ws, L);
+  MOE_TRY(launch_lists(ids, T, lists, status, s));
+  MOE_TRY(rec());
+  moe_bf16 *hr = at<moe_bf16>(ws, L.h_routed);
+  moe_bf16 *hs = at<moe_bf16>(ws, L.h_shared);
+  float *y = at<float>(ws, L.y);
+  MOE_TRY(launch_gateup_simt(x, T, H, I, Is, *w, lists, hr, hs, s));
+  MOE_TRY(rec());
+  MOE_TRY(launch_down_simt(T, H, I, Is, *w, lists, hr, hs, y, s));
+  MOE_TRY(rec());
+  MOE_TRY(launch_combine(T, H, y, wts, wg ? sg : nullptr, out, s));
+  MOE_TRY(rec());
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null, misaligned or negative)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA launch or copy failed";
+  }
+  return "unknown status";
+}
+
+size_t moe_workspace_bytes(const moe_dims *dims, int T_max) {
+  if (check_dims(dims) != MOE_OK || T_max < 0 || T_max > kMaxT) return 0;
+  return layout(dims, T_max < 1 ? 1 : T_max).total;
+}
+
+moe_status moe_router_logits(const moe_dims *dims, const moe_weights *w, const moe_bf16 *x,
+                             int T, float *logits, float *shared_gate_logit, void *stream) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_weights(dims, w, true, false)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(x) || !ptr_ok(logits) || !opt_ok(shared_gate_logit)) return MOE_ERR_INVALID_ARG;
+  const moe_bf16 *wg = dims->shared_inter > 0 ? w->w_shared_gate : nullptr;
+  return cuda_status(launch_router_gemv(x, T, dims->hidden, w->w_router, wg,
+                                        logits, wg ? shared_gate_logit : nullptr,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_select_top8(const float *logits, int T, int ld, int E,
+                           const float *shared_gate_logit, int32_t *ids, float *weights,
+                           float *shared_gate, void *workspace, size_t ws_bytes, void *stream) {
+  if (T < 0 || ld < E) return MOE_ERR_INVALID_ARG;
+  if (E != kE || T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(logits) || ld % 4 || !ptr_ok(ids) || !ptr_ok(weights) ||
+      !opt_ok(shared_gate_logit) || !opt_ok(shared_gate))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_select(logits, T, ld, shared_gate_logit, ids, weights,
+                                   shared_gate_logit ? shared_gate : nullptr,
+                                   static_cast<uint32_t *>(workspace),
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_build_expert_lists(const int32_t *ids, int T, int E, int32_t *counts,
+                                  int32_t *offsets, int32_t *perm, void *workspace,
+                                  size_t ws_bytes, void *stream) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (E != kE || T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  // status word + the active list
+  if (ws_bytes < 256 + up256(4 * (kE + 1))) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(ids) || !ptr_ok(counts) || !ptr_ok(offsets) || !ptr_ok(perm))
+    return MOE_ERR_INVALID_ARG;
+  Lists L{counts, offsets, perm, nullptr, at<int32_t>(workspace, 256)};
+  return cuda_status(launch_lists(ids, T, L, static_cast<uint32_t *>(workspace),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_swiglu_w8(const moe_dims *dims, const moe_weights *w, const moe_bf16 *x,
+                                int T, const int32_t *ids, float *y, void *workspace,
+                                size_t ws_bytes, void *stream) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_weights(dims, w, false, true)) != MOE_OK) return st;
+  Layout L;
+  if ((st = check_ws(dims, T, workspace, ws_bytes, L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(x) || !ptr_ok(ids) || !ptr_ok(y)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int H = dims->hidden, I = dims->expert_inter, Is = dims->shared_inter;
+  uint32_t *status = at<uint32_t>(workspace, L.status);
+  const Lists lists = lists_in(workspace, L);
+  MOE_TRY(launch_lists(ids, T, lists, status, s));
+  moe_bf16 *hr = at<moe_bf16>(workspace, L.h_routed);
+  moe_bf16 *hs = at<moe_bf16>(workspace, L.h_shared);
+  if (Is == 0) {
+    // slot K is defined as zeros when there is no shared expert
+    MOE_TRY(cudaMemset2DAsync(y + static_cast<size_t>(kK) * H, sizeof(float) * (kK + 1) * H, 0,
+                              sizeof(float) * H, T, s));
+  }
+  MOE_TRY(launch_gateup_simt(x, T, H, I, Is, *w, lists, hr, hs, s));
+  MOE_TRY(launch_down_simt(T, H, I, Is, *w, lists, hr, hs, y, s));
+  return MOE_OK;
+}
+
+moe_status moe_combine(const moe_dims *dims, int T, const float *y, const float *weights,
+                       const float *shared_gate, moe_bf16 *out, void *stream) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(y) || !ptr_ok(weights) || !opt_ok(shared_gate) || !ptr_ok(out))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(T, dims->hidden, y, weights, shared_gate, out,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_block_forward(const moe_dims *dims, const moe_weights *w, const moe_bf16 *x,
+                             int T, moe_bf16 *out, int32_t *ids_out, float *weights_out,
+                             float *logits_out, float *gate_logit_out, void *workspace,
+                             size_t ws_bytes, void *stream) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_weights(dims, w, true, true)) != MOE_OK) return st;
+  Layout L;
+  if ((st = check_ws(dims, T, workspace, ws_bytes, L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(x) || !ptr_ok(out) || !opt_ok(ids_out) || !opt_ok(weights_out) ||
+      !opt_ok(logits_out) || !opt_ok(gate_logit_out))
+    return MOE_ERR_INVALID_ARG;
+  return block_forward_device(dims, w, x, T, out, ids_out, weights_out, logits_out,
+                              gate_logit_out, workspace, L, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_block_forward_host(const moe_dims *dims, const moe_weights *w,
+                                  const moe_bf16 *x_host, int T, moe_bf16 *out_host,
+                                  void *workspace, size_t ws_bytes, void *stream) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_weights(dims, w, true, true)) != MOE_OK) return st;
+  Layout L;
+  if ((st = check_ws(dims, T, workspace, ws_bytes, L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = sizeof(moe_bf16) * static_cast<size_t>(T) * dims->hidden;
+  moe_bf16 *xd = at<moe_bf16>(workspace, L.xstage);
+  moe_bf16 *od = at<moe_bf16>(workspace, L.ostage);
+  MOE_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+  st = block_forward_device(dims, w, xd, T, od, nullptr, nullptr, nullptr, nullptr, workspace,
+                            L, s);
+  if (st != MOE_OK) return st;
+  MOE_TRY(cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, s));
+  MOE_TRY(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+moe_status moe_block_forward_profiled(const moe_dims *dims, const moe_weights *w,
+                                      const moe_bf16 *x, int T, moe_bf16 *out, void *workspace,
+                                      size_t ws_bytes, void *const *events, int n_events,
+                                      void *stream) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_weights(dims, w, true, true)) != MOE_OK) return st;
+  Layout L;
+  if ((st = check_ws(dims, T, workspace, ws_bytes, L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(x) || !ptr_ok(out) || !events || n_events < 1 + kStages)
+    return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 1 + kStages; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return block_forward_device(dims, w, x, T, out, nullptr, nullptr, nullptr, nullptr, workspace,
+                              L, static_cast<cudaStream_t>(stream),
+                              reinterpret_cast<cudaEvent_t const *>(events));
+}
+
+int moe_block_kernel_count(const moe_dims *dims, int T) {
+  if (check_dims(dims) != MOE_OK || T < 1 || T > kMaxT) return 0;
+  return kStages;
+}
+
+const char *moe_block_kernel_name(const moe_dims *dims, int T, int i) {
+  const int n = moe_block_kernel_count(dims, T);
+  return (i >= 0 && i < n) ? kStageNames[i] : nullptr;
+}
+
+moe_status moe_read_status(const void *workspace, void *stream, uint32_t *bits) {
+  if (!workspace || !aligned(workspace, 256) || !bits) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_TRY(cudaMemcpyAsync(bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+  MOE_TRY(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+moe_status moe_clear_status(void *workspace, void *stream) {
+  if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// kernels.h -- host-side launchers of the sm_103a kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+// Token -> expert lists as the expert kernels consume them.
+struct Lists {
+  int32_t *counts;   // [E]
+  int32_t *offsets;  // [E+1]
+  int32_t *perm;     // [T*K] entries t*K+j sorted by (e, t, j)
+  int32_t *slot_of;  // [T*K] inverse of perm (position of entry t*K+j), or -1
+  int32_t *active;   // [1+E]: active[0] = number of active experts, then ids
+};
+
+// A1: router GEMV for any T (SIMT, fp32 accumulate).
+cudaError_t launch_router_gemv(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
+                               const moe_bf16 *w_gate, float *logits, float *gate_logit,
+                               cudaStream_t s);
+
+// A2: one warp per token.
+cudaError_t launch_select(const float *logits, int T, int ld, const float *gate_logit,
+                          int32_t *ids, float *weights, float *sgate, uint32_t *status,
+                          cudaStream_t s);
+
+// A3: deterministic counting sort of the T*K entries (single CTA).
+cudaError_t launch_lists(const int32_t *ids, int T, Lists L, uint32_t *status, cudaStream_t s);
+
+// A4/A6: gate|up + SwiGLU, weight-streaming SIMT kernel.  h_routed [T*K][I]
+// in list order, h_shared [T][Is].
+cudaError_t launch_gateup_simt(const moe_bf16 *x, int T, int H, int I, int Is,
+                               const moe_weights &w, Lists L, moe_bf16 *h_routed,
+                               moe_bf16 *h_shared, cudaStream_t s);
+
+// A5/A6: down projection into per-slot rows y [T][K+1][H] (fp32).
+cudaError_t launch_down_simt(int T, int H, int I, int Is, const moe_weights &w, Lists L,
+                             const moe_bf16 *h_routed, const moe_bf16 *h_shared, float *y,
+                             cudaStream_t s);
+
+// A7: out[t] = bf16(sum_j w[t][j] y[t][j] + sg[t] y[t][K]).
+cudaError_t launch_combine(int T, int H, const float *y, const float *weights,
+                           const float *sgate, moe_bf16 *out, cudaStream_t s);
+
+}  // namespace moe

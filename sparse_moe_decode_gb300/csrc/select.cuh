@@ -1,0 +1,113 @@
+// select.cuh -- warp-per-token top-8 selection (A2).
+//
+// Method (ninfer-windows PR #8, "...in place of eight dependent rounds"):
+// each lane holds 8 candidates sorted under the selector's total order; five
+// xor exchanges merge runs pairwise, each exchange being 8 independent
+// shuffles followed by three compare-exchange stages over static indices.
+// The tail is a softmax over the 8 selected logits and a sigmoid of the
+// shared-expert gate logit.
+//
+// GB300 form: the (value, id) pair is one 64-bit key whose unsigned order is
+// the selector's total order (value first, then lower id), so each
+// compare-exchange is a 64-bit max/min.  -0.0 is mapped to +0.0 before the
+// key is built, so the two zeros tie and the lower id wins, as IEEE ==
+// prescribes.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ uint64_t rank_key(float v, int id) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;                          // -0 -> +0
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);      // order-preserving
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFF - id);
+}
+
+__device__ __forceinline__ int key_id(uint64_t k) {
+  return 0xFFFF - static_cast<int>(k & 0xFFFFu);
+}
+
+__device__ __forceinline__ float key_value(uint64_t k) {
+  uint32_t u = static_cast<uint32_t>(k >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+// compare-exchange so that a keeps the better (larger) key
+__device__ __forceinline__ void cx(uint64_t &a, uint64_t &b) {
+  const uint64_t hi = a > b ? a : b;
+  const uint64_t lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// 19-comparator sorting network, descending.
+__device__ __forceinline__ void sort8(uint64_t (&k)[8]) {
+  cx(k[0], k[2]); cx(k[1], k[3]); cx(k[4], k[6]); cx(k[5], k[7]);
+  cx(k[0], k[4]); cx(k[1], k[5]); cx(k[2], k[6]); cx(k[3], k[7]);
+  cx(k[0], k[1]); cx(k[2], k[3]); cx(k[4], k[5]); cx(k[6], k[7]);
+  cx(k[2], k[4]); cx(k[3], k[5]);
+  cx(k[1], k[4]); cx(k[3], k[6]);
+  cx(k[1], k[2]); cx(k[3], k[4]); cx(k[5], k[6]);
+}
+
+// Keep the best 8 of the union of this lane's sorted run and its partner's
+// (lane ^ mask): elementwise best of A[i] and B[7-i] is bitonic and holds
+// the 8 best; three half-cleaner stages sort it.
+__device__ __forceinline__ void merge_level(uint64_t (&k)[8], int mask) {
+  uint64_t p[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(0xFFFFFFFFu, k[i], mask);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) k[i] = k[i] > p[7 - i] ? k[i] : p[7 - i];
+  cx(k[0], k[4]); cx(k[1], k[5]); cx(k[2], k[6]); cx(k[3], k[7]);
+  cx(k[0], k[2]); cx(k[1], k[3]); cx(k[4], k[6]); cx(k[5], k[7]);
+  cx(k[0], k[1]); cx(k[2], k[3]); cx(k[4], k[5]); cx(k[6], k[7]);
+}
+
+// Select for one token with the whole warp.  `row` holds 256 fp32 logits
+// (16-byte aligned).  On return every lane holds the token's ids (rank
+// order) and softmax weights; returns false for a non-finite row (ids -1,
+// weights 0).
+__device__ __forceinline__ bool select_top8_warp(const float *row, int lane, int (&ids)[8],
+                                                 float (&w)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(row)[2 * lane];
+  const float4 b = reinterpret_cast<const float4 *>(row)[2 * lane + 1];
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  bool finite = true;
+  uint64_t k[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    finite &= isfinite(v[i]);
+    k[i] = rank_key(v[i], 8 * lane + i);
+  }
+  if (!__all_sync(0xFFFFFFFFu, finite)) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { ids[i] = -1; w[i] = 0.0f; }
+    return false;
+  }
+  sort8(k);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) merge_level(k, m);
+  // softmax over the 8 selected logits, max-subtracted (rank 0 is the max)
+  const float z0 = key_value(k[0]);
+  float e[8], s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    e[i] = expf(key_value(k[i]) - z0);
+    s += e[i];
+  }
+  const float inv = 1.0f / s;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ids[i] = key_id(k[i]);
+    w[i] = e[i] * inv;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
+
+}  // namespace moe

@@ -1,0 +1,112 @@
+"""The C-ABI library loads and exports what include/moe_gb300.h declares;
+host-side argument checks reject bad calls before any device work (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__ as g
+    g.build()
+    import sparse_moe_decode_gb300 as m
+    return m
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_router_logits", "moe_select_top8", "moe_expert_swiglu_w8", "moe_combine",
+              "moe_block_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    L = moe.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert set(declared_functions()) == set(moe.EXPORTS)
+    assert L.moe_abi_version() == 1
+
+
+def test_library_is_built_for_sm_103a(moe):
+    from sparse_moe_decode_gb300 import build
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+    assert os.path.exists(moe.LIB_PATH)
+
+
+def test_workspace_bytes_and_unsupported_dims(moe):
+    d = moe.Dims.make(2048, 512, 512)
+    small, big = moe.moe_workspace_bytes(d, 1), moe.moe_workspace_bytes(d, 2048)
+    assert 0 < small < big
+    assert moe.moe_workspace_bytes(d, 65537) == 0
+    for bad in (moe.Dims.make(2048, 512, 512, num_experts=128),
+                moe.Dims.make(2048, 512, 512, top_k=4),
+                moe.Dims.make(2000, 512, 512),
+                moe.Dims.make(2048, 500, 512),
+                moe.Dims.make(2048, 512, 100),
+                moe.Dims.make(2048, 512, 512, group=64)):
+        assert moe.moe_workspace_bytes(bad, 4) == 0
+
+
+def test_host_checks_reject_before_touching_the_device(moe):
+    L = moe.lib()
+    d = moe.Dims.make(512, 128, 128)
+    w = moe.Weights()
+    # null weights
+    st = L.moe_block_forward(ctypes.byref(d), ctypes.byref(w), 4096, 4, 4096, None, None,
+                             None, None, 256, 1 << 30, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    fake = 1 << 20  # aligned fake addresses are never dereferenced on these paths
+    w = moe.Weights(*([fake] * 10))
+    st = L.moe_block_forward(ctypes.byref(d), ctypes.byref(w), fake, 4, fake, None, None, None,
+                             None, fake, 16, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    st = L.moe_block_forward(ctypes.byref(d), ctypes.byref(w), fake, -1, fake, None, None, None,
+                             None, fake, 1 << 30, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = L.moe_block_forward(ctypes.byref(d), ctypes.byref(w), fake, 70000, fake, None, None,
+                             None, None, fake, 1 << 40, None)
+    assert st == moe.MOE_ERR_UNSUPPORTED
+    st = L.moe_block_forward(ctypes.byref(d), ctypes.byref(w), fake + 8, 4, fake, None, None,
+                             None, None, fake, 1 << 30, None)
+    assert st == moe.MOE_ERR_INVALID_ARG  # misaligned x
+    st = L.moe_block_forward(ctypes.byref(d), ctypes.byref(w), fake, 4, fake, None, None, None,
+                             None, fake + 16, 1 << 30, None)
+    assert st == moe.MOE_ERR_INVALID_ARG  # workspace not 256-aligned
+    # T == 0 is a no-op
+    st = L.moe_block_forward(ctypes.byref(d), ctypes.byref(w), None, 0, None, None, None, None,
+                             None, fake, 1 << 30, None)
+    assert st == moe.MOE_OK
+    # selector: E must be 256, ld >= E
+    assert L.moe_select_top8(fake, 4, 256, 128, None, fake, fake, None, fake, 256,
+                             None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_select_top8(fake, 4, 100, 256, None, fake, fake, None, fake, 256,
+                             None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_select_top8(fake, 4, 256, 256, None, fake, fake, None, fake, 16,
+                             None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_combine(ctypes.byref(d), 4, None, fake, None, fake,
+                         None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_status_string(moe.MOE_ERR_WORKSPACE) == b"workspace too small"
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_moe_decode_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in src and "moe_oracle" not in src, fn

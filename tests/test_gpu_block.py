@@ -1,0 +1,153 @@
+"""moe_block_forward (A1..A7) on the GPU against the oracle.
+
+Routing: the oracle selects on the GPU's own fp32 logits, so ids and order
+must match bit for bit; against the oracle's own fp64-derived logits, a token
+may differ only where the oracle's ranking has a near tie.  Output: the bf16
+tolerance of the block.  Large T is checked on a seeded sample of tokens.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from util import assert_out_close, bits, gpu_env, ncpu, near_tie, to_dev, workload, workload_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    return gpu_env()
+
+
+def forward(moe, dev, name, x, T_max=None):
+    import torch
+    dims, w = workload(name)
+    wd = workload_dev(name, dev)
+    T = x.shape[0]
+    blk = moe.MoEBlock(dims.H, dims.I, dims.Is, wd, T_max=T_max or T, device=dev)
+    o = {
+        "out": torch.empty((T, dims.H), dtype=torch.int16, device=dev),
+        "ids": torch.empty((T, 8), dtype=torch.int32, device=dev),
+        "weights": torch.empty((T, 8), dtype=torch.float32, device=dev),
+        "logits": torch.empty((T, 256), dtype=torch.float32, device=dev),
+        "gate": torch.empty((T,), dtype=torch.float32, device=dev),
+    }
+    blk.forward(to_dev(x, dev), out=o["out"], ids=o["ids"], weights=o["weights"],
+                logits=o["logits"], gate_logit=o["gate"])
+    torch.cuda.synchronize()
+    assert blk.status() == 0
+    res = {k: (bits(v) if k == "out" else v.cpu().numpy()) for k, v in o.items()}
+    return dims, w, res, blk
+
+
+def sample_tokens(T, n, seed):
+    if T <= n:
+        return None
+    s = np.sort(W.permutation(T, W.stream_key(seed, "misc"))[: n - 2])
+    return np.unique(np.concatenate([[0, T - 1], s])).astype(np.int32)
+
+
+def check_block(moe, dev, name, x, n_sample=64, seed=0):
+    dims, w, g, _ = forward(moe, dev, name, x)
+    T = x.shape[0]
+    toks = sample_tokens(T, n_sample, seed)
+    rows = np.arange(T) if toks is None else toks
+    ref = oracle.block_forward(dims.as_dict(), w, x, tokens=toks, route_logits=g["logits"],
+                               route_gate=g["gate"], nthreads=ncpu(),
+                               want=("out", "out_f64"))
+    assert np.array_equal(g["ids"][rows], ref["ids"][rows])
+    assert np.abs(g["weights"][rows] - ref["weights"][rows]).max() <= 1e-6
+    assert_out_close(g["out"][rows], ref["out"][rows], name)
+    # routing on the oracle's own logits: any difference needs a near tie there
+    own_ids, _, _, _ = oracle.select_topk(ref["logits"][rows], K=8)
+    for i, t in enumerate(rows):
+        if not np.array_equal(own_ids[i], g["ids"][t]):
+            assert near_tie(ref["logits"][t]), "token %d routes differently without a tie" % t
+    return dims, w, g
+
+
+def test_block_pr1(env):
+    moe, dev = env
+    dims, w = workload("pr1")
+    x, _ = W.make_x(dims, 4, 0)
+    check_block(moe, dev, "pr1", x)
+
+
+def test_block_pr1_ragged_T(env):
+    moe, dev = env
+    dims, w = workload("pr1")
+    for T in (1, 3, 9, 33, 65):
+        x, _ = W.make_x(dims, T, 7 + T)
+        check_block(moe, dev, "pr1", x)
+
+
+def test_block_decode_T1(env):
+    moe, dev = env
+    dims, w, x, _ = W.workload_inputs("decode")
+    check_block(moe, dev, "decode", x)
+
+
+def test_block_verify_T32_skewed(env):
+    moe, dev = env
+    dims, w, x, info = W.workload_inputs("verify")
+    _, _, g = check_block(moe, dev, "verify", x)
+    assert (g["ids"][info["skewed"], 0] == info["e_star"]).all()
+    assert len(np.unique(g["ids"])) > 100  # many distinct experts are active
+
+
+@pytest.mark.parametrize("T", [2, 19, 20, 46, 47, 768, 4097])
+def test_block_decode_dims_T_sweep(env, T):
+    moe, dev = env
+    dims, _ = workload("decode")
+    x, _ = W.make_x(dims, T, 100 + T)
+    check_block(moe, dev, "decode", x, n_sample=48, seed=T)
+
+
+def test_block_prefill_T2048_sampled(env):
+    moe, dev = env
+    dims, w, x, _ = W.workload_inputs("prefill")
+    _, _, g = check_block(moe, dev, "prefill", x, n_sample=48, seed=3)
+    counts = np.bincount(g["ids"].ravel(), minlength=256)
+    assert counts.min() > 0  # uniform routing touches every expert
+
+
+def test_block_batch_width_invariance_decode_route(env):
+    """A token's output bits do not depend on the batch it rides in."""
+    moe, dev = env
+    dims, _ = workload("decode")
+    x, _ = W.make_x(dims, 32, 77)
+    _, _, full, _ = forward(moe, dev, "decode", x)
+    for t in (0, 13, 31):
+        _, _, one, _ = forward(moe, dev, "decode", x[t:t + 1])
+        assert np.array_equal(one["out"][0], full["out"][t])
+        assert np.array_equal(one["ids"][0], full["ids"][t])
+
+
+def test_block_host_entry_matches_device_entry(env):
+    import torch
+    moe, dev = env
+    dims, _ = workload("pr1")
+    x, _ = W.make_x(dims, 6, 5)
+    _, _, g, blk = forward(moe, dev, "pr1", x)
+    out = np.zeros((6, dims.H), np.uint16)
+    moe.moe_block_forward_host(blk.dims, blk.w, np.ascontiguousarray(x), 6, out, blk.workspace,
+                               blk.ws_bytes)
+    assert np.array_equal(out, g["out"])
+
+
+def test_block_nonfinite_input_sets_status_and_keeps_shared(env):
+    import torch
+    moe, dev = env
+    dims, w = workload("pr1")
+    x, _ = W.make_x(dims, 3, 9)
+    x[1, 5] = 0x7FC0  # NaN activation -> NaN logits for token 1
+    wd = workload_dev("pr1", dev)
+    blk = moe.MoEBlock(dims.H, dims.I, dims.Is, wd, T_max=3, device=dev)
+    ids = torch.empty((3, 8), dtype=torch.int32, device=dev)
+    out = torch.empty((3, dims.H), dtype=torch.int16, device=dev)
+    blk.forward(to_dev(x, dev), out=out, ids=ids)
+    assert blk.status() & moe.DEV_NONFINITE
+    assert (ids[1].cpu().numpy() == -1).all() and (ids[0].cpu().numpy() >= 0).all()
+    blk.clear_status()
+    assert blk.status() == 0

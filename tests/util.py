@@ -1,0 +1,115 @@
+"""Shared helpers of the test suite: device upload, bf16 views, tolerances.
+
+The tolerances are the block's contract:
+  * routing: ids and their order bit-exact when both sides select on the same
+    fp32 logits;
+  * softmax weights: |gpu - oracle| <= 1e-6;
+  * logits: |gpu - oracle| <= 1e-5 * |x|_2 * |w_e|_2 (fp32 sums of exact
+    products against an fp64 sum);
+  * bf16 block output: max|gpu - bf16(ref)| <= 2e-2 * max|ref| and
+    sum|gpu - bf16(ref)| / sum|bf16(ref)| <= 1e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import workloads as W
+
+OUT_MAX_REL = 2e-2
+OUT_MEAN_REL = 1e-3
+WEIGHT_ABS = 1e-6
+LOGIT_REL = 1e-5
+
+
+def to_dev(a, dev):
+    import torch
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def weights_to_dev(w: dict, dev) -> dict:
+    return {k: to_dev(v, dev) for k, v in w.items()}
+
+
+def bits(t) -> np.ndarray:
+    """uint16 bit patterns of a device int16/bf16 tensor."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        t = t.view(torch.int16)
+    return t.cpu().numpy().view(np.uint16)
+
+
+def bf16_f64(b) -> np.ndarray:
+    return W.bf16_bits_to_f32(b).astype(np.float64)
+
+
+def out_errors(gpu_bits, ref_bits):
+    got, want = bf16_f64(gpu_bits), bf16_f64(ref_bits)
+    err = np.abs(got - want)
+    denom = np.abs(want).sum()
+    return err.max(), np.abs(want).max(), err.sum() / max(denom, 1e-300)
+
+
+def assert_out_close(gpu_bits, ref_bits, what=""):
+    emax, refmax, mean_rel = out_errors(gpu_bits, ref_bits)
+    assert emax <= OUT_MAX_REL * refmax, "%s max|diff| %.4g > %.3g * %.4g" % (
+        what, emax, OUT_MAX_REL, refmax)
+    assert mean_rel <= OUT_MEAN_REL, "%s mean relative error %.4g > %.3g" % (
+        what, mean_rel, OUT_MEAN_REL)
+    return emax, mean_rel
+
+
+def assert_f32_close(got, want, what=""):
+    """Per-slot fp32 tensors against fp64: same two bars as the block output."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    err = np.abs(got - want)
+    assert err.max() <= OUT_MAX_REL * np.abs(want).max(), what
+    assert err.sum() / max(np.abs(want).sum(), 1e-300) <= OUT_MEAN_REL, what
+
+
+def near_tie(logits_row, k=8, rel=1e-5):
+    """True when the oracle's own ranking has a near tie that a 1e-5 relative
+    logit difference could reorder (around rank k or inside the top k)."""
+    v = np.sort(np.asarray(logits_row, np.float64))[::-1]
+    scale = max(np.abs(v).max(), 1e-30)
+    gaps = np.diff(v[: k + 1])
+    return bool(np.any(np.abs(gaps) <= rel * scale))
+
+
+# ------------------------------------------------------ cached workloads
+
+_CACHE = {}
+
+
+def workload(name: str):
+    """(dims, host weights) of a named workload, generated once per process."""
+    if name not in _CACHE:
+        wl = W.WORKLOADS[name]
+        _CACHE[name] = (wl.dims, W.make_weights(wl.dims, wl.seed))
+    return _CACHE[name]
+
+
+def workload_dev(name: str, dev):
+    key = (name, str(dev))
+    if key not in _CACHE:
+        dims, w = workload(name)
+        _CACHE[key] = weights_to_dev(w, dev)
+    return _CACHE[key]
+
+
+def gpu_env():
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    import sparse_moe_decode_gb300 as moe
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return moe, torch.device("cuda:0")
+
+
+def ncpu() -> int:
+    import os
+    return max(1, min(32, os.cpu_count() or 1))
