@@ -194,7 +194,7 @@ class Bench:
                                                 self.out, self.ws, self.ws_bytes, events,
                                                 self.stream)
 
-    def graphs(self, profiled_steps=0):
+    def graphs(self):
         torch = self.torch
         gs = []
         with torch.cuda.stream(self.stream):
@@ -204,52 +204,49 @@ class Bench:
                     self.step(r)
                 gs.append(g)
         self.plain = gs
-        self.prof = []
-        self.prof_events = []
-        with torch.cuda.stream(self.stream):
-            for i in range(profiled_steps):
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(self.nk + 1)]
-                for e in ev:  # creates the underlying cudaEvent_t before capture
-                    e.record(self.stream)
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=self.stream):
-                    self.step(i % self.R, ev)
-                self.prof.append(g)
-                self.prof_events.append(ev)
 
     def run(self, steps, warmup, barrier, clocks_index):
         torch = self.torch
-        self.graphs(profiled_steps=steps)
+        self.graphs()
         s = self.stream
-        for i in range(warmup):
-            self.plain[i % self.R].replay()
+        with torch.cuda.stream(s):  # replays launch on the current stream
+            for i in range(warmup):
+                self.plain[i % self.R].replay()
         torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(self.nk + 1)]
+                  for _ in range(steps)]
         with Clocks(clocks_index) as clk:
             torch.cuda.synchronize()
             barrier()
             t_wall = time.perf_counter()
-            e0.record(s)
-            for i in range(steps):
-                self.plain[i % self.R].replay()
-            e1.record(s)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                for i in range(steps):
+                    self.plain[i % self.R].replay()
+                e1.record(s)
             torch.cuda.synchronize()
             t_wall = time.perf_counter() - t_wall
             barrier()
             ms = e0.elapsed_time(e1) / steps
-            # profiled pass: same steps, events between kernels
-            for i in range(min(warmup, len(self.prof))):
-                self.prof[i].replay()
-            torch.cuda.synchronize()
-            for g in self.prof:
-                g.replay()
+            # profiled pass: the same K steps through the profiled entry point,
+            # events between kernels; a bounded sleep kernel first lets the host
+            # enqueue every step so kernels run back to back on the device
+            with torch.cuda.stream(s):
+                for ev in events:
+                    for e in ev:
+                        e.record(s)  # creates the event handles
+                torch.cuda.synchronize()
+                torch.cuda._sleep(50_000_000)
+                for i in range(steps):
+                    self.step(i % self.R, events[i])
             torch.cuda.synchronize()
         per_kernel = np.zeros(self.nk)
-        for ev in self.prof_events:
+        for ev in events:
             for k in range(self.nk):
                 per_kernel[k] += ev[k].elapsed_time(ev[k + 1])
-        per_kernel /= max(1, len(self.prof_events))
+        per_kernel /= max(1, steps)
         assert self.moe.moe_read_status(self.ws) == 0
         return ms, t_wall, per_kernel, clk.summary()
 

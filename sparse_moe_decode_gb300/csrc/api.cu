@@ -54,8 +54,13 @@ size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 struct Layout {
   size_t status, logits, gate_logit, ids, weights, sgate;
   size_t counts, offsets, active, perm, slot_of;
-  size_t h_routed, h_shared, y, xstage, ostage, total;
+  size_t h_routed, h_shared, y, xstage, ostage;
+  size_t xs, acc, items, counters, total;
 };
+
+// Token count from which moe_block_forward runs the tcgen05 grouped GEMMs
+// instead of the weight-streaming GEMV kernels.
+constexpr int kTcMinT = 128;
 
 Layout layout(const moe_dims *d, int T) {
   Layout L{};
@@ -79,6 +84,13 @@ Layout layout(const moe_dims *d, int T) {
   L.y = take(4 * t * (kK + 1) * H);
   L.xstage = take(2 * t * H);
   L.ostage = take(2 * t * H);
+  if (T >= kTcMinT) {
+    L.xs = take(2 * t * kK * H);
+    L.acc = take(4 * t * H);
+    L.items = take(tc_items_bytes(T, static_cast<int>(I), static_cast<int>(Is),
+                                  static_cast<int>(H)));
+    L.counters = take(16);
+  }
   L.total = o;
   return L;
 }
@@ -108,17 +120,23 @@ moe_status check_ws(const moe_dims *d, int T, const void *ws, size_t ws_bytes, L
   return MOE_OK;
 }
 
-// Kernel sequence of moe_block_forward (decode/verify route).
+// Kernel sequences of moe_block_forward: decode/verify route (GEMV kernels)
+// and prefill route (tcgen05 grouped GEMMs).
 const char *const kStageNames[] = {"router_gemv", "select_top8", "expert_lists",
                                    "gateup_swiglu", "down", "combine"};
 constexpr int kStages = 6;
+const char *const kTcStageNames[] = {"router_tc", "router_gate_gemv", "select_top8",
+                                     "expert_lists", "build_items", "gather_rows", "zero_acc",
+                                     "gateup_swiglu_tc", "down_combine_tc", "acc_to_bf16"};
+constexpr int kTcStages = 10;
 
 // Records `ev[i]` after kernel i-1 when profiling (ev[0] before the first).
-struct Rec {
+struct Rec : StageRecorder {
   cudaEvent_t const *ev;
   cudaStream_t s;
   int i = 0;
-  cudaError_t operator()() { return ev ? cudaEventRecord(ev[i++], s) : cudaSuccess; }
+  Rec(cudaEvent_t const *e, cudaStream_t st) : ev(e), s(st) {}
+  cudaError_t operator()() override { return ev ? cudaEventRecord(ev[i++], s) : cudaSuccess; }
 };
 
 // The decode/verify path: router -> select -> lists -> gate|up -> down -> combine.
@@ -136,23 +154,43 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   float *wts = weights_out ? weights_out : at<float>(ws, L.weights);
   float *sg = at<float>(ws, L.sgate);
   const moe_bf16 *wg = Is > 0 ? w->w_shared_gate : nullptr;
-  MOE_TRY(rec());
-  MOE_TRY(launch_router_gemv(x, T, H, w->w_router, wg, logits, wg ? glog : nullptr, s));
-  MOE_TRY(rec());
-  MOE_TRY(launch_select(logits, T, kE, wg ? glog : nullptr, ids, wts, wg ? sg : nullptr, status, s));
-  MOE_TRY(rec());
   const Lists lists = lists_in(ws, L);
-  MOE_TRY(launch_lists(ids, T, lists, status, s));
-  MOE_TRY(rec());
   moe_bf16 *hr = at<moe_bf16>(ws, L.h_routed);
   moe_bf16 *hs = at<moe_bf16>(ws, L.h_shared);
-  float *y = at<float>(ws, L.y);
-  MOE_TRY(launch_gateup_simt(x, T, H, I, Is, *w, lists, hr, hs, s));
   MOE_TRY(rec());
-  MOE_TRY(launch_down_simt(T, H, I, Is, *w, lists, hr, hs, y, s));
+  if (T < kTcMinT) {
+    MOE_TRY(launch_router_gemv(x, T, H, w->w_router, wg, logits, wg ? glog : nullptr, s));
+    MOE_TRY(rec());
+    MOE_TRY(launch_select(logits, T, kE, wg ? glog : nullptr, ids, wts, wg ? sg : nullptr,
+                          status, s));
+    MOE_TRY(rec());
+    MOE_TRY(launch_lists(ids, T, lists, status, s));
+    MOE_TRY(rec());
+    float *y = at<float>(ws, L.y);
+    MOE_TRY(launch_gateup_simt(x, T, H, I, Is, *w, lists, hr, hs, s));
+    MOE_TRY(rec());
+    MOE_TRY(launch_down_simt(T, H, I, Is, *w, lists, hr, hs, y, s));
+    MOE_TRY(rec());
+    MOE_TRY(launch_combine(T, H, y, wts, wg ? sg : nullptr, out, s));
+    MOE_TRY(rec());
+    return MOE_OK;
+  }
+  int4 *items = at<int4>(ws, L.items);
+  int *counters = at<int>(ws, L.counters);
+  MOE_TRY(launch_router_tc(x, T, H, w->w_router, logits, status, s));
   MOE_TRY(rec());
-  MOE_TRY(launch_combine(T, H, y, wts, wg ? sg : nullptr, out, s));
+  if (wg) {
+    MOE_TRY(launch_router_gemv(x, T, H, w->w_router, wg, logits, glog, s, true));
+    MOE_TRY(rec());
+  }
+  MOE_TRY(launch_select(logits, T, kE, wg ? glog : nullptr, ids, wts, wg ? sg : nullptr,
+                        status, s));
   MOE_TRY(rec());
+  MOE_TRY(launch_lists(ids, T, lists, status, s));
+  MOE_TRY(rec());
+  MOE_TRY(launch_experts_tc(x, T, H, I, Is, *w, lists, lists.perm, wts, wg ? sg : nullptr,
+                            at<moe_bf16>(ws, L.xs), hr, hs, at<float>(ws, L.acc), out, items,
+                            counters, status, s, rec));
   return MOE_OK;
 }
 
@@ -191,9 +229,15 @@ moe_status moe_router_logits(const moe_dims *dims, const moe_weights *w, const m
   if (T == 0) return MOE_OK;
   if (!ptr_ok(x) || !ptr_ok(logits) || !opt_ok(shared_gate_logit)) return MOE_ERR_INVALID_ARG;
   const moe_bf16 *wg = dims->shared_inter > 0 ? w->w_shared_gate : nullptr;
-  return cuda_status(launch_router_gemv(x, T, dims->hidden, w->w_router, wg,
-                                        logits, wg ? shared_gate_logit : nullptr,
-                                        static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T < kTcMinT)
+    return cuda_status(launch_router_gemv(x, T, dims->hidden, w->w_router, wg, logits,
+                                          wg ? shared_gate_logit : nullptr, s));
+  MOE_TRY(launch_router_tc(x, T, dims->hidden, w->w_router, logits, nullptr, s));
+  if (wg && shared_gate_logit)
+    MOE_TRY(launch_router_gemv(x, T, dims->hidden, w->w_router, wg, logits, shared_gate_logit,
+                               s, true));
+  return MOE_OK;
 }
 
 moe_status moe_select_top8(const float *logits, int T, int ld, int E,
@@ -327,9 +371,9 @@ moe_status moe_block_forward_profiled(const moe_dims *dims, const moe_weights *w
   Layout L;
   if ((st = check_ws(dims, T, workspace, ws_bytes, L)) != MOE_OK) return st;
   if (T == 0) return MOE_OK;
-  if (!ptr_ok(x) || !ptr_ok(out) || !events || n_events < 1 + kStages)
-    return MOE_ERR_INVALID_ARG;
-  for (int i = 0; i < 1 + kStages; ++i)
+  const int nk = moe_block_kernel_count(dims, T);
+  if (!ptr_ok(x) || !ptr_ok(out) || !events || n_events < 1 + nk) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 1 + nk; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   return block_forward_device(dims, w, x, T, out, nullptr, nullptr, nullptr, nullptr, workspace,
                               L, static_cast<cudaStream_t>(stream),
@@ -338,12 +382,16 @@ moe_status moe_block_forward_profiled(const moe_dims *dims, const moe_weights *w
 
 int moe_block_kernel_count(const moe_dims *dims, int T) {
   if (check_dims(dims) != MOE_OK || T < 1 || T > kMaxT) return 0;
-  return kStages;
+  if (T < kTcMinT) return kStages;
+  return dims->shared_inter > 0 ? kTcStages : kTcStages - 1;
 }
 
 const char *moe_block_kernel_name(const moe_dims *dims, int T, int i) {
   const int n = moe_block_kernel_count(dims, T);
-  return (i >= 0 && i < n) ? kStageNames[i] : nullptr;
+  if (i < 0 || i >= n) return nullptr;
+  if (T < kTcMinT) return kStageNames[i];
+  if (dims->shared_inter == 0 && i >= 1) ++i;  // no gate-logit GEMV
+  return kTcStageNames[i];
 }
 
 moe_status moe_read_status(const void *workspace, void *stream, uint32_t *bits) {

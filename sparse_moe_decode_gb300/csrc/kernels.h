@@ -8,6 +8,11 @@
 
 namespace moe {
 
+// Records a profiling event after each kernel launch (no-op when not profiling).
+struct StageRecorder {
+  virtual cudaError_t operator()() = 0;
+};
+
 // Token -> expert lists as the expert kernels consume them.
 struct Lists {
   int32_t *counts;   // [E]
@@ -20,7 +25,7 @@ struct Lists {
 // A1: router GEMV for any T (SIMT, fp32 accumulate).
 cudaError_t launch_router_gemv(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
                                const moe_bf16 *w_gate, float *logits, float *gate_logit,
-                               cudaStream_t s);
+                               cudaStream_t s, bool gate_only = false);
 
 // A2: one warp per token.
 cudaError_t launch_select(const float *logits, int T, int ld, const float *gate_logit,
@@ -44,5 +49,25 @@ cudaError_t launch_down_simt(int T, int H, int I, int Is, const moe_weights &w, 
 // A7: out[t] = bf16(sum_j w[t][j] y[t][j] + sg[t] y[t][K]).
 cudaError_t launch_combine(int T, int H, const float *y, const float *weights,
                            const float *sgate, moe_bf16 *out, cudaStream_t s);
+
+// ---- prefill-size T: tcgen05 grouped GEMMs (tc_gemm.cu)
+
+// Bytes of the work-item lists for T tokens.
+size_t tc_items_bytes(int T, int I, int Is, int H);
+
+// A1 router logits [T][E] as a tcgen05 GEMM (the gate row is left to the
+// GEMV launcher with gate_only = true).  `status` may be NULL.
+cudaError_t launch_router_tc(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
+                             float *logits, uint32_t *status, cudaStream_t s);
+
+// A4..A7 for prefill-size T: gathers each expert's tokens (xs [T*K][H]),
+// runs gate|up + SwiGLU and down + weighted combine as grouped tcgen05 GEMMs
+// into out_acc [T][H] (fp32, zeroed here), then rounds out_acc to bf16.
+cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
+                              const moe_weights &w, const Lists &L, const int32_t *perm,
+                              const float *weights, const float *sgate, moe_bf16 *xs,
+                              moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
+                              moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
+                              cudaStream_t s, StageRecorder &rec);
 
 }  // namespace moe

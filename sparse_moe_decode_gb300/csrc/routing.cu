@@ -16,9 +16,9 @@ constexpr int kRouterTok = 8;
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_gemv_kernel(const moe_bf16 *__restrict__ x, int T, int H,
                    const moe_bf16 *__restrict__ w_router, const moe_bf16 *__restrict__ w_gate,
-                   float *__restrict__ logits, float *__restrict__ gate_logit) {
+                   float *__restrict__ logits, float *__restrict__ gate_logit, int row_begin) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r = blockIdx.x * kRouterWarps + warp;
+  const int r = row_begin + blockIdx.x * kRouterWarps + warp;
   const int rows = kE + (w_gate != nullptr ? 1 : 0);
   if (r >= rows) return;
   const moe_bf16 *wrow = r < kE ? w_router + static_cast<size_t>(r) * H : w_gate;
@@ -56,11 +56,14 @@ router_gemv_kernel(const moe_bf16 *__restrict__ x, int T, int H,
 
 cudaError_t launch_router_gemv(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
                                const moe_bf16 *w_gate, float *logits, float *gate_logit,
-                               cudaStream_t s) {
-  const int rows = kE + (w_gate && gate_logit ? 1 : 0);
+                               cudaStream_t s, bool gate_only) {
+  const int row_begin = gate_only ? kE : 0;
+  const int rows = kE + (w_gate && gate_logit ? 1 : 0) - row_begin;
+  if (rows <= 0) return cudaSuccess;
   dim3 grid((rows + kRouterWarps - 1) / kRouterWarps, (T + kRouterTok - 1) / kRouterTok);
   router_gemv_kernel<<<grid, kRouterWarps * 32, 0, s>>>(
-      x, T, H, w_router, (w_gate && gate_logit) ? w_gate : nullptr, logits, gate_logit);
+      x, T, H, w_router, (w_gate && gate_logit) ? w_gate : nullptr, logits, gate_logit,
+      row_begin);
   return cudaGetLastError();
 }
 

@@ -59,6 +59,11 @@ def check_block(moe, dev, name, x, n_sample=64, seed=0):
     assert np.array_equal(g["ids"][rows], ref["ids"][rows])
     assert np.abs(g["weights"][rows] - ref["weights"][rows]).max() <= 1e-6
     assert_out_close(g["out"][rows], ref["out"][rows], name)
+    # the GPU's logits against the oracle's fp64-derived fp32 logits
+    xn = np.linalg.norm(W.bf16_bits_to_f32(x[rows]).astype(np.float64), axis=1)
+    wn = np.linalg.norm(W.bf16_bits_to_f32(w["w_router"]).astype(np.float64), axis=1)
+    assert (np.abs(g["logits"][rows] - ref["logits"][rows]) <=
+            1e-5 * xn[:, None] * wn[None, :]).all()
     # routing on the oracle's own logits: any difference needs a near tie there
     own_ids, _, _, _ = oracle.select_topk(ref["logits"][rows], K=8)
     for i, t in enumerate(rows):

@@ -14,8 +14,8 @@ def env():
     return gpu_env()
 
 
-@pytest.mark.parametrize("name,T", [("pr1", 4), ("pr1", 37), ("decode", 1), ("decode", 32),
-                                    ("decode", 129)])
+@pytest.mark.parametrize("name,T", [("pr1", 4), ("pr1", 37), ("pr1", 200), ("decode", 1),
+                                    ("decode", 32), ("decode", 129), ("decode", 2048)])
 def test_router_logits(env, name, T):
     import torch
     moe, dev = env
