@@ -184,6 +184,27 @@ moe_status moe_block_forward_profiled(const moe_dims *dims, const moe_weights *w
 int moe_block_kernel_count(const moe_dims *dims, int T);
 const char *moe_block_kernel_name(const moe_dims *dims, int T, int i);
 
+/* moe_block_forward for callers that cannot allocate device memory (a
+ * plugin in a runtime that owns all device memory, a process with a fixed
+ * device-memory budget, a latency-critical path that cannot take
+ * cudaMalloc's implicit synchronisation).  There is no counterpart on the
+ * pages: this is a packaging variant of the same block.  The caller passes
+ * only inputs and outputs; the scratch is a 4 MiB array that the library
+ * holds on every GPU that loads it, until the process exits.
+ *   - A (dims, T) whose moe_workspace_bytes exceeds 4 MiB is rejected with
+ *     MOE_ERR_WORKSPACE (at H = 2048, I = Is = 512 that allows T <= 44).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents:
+ *     calls that overlap on the GPU (other streams, other threads) race.
+ *   - The device status word lives in the array and is cleared at the start
+ *     of each call; it is not reported. */
+moe_status moe_block_forward_noalloc(const moe_dims *dims, const moe_weights *w,
+                                     const moe_bf16 *x, int T, moe_bf16 *out,
+                                     void *stream);
+
 /* Copy the device status word to *bits (synchronises the stream). */
 moe_status moe_read_status(const void *workspace, void *stream, uint32_t *bits);
 /* Zero the device status word (asynchronous). */

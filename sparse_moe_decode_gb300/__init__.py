@@ -27,6 +27,7 @@ __all__ = [
     "moe_workspace_bytes", "moe_read_status", "moe_clear_status", "MoEBlock",
     "DEV_NONFINITE", "DEV_BAD_EXPERT", "DEV_TIMEOUT", "EXPORTS",
     "moe_block_forward_profiled", "moe_block_kernel_count", "moe_block_kernel_name",
+    "moe_block_forward_noalloc",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,6 +43,7 @@ EXPORTS = (
     "moe_block_forward", "moe_block_forward_host", "moe_read_status",
     "moe_clear_status", "moe_status_string", "moe_abi_version",
     "moe_block_forward_profiled", "moe_block_kernel_count", "moe_block_kernel_name",
+    "moe_block_forward_noalloc",
 )
 
 
@@ -102,6 +104,7 @@ def lib() -> ctypes.CDLL:
                                                    ctypes.POINTER(P), I, P]),
                 "moe_block_kernel_count": (I, [DP, I]),
                 "moe_block_kernel_name": (ctypes.c_char_p, [DP, I, I]),
+                "moe_block_forward_noalloc": (I, [DP, WP, P, I, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -215,6 +218,14 @@ def moe_block_kernel_count(dims, T) -> int:
 def moe_block_kernel_name(dims, T, i) -> str:
     r = lib().moe_block_kernel_name(ctypes.byref(dims), int(T), int(i))
     return None if r is None else r.decode()
+
+
+def moe_block_forward_noalloc(dims, weights: Weights, x, T, out, stream=None):
+    """moe_block_forward with the library's fixed 4 MiB device scratch instead
+    of a caller workspace (for callers that cannot allocate)."""
+    _check(lib().moe_block_forward_noalloc(ctypes.byref(dims), ctypes.byref(weights), _a(x),
+                                           int(T), _a(out), _s(stream)),
+           "moe_block_forward_noalloc")
 
 
 def moe_read_status(workspace, stream=None) -> int:
