@@ -35,6 +35,11 @@
  *   - T == 0 is a no-op returning MOE_OK.
  *   - One workspace per concurrently running stream: two calls in flight on
  *     different streams must not share a workspace.
+ *   - The first 256 bytes of a workspace (the device status word and the
+ *     decode kernel's grid-barrier counter) must be zero before its first
+ *     use, e.g. by moe_clear_status; the library keeps them consistent after
+ *     that, except after a MOE_DEV_TIMEOUT, when moe_clear_status must be
+ *     called again before the workspace is reused.
  *   - Supported shapes: num_experts == 256, top_k == 8, group == 128, hidden
  *     and expert_inter multiples of 128 (hidden <= 8192, expert_inter <= 2048),
  *     shared_inter 0 or a multiple of 128 (<= 2048), 1 <= T <= 65536.
@@ -149,9 +154,13 @@ moe_status moe_combine(const moe_dims *dims, int T, const float *y,
 
 /* A1..A7 in one call: out [T][H] bf16 from x [T][H] bf16.  Optional outputs
  * (each nullable): ids_out [T][8], weights_out [T][8], logits_out [T][E],
- * gate_logit_out [T].  Decode-size T runs weight-streaming GEMV kernels;
- * large T runs tcgen05 grouped GEMMs; both meet the same tolerance and
- * route on the same fp32 logits.  For large T the routed terms are summed
+ * gate_logit_out [T].  Routes, chosen by sizes only: T <= 64 with
+ * hidden <= 2048 (a multiple of 256) and intermediate sizes <= 2048 runs one
+ * persistent cooperative kernel (one CTA per SM, bounded grid barriers);
+ * other T < 128 run separate weight-streaming kernels; T >= 128 runs tcgen05
+ * grouped GEMMs.  All routes meet the same tolerance and route on the same
+ * fp32 logits.  The environment variable MOE_DECODE_ROUTE=gemv (read once
+ * per process) forces the separate kernels below T = 128, for diagnostics.  For large T the routed terms are summed
  * with fp32 atomics, so the last fp32 bit of an unrounded sum (and, rarely,
  * the bf16 rounding of out) may vary between runs. */
 moe_status moe_block_forward(const moe_dims *dims, const moe_weights *w,
@@ -192,7 +201,7 @@ const char *moe_block_kernel_name(const moe_dims *dims, int T, int i);
  * only inputs and outputs; the scratch is a 4 MiB array that the library
  * holds on every GPU that loads it, until the process exits.
  *   - A (dims, T) whose moe_workspace_bytes exceeds 4 MiB is rejected with
- *     MOE_ERR_WORKSPACE (at H = 2048, I = Is = 512 that allows T <= 44).
+ *     MOE_ERR_WORKSPACE (at H = 2048, I = Is = 512 that allows T <= 64).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
@@ -207,7 +216,8 @@ moe_status moe_block_forward_noalloc(const moe_dims *dims, const moe_weights *w,
 
 /* Copy the device status word to *bits (synchronises the stream). */
 moe_status moe_read_status(const void *workspace, void *stream, uint32_t *bits);
-/* Zero the device status word (asynchronous). */
+/* Zero the first 256 bytes of the workspace: the device status word and the
+ * decode kernel's grid-barrier counter (asynchronous). */
 moe_status moe_clear_status(void *workspace, void *stream);
 
 const char *moe_status_string(moe_status s);

@@ -2,6 +2,8 @@
 // workspace carving, and the order of kernel launches on the caller's stream.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -54,13 +56,36 @@ size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 struct Layout {
   size_t status, logits, gate_logit, ids, weights, sgate;
   size_t counts, offsets, active, perm, slot_of;
-  size_t h_routed, h_shared, y, xstage, ostage;
+  size_t h_routed, h_shared, y, rpart, xstage, ostage;
   size_t xs, acc, items, counters, total;
 };
 
 // Token count from which moe_block_forward runs the tcgen05 grouped GEMMs
-// instead of the weight-streaming GEMV kernels.
+// instead of the weight-streaming kernels.
 constexpr int kTcMinT = 128;
+
+// Routes of moe_block_forward, chosen by sizes only (so that workspace sizes
+// never depend on the device): the fused persistent decode kernel, the
+// separate GEMV kernels, or the tcgen05 grouped GEMMs.  MOE_DECODE_ROUTE=gemv
+// in the environment forces the GEMV kernels below kTcMinT (diagnostics).
+enum Route { kRouteFused, kRouteGemv, kRouteTc };
+
+bool force_gemv() {
+  static int v = -1;
+  if (v < 0) {
+    const char *e = getenv("MOE_DECODE_ROUTE");
+    v = (e && strcmp(e, "gemv") == 0) ? 1 : 0;
+  }
+  return v == 1;
+}
+
+Route route_of(const moe_dims *d, int T) {
+  if (T >= kTcMinT) return kRouteTc;
+  if (!force_gemv() && T <= kFusedMaxT && d->hidden <= kFusedMaxH && d->hidden % 256 == 0 &&
+      d->expert_inter <= kFusedMaxI && d->shared_inter <= kFusedMaxI)
+    return kRouteFused;
+  return kRouteGemv;
+}
 
 Layout layout(const moe_dims *d, int T) {
   Layout L{};
@@ -81,10 +106,12 @@ Layout layout(const moe_dims *d, int T) {
   L.slot_of = take(4 * t * kK);
   L.h_routed = take(2 * t * kK * I);
   L.h_shared = take(2 * t * (Is ? Is : 1));
-  L.y = take(4 * t * (kK + 1) * H);
+  const Route r = route_of(d, T);
+  if (r == kRouteGemv) L.y = take(4 * t * (kK + 1) * H);
+  if (r == kRouteFused) L.rpart = take(4 * t * (kE + 1) * (H / 256));
   L.xstage = take(2 * t * H);
   L.ostage = take(2 * t * H);
-  if (T >= kTcMinT) {
+  if (r == kRouteTc) {
     L.xs = take(2 * t * kK * H);
     L.acc = take(4 * t * H);
     L.items = take(tc_items_bytes(T, static_cast<int>(I), static_cast<int>(Is),
@@ -125,6 +152,7 @@ moe_status check_ws(const moe_dims *d, int T, const void *ws, size_t ws_bytes, L
 const char *const kStageNames[] = {"router_gemv", "select_top8", "expert_lists",
                                    "gateup_swiglu", "down", "combine"};
 constexpr int kStages = 6;
+const char *const kFusedStageNames[] = {"decode_fused"};
 const char *const kTcStageNames[] = {"router_tc", "router_gate_gemv", "select_top8",
                                      "expert_lists", "build_items", "gather_rows", "zero_acc",
                                      "gateup_swiglu_tc", "down_combine_tc", "acc_to_bf16"};
@@ -158,7 +186,16 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   moe_bf16 *hr = at<moe_bf16>(ws, L.h_routed);
   moe_bf16 *hs = at<moe_bf16>(ws, L.h_shared);
   MOE_TRY(rec());
-  if (T < kTcMinT) {
+  const Route route = route_of(d, T);
+  if (route == kRouteFused) {
+    if (!fused_decode_supported(T, H, I, Is)) return MOE_ERR_UNSUPPORTED;
+    unsigned *grid_bar = reinterpret_cast<unsigned *>(at<uint8_t>(ws, L.status) + 4);
+    MOE_TRY(launch_decode_fused(x, T, H, I, Is, *w, at<float>(ws, L.rpart), hr, hs, out, ids_out,
+                                weights_out, logits_out, gate_logit_out, status, grid_bar, s));
+    MOE_TRY(rec());
+    return MOE_OK;
+  }
+  if (route == kRouteGemv) {
     MOE_TRY(launch_router_gemv(x, T, H, w->w_router, wg, logits, wg ? glog : nullptr, s));
     MOE_TRY(rec());
     MOE_TRY(launch_select(logits, T, kE, wg ? glog : nullptr, ids, wts, wg ? sg : nullptr,
@@ -216,7 +253,16 @@ const char *moe_status_string(moe_status s) {
 
 size_t moe_workspace_bytes(const moe_dims *dims, int T_max) {
   if (check_dims(dims) != MOE_OK || T_max < 0 || T_max > kMaxT) return 0;
-  return layout(dims, T_max < 1 ? 1 : T_max).total;
+  if (T_max < 1) T_max = 1;
+  // sizes grow with T inside a route; take the largest route boundary <= T_max
+  size_t need = layout(dims, T_max).total;
+  const int cands[2] = {kTcMinT - 1, kFusedMaxT};
+  for (int c : cands)
+    if (c < T_max) {
+      const size_t v = layout(dims, c).total;
+      if (v > need) need = v;
+    }
+  return need;
 }
 
 moe_status moe_router_logits(const moe_dims *dims, const moe_weights *w, const moe_bf16 *x,
@@ -382,14 +428,18 @@ moe_status moe_block_forward_profiled(const moe_dims *dims, const moe_weights *w
 
 int moe_block_kernel_count(const moe_dims *dims, int T) {
   if (check_dims(dims) != MOE_OK || T < 1 || T > kMaxT) return 0;
-  if (T < kTcMinT) return kStages;
+  const Route r = route_of(dims, T);
+  if (r == kRouteFused) return 1;
+  if (r == kRouteGemv) return kStages;
   return dims->shared_inter > 0 ? kTcStages : kTcStages - 1;
 }
 
 const char *moe_block_kernel_name(const moe_dims *dims, int T, int i) {
   const int n = moe_block_kernel_count(dims, T);
   if (i < 0 || i >= n) return nullptr;
-  if (T < kTcMinT) return kStageNames[i];
+  const Route r = route_of(dims, T);
+  if (r == kRouteFused) return kFusedStageNames[i];
+  if (r == kRouteGemv) return kStageNames[i];
   if (dims->shared_inter == 0 && i >= 1) ++i;  // no gate-logit GEMV
   return kTcStageNames[i];
 }
@@ -404,7 +454,7 @@ moe_status moe_read_status(const void *workspace, void *stream, uint32_t *bits) 
 
 moe_status moe_clear_status(void *workspace, void *stream) {
   if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
-  MOE_TRY(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)));
+  MOE_TRY(cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

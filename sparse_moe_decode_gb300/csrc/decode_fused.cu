@@ -1,0 +1,724 @@
+// decode_fused.cu -- the whole block (A1..A7) for decode-size T in one
+// persistent cooperative kernel: one CTA per SM, phases separated by two
+// bounded grid barriers.
+//
+//   R  router: 257 rows x (H/256) K-slices of 256, one warp each, fp32
+//      partials (the pages' S1 split of the router into K-slices);
+//   -- grid barrier 1 --
+//   S  every CTA folds the partials of every token, selects its top-8 with
+//      the warp merge network and builds the token -> expert lists in shared
+//      memory (redundant per CTA: cheaper than another grid barrier);
+//   W  gate|up + SwiGLU: work unit = 8 gate rows + their 8 up rows of one
+//      expert (16 rows x H int8); units are dealt round-robin to the CTAs; a
+//      producer warp streams each unit's rows with bulk async copies into a
+//      5-stage shared-memory ring (the shared expert's first unit is fetched
+//      before routing is known); four warp quads consume units, each warp a
+//      quarter of K, as m16n8k16 bf16 tensor-core MMAs with the int8 weights
+//      converted exactly to bf16 in registers and the group scales promoted
+//      per 128-wide K group in fp32; h = bf16(silu(gate) * up) goes to global;
+//   -- grid barrier 2 --
+//   D  down + combine: CTA c owns output rows 16c .. 16c+15 of every expert;
+//      the producer has been streaming those rows since its gate|up units
+//      were done; y for every (token, slot) of those rows stays in shared
+//      memory and the CTA writes the combined bf16 output rows itself.
+//
+// The tensor cores here are the register-fragment form (mma.sync): at
+// decode sizes each weight meets 1..~10 tokens, the kernel is bound by HBM,
+// and register fragments avoid a shared-memory round trip for the converted
+// weights.  Every wait (mbarrier, grid barrier) is bounded by a %globaltimer
+// budget; a wait that gives up sets MOE_DEV_TIMEOUT and the kernel runs to
+// its end without waiting again.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "select.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kFQuads = 4;
+constexpr int kFConsumerWarps = 4 * kFQuads;
+constexpr int kFConsumers = kFConsumerWarps * 32;
+constexpr int kFThreads = kFConsumers + 32;  // + one producer warp
+constexpr int kFStages = 5;
+constexpr int kFRowPad = 16;                 // bytes of padding per staged row
+constexpr int kFStageBytes = 16 * (kFusedMaxH + kFRowPad);
+constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
+
+struct FusedParams {
+  const moe_bf16 *x;
+  int T, H, I, Is, KS;  // KS = H / 256 router K-slices
+  const moe_bf16 *w_router, *w_gate;
+  const int8_t *w13_q;
+  const moe_bf16 *w13_s;
+  const int8_t *w2_q;
+  const moe_bf16 *w2_s;
+  const int8_t *ws13_q;
+  const moe_bf16 *ws13_s;
+  const int8_t *ws2_q;
+  const moe_bf16 *ws2_s;
+  float *rpart;        // [T][257][KS] router partial sums
+  moe_bf16 *h_routed;  // [T*K][I], rows in list order
+  moe_bf16 *h_shared;  // [T][Is]
+  moe_bf16 *out;       // [T][H]
+  int32_t *ids_out;
+  float *weights_out, *logits_out, *gate_logit_out;
+  uint32_t *status;
+  unsigned *grid_bar;
+  unsigned long long budget_ns;
+};
+
+struct FusedSmem {
+  uint8_t ring[kFStages][kFStageBytes];
+  union {
+    float red[kFQuads][4][2][32][4];         // gate|up: quad reduction
+    float ys[16][kFusedMaxT * (kK + 1)];     // down: y of this CTA's 16 rows
+  } u;
+  int32_t ids[kFusedMaxT][kK];
+  float wts[kFusedMaxT][kK];
+  float sg[kFusedMaxT];
+  int32_t slot_of[kFusedMaxT][kK];
+  int32_t perm[kFusedMaxT * kK];
+  int32_t counts[kE];
+  int32_t offsets[kE + 1];
+  int32_t active[kE + 1];
+  unsigned long long mask[kE];
+  int scan_tmp[8];
+  uint64_t full[kFStages], empty[kFStages], routed;
+  int abort;
+};
+
+// ------------------------------------------------------------ helpers
+
+// 16 int8 -> 16 bf16 (8 packed words), exact: magic-number fp32 then the
+// upper halves.  Word m holds bytes 2m (low) and 2m+1 (high).
+__device__ __forceinline__ void i8x16_to_bf16(const uint4 q, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const f4 f = i8x4_to_f32(w[i]);
+    o[2 * i] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
+    o[2 * i + 1] = __byte_perm(__float_as_uint(f.z), __float_as_uint(f.w), 0x7632);
+  }
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate (register fragments).
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 1-D bulk copy global -> shared completing on an mbarrier, L2 evict-first.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(ptx::smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(ptx::smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_cg16(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float *p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool aborted(FusedSmem &S) {
+  return *reinterpret_cast<volatile int *>(&S.abort) != 0;
+}
+
+// Bounded wait used by consumers and the producer: after an abort it no
+// longer waits, so control flow (and every named barrier) still completes.
+__device__ __forceinline__ void fwait(uint64_t *bar, uint32_t parity, FusedSmem &S,
+                                      uint64_t budget) {
+  if (aborted(S)) return;
+  ptx::mbar_wait(bar, parity, &S.abort, budget);
+}
+
+// Grid-wide barrier of the consumer threads of every CTA.  Self-resetting:
+// CTA 0 adds 2^31 - (G - 1), the others 1, so each barrier flips bit 31 of the
+// counter and leaves its low bits unchanged.  Bounded by the wait budget.
+__device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t budget) {
+  ptx::named_barrier(1, kFConsumers);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1) : 1u;
+    const unsigned old = atomicAdd(bar, inc);
+    const uint64_t t0 = ptx::globaltimer();
+    while (((ld_acquire_u32(bar) ^ old) & 0x80000000u) == 0u) {
+      if (aborted(S) || ptx::globaltimer() - t0 > budget) {
+        *reinterpret_cast<volatile int *>(&S.abort) = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+  }
+  ptx::named_barrier(1, kFConsumers);
+}
+
+// Routing-derived work of this CTA (identical in every thread of the CTA).
+struct Work {
+  int nSb, nIb;        // gate|up units of the shared expert, per routed expert
+  int n_units;         // gate|up units in the whole grid
+  int n_local;         // gate|up units of this CTA: global index blockIdx.x + j * gridDim.x
+  int n0;              // first output row of this CTA in the down phase (-1: none)
+  int n_down_units;    // shared expert + active experts (0 if n0 < 0)
+  int unit_stride;     // bytes of one down unit (16 rows) in a ring stage
+  int units_per_stage;
+  int n_down_stages;
+};
+
+// gate|up unit b: the expert (kE = shared) and its first row pair i0
+__device__ __forceinline__ void gu_unit(const FusedSmem &S, const Work &wk, int b, int &e,
+                                        int &i0) {
+  if (b < wk.nSb) {
+    e = kE;
+    i0 = 8 * b;
+  } else {
+    const int a = (b - wk.nSb) / wk.nIb;
+    e = S.active[1 + a];
+    i0 = 8 * ((b - wk.nSb) % wk.nIb);
+  }
+}
+
+// down unit u of this CTA: the expert (kE = shared)
+__device__ __forceinline__ int down_unit(const FusedSmem &S, const FusedParams &p, int u) {
+  if (p.Is > 0) return u == 0 ? kE : S.active[u];
+  return S.active[1 + u];
+}
+
+__device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams &p) {
+  Work wk;
+  wk.nSb = p.Is / 8;
+  wk.nIb = p.I / 8;
+  const int n_active = S.active[0];
+  wk.n_units = wk.nSb + n_active * wk.nIb;
+  wk.n_local = blockIdx.x < wk.n_units
+                   ? (wk.n_units - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
+                   : 0;
+  wk.n0 = 16 * static_cast<int>(blockIdx.x) < p.H ? 16 * static_cast<int>(blockIdx.x) : -1;
+  wk.n_down_units = wk.n0 >= 0 ? (p.Is > 0 ? 1 : 0) + n_active : 0;
+  const int imax = p.I > p.Is ? p.I : p.Is;
+  wk.unit_stride = 16 * (imax + kFRowPad);
+  wk.units_per_stage = kFStageBytes / wk.unit_stride;
+  wk.n_down_stages = (wk.n_down_units + wk.units_per_stage - 1) / wk.units_per_stage;
+  return wk;
+}
+
+// Producer: issue gate|up unit j (expert e, row pairs i0..i0+7) into ring
+// stage j % kFStages.
+__device__ __forceinline__ void produce_gu(FusedSmem &S, const FusedParams &p, int j, int e,
+                                           int i0, uint64_t pol, uint64_t budget, int lane) {
+  const int s = j % kFStages;
+  if (lane == 0) {
+    fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
+    if (!aborted(S)) ptx::mbar_expect_tx(&S.full[s], 16u * p.H);
+  }
+  __syncwarp();
+  if (aborted(S)) return;
+  if (lane < 16) {
+    const int half = e == kE ? p.Is : p.I;
+    const int row = lane < 8 ? i0 + lane : half + i0 + lane - 8;
+    const int8_t *src = e == kE ? p.ws13_q + static_cast<size_t>(row) * p.H
+                                : p.w13_q + (static_cast<size_t>(e) * 2 * p.I + row) * p.H;
+    bulk_g2s(S.ring[s] + lane * (p.H + kFRowPad), src, p.H, &S.full[s], pol);
+  }
+  __syncwarp();
+}
+
+// Producer: issue down stage k (units k*U .. ) into ring stage (n_local + k).
+__device__ __forceinline__ void produce_down(FusedSmem &S, const FusedParams &p, const Work &wk,
+                                             int k, uint64_t pol, uint64_t budget, int lane) {
+  const int j = wk.n_local + k;
+  const int s = j % kFStages;
+  const int u0 = k * wk.units_per_stage;
+  const int nu = min(wk.units_per_stage, wk.n_down_units - u0);
+  if (lane == 0) {
+    fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
+    uint32_t tx = 0;
+    for (int u = 0; u < nu; ++u) tx += 16u * (down_unit(S, p, u0 + u) == kE ? p.Is : p.I);
+    if (!aborted(S)) ptx::mbar_expect_tx(&S.full[s], tx);
+  }
+  __syncwarp();
+  if (aborted(S)) return;
+  const int imax = p.I > p.Is ? p.I : p.Is;
+  for (int idx = lane; idx < nu * 16; idx += 32) {
+    const int u = idx >> 4, r = idx & 15;
+    const int e = down_unit(S, p, u0 + u);
+    const int Ii = e == kE ? p.Is : p.I;
+    const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(wk.n0 + r) * p.Is
+                                : p.w2_q + (static_cast<size_t>(e) * p.H + wk.n0 + r) * p.I;
+    bulk_g2s(S.ring[s] + u * wk.unit_stride + r * (imax + kFRowPad), src, Ii, &S.full[s], pol);
+  }
+  __syncwarp();
+}
+
+// Phase R: router partials.  Task (r, ks): one warp dots row r (256 expert
+// rows, row 256 = shared gate) over K-slice ks with every token.
+__device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, int lane) {
+  const int rows = kE + (p.Is > 0 ? 1 : 0);
+  const int n_tasks = rows * p.KS;
+  for (int task = blockIdx.x * kFConsumerWarps + cwarp; task < n_tasks;
+       task += gridDim.x * kFConsumerWarps) {
+    const int r = task / p.KS, ks = task % p.KS;
+    const int k = ks * 256 + lane * 8;
+    const moe_bf16 *wrow = r < kE ? p.w_router + static_cast<size_t>(r) * p.H : p.w_gate;
+    const uint4 wv = ld_nc(wrow + k);
+    const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                         bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+    for (int t = 0; t < p.T; ++t) {
+      const uint4 xv = ld_nc(p.x + static_cast<size_t>(t) * p.H + k);
+      float a = wf[0] * bf16_lo(xv.x);
+      a = fmaf(wf[1], bf16_hi(xv.x), a); a = fmaf(wf[2], bf16_lo(xv.y), a);
+      a = fmaf(wf[3], bf16_hi(xv.y), a); a = fmaf(wf[4], bf16_lo(xv.z), a);
+      a = fmaf(wf[5], bf16_hi(xv.z), a); a = fmaf(wf[6], bf16_lo(xv.w), a);
+      a = fmaf(wf[7], bf16_hi(xv.w), a);
+      a = warp_sum(a);
+      if (lane == 0) p.rpart[(static_cast<size_t>(t) * (kE + 1) + r) * p.KS + ks] = a;
+    }
+  }
+}
+
+// Phase S: fold partials (fixed K-slice order), select, and build the lists.
+__device__ __forceinline__ void phase_select(FusedSmem &S, const FusedParams &p, int cwarp,
+                                             int lane) {
+  const bool out_cta = blockIdx.x == 0;
+  for (int t = cwarp; t < p.T; t += kFConsumerWarps) {
+    const float *rp = p.rpart + static_cast<size_t>(t) * (kE + 1) * p.KS;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = 8 * lane + i;
+      float a = 0.0f;
+      for (int ks = 0; ks < p.KS; ++ks) a += ld_cg_f32(rp + e * p.KS + ks);
+      v[i] = a;
+    }
+    float g = 0.0f;
+    if (p.Is > 0)
+      for (int ks = 0; ks < p.KS; ++ks) g += ld_cg_f32(rp + kE * p.KS + ks);
+    int id[8];
+    float w[8];
+    const bool ok = select_top8_regs(v, lane, id, w);
+    if (lane < 8) {
+      int myid = id[0];
+      float myw = w[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i)
+        if (lane == i) { myid = id[i]; myw = w[i]; }
+      S.ids[t][lane] = myid;
+      S.wts[t][lane] = myw;
+      if (out_cta) {
+        if (p.ids_out) p.ids_out[t * kK + lane] = myid;
+        if (p.weights_out) p.weights_out[t * kK + lane] = myw;
+      }
+    }
+    if (lane == 0) {
+      S.sg[t] = p.Is > 0 ? sigmoidf_(g) : 0.0f;
+      if (out_cta && p.gate_logit_out && p.Is > 0) p.gate_logit_out[t] = g;
+      if (out_cta && !ok) set_status(p.status, MOE_DEV_NONFINITE);
+    }
+    if (out_cta && p.logits_out) {
+      float4 *dst = reinterpret_cast<float4 *>(p.logits_out + static_cast<size_t>(t) * kE + 8 * lane);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+  const int tid = threadIdx.x;  // consumer threads 0 .. 511
+  if (tid < kE) {
+    S.counts[tid] = 0;
+    S.mask[tid] = 0ull;
+  }
+  ptx::named_barrier(1, kFConsumers);
+  for (int i = tid; i < p.T * kK; i += kFConsumers) {
+    const int t = i / kK, e = S.ids[t][i % kK];
+    if (e >= 0) {
+      atomicAdd(&S.counts[e], 1);
+      atomicOr(&S.mask[e], 1ull << t);
+    }
+  }
+  ptx::named_barrier(1, kFConsumers);
+  // exclusive scans of counts (offsets) and of (counts > 0) (active list)
+  if (tid < kE) {
+    const int c = S.counts[tid];
+    int incl = c, act = c > 0 ? 1 : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n1 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      const int n2 = __shfl_up_sync(0xFFFFFFFFu, act, o);
+      if (lane >= o) { incl += n1; act += n2; }
+    }
+    if (lane == 31) S.scan_tmp[cwarp] = incl | (act << 20);
+    ptx::named_barrier(6, kE);  // ids 2..5 belong to the quads
+    int base = 0, abase = 0;
+    for (int w2 = 0; w2 < cwarp; ++w2) {
+      base += S.scan_tmp[w2] & 0xFFFFF;
+      abase += S.scan_tmp[w2] >> 20;
+    }
+    const int off = base + incl - c;
+    const int a_idx = abase + act - (c > 0 ? 1 : 0);
+    S.offsets[tid] = off;
+    if (c > 0) S.active[1 + a_idx] = tid;
+    if (tid == kE - 1) {
+      S.offsets[kE] = off + c;
+      S.active[0] = a_idx + (c > 0 ? 1 : 0);
+    }
+  }
+  ptx::named_barrier(1, kFConsumers);
+  for (int i = tid; i < p.T * kK; i += kFConsumers) {
+    const int t = i / kK, j = i % kK, e = S.ids[t][j];
+    int pos = -1;
+    if (e >= 0) {
+      pos = S.offsets[e] + __popcll(S.mask[e] & ((1ull << t) - 1ull));
+      S.perm[pos] = i;
+    }
+    S.slot_of[t][j] = pos;
+  }
+  ptx::named_barrier(1, kFConsumers);
+}
+
+// One 64-wide K slice of a 16-row unit against up to two n8 token tiles:
+// A rows g and g+8 from the staged rows (int8 -> bf16 in registers), B from
+// the tokens' activation rows.  Logical k (2c, 2c+1 | 2c+8, 2c+9) of MMA jj
+// maps to physical k 16c + 4jj + (0, 1 | 2, 3) for A and B alike.
+__device__ __forceinline__ void slice_mma(const uint8_t *rows, int stride, int k0,
+                                          const moe_bf16 *const (&brow)[2], int ntiles, int g,
+                                          int c, float (&part)[2][4], bool cg_loads) {
+  const uint4 qa = *reinterpret_cast<const uint4 *>(rows + g * stride + k0 + 16 * c);
+  const uint4 qb = *reinterpret_cast<const uint4 *>(rows + (g + 8) * stride + k0 + 16 * c);
+  uint32_t a[8], b[8];
+  i8x16_to_bf16(qa, a);
+  i8x16_to_bf16(qb, b);
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    if (nt >= ntiles) break;
+    uint32_t xw[8];
+    if (brow[nt]) {
+      const moe_bf16 *src = brow[nt] + k0 + 16 * c;
+      const uint4 x0 = cg_loads ? ld_cg16(src) : ld_nc(src);
+      const uint4 x1 = cg_loads ? ld_cg16(src + 8) : ld_nc(src + 8);
+      xw[0] = x0.x; xw[1] = x0.y; xw[2] = x0.z; xw[3] = x0.w;
+      xw[4] = x1.x; xw[5] = x1.y; xw[6] = x1.z; xw[7] = x1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xw[i] = 0u;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      mma16816(part[nt], a[2 * jj], b[2 * jj], a[2 * jj + 1], b[2 * jj + 1], xw[2 * jj],
+               xw[2 * jj + 1]);
+  }
+}
+
+// Phase W consumer: gate|up unit j of this CTA, by quad q (warp wq of 4
+// takes K quarter wq).
+__device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, const Work &wk,
+                                           int j, int q, int wq, int lane, uint64_t budget) {
+  const int s = j % kFStages;
+  fwait(&S.full[s], (j / kFStages) & 1, S, budget);
+  int e, i0;
+  gu_unit(S, wk, blockIdx.x + j * gridDim.x, e, i0);
+  const bool sh = e == kE;
+  const int half = sh ? p.Is : p.I;
+  const int n_tok = sh ? p.T : S.counts[e];
+  const int p0 = sh ? 0 : S.offsets[e];
+  const int g = lane >> 2, c = lane & 3;
+  const int ng = p.H / kG;
+  const moe_bf16 *sbase = sh ? p.ws13_s : p.w13_s + static_cast<size_t>(e) * 2 * p.I * ng;
+  const moe_bf16 *s_gate = sbase + static_cast<size_t>(i0 + g) * ng;
+  const moe_bf16 *s_up = sbase + static_cast<size_t>(half + i0 + g) * ng;
+  const int kq = p.H / 4, kb = wq * kq;
+  const uint8_t *rows = S.ring[s];
+  const int stride = p.H + kFRowPad;
+  for (int tb = 0; tb < n_tok; tb += kFPass) {
+    const int ntiles = min(2, (n_tok - tb + 7) / 8);
+    const moe_bf16 *brow[2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int idx = tb + 8 * nt + g;
+      brow[nt] = nullptr;
+      if (idx < n_tok) {
+        const int t = sh ? idx : S.perm[p0 + idx] / kK;
+        brow[nt] = p.x + static_cast<size_t>(t) * p.H;
+      }
+    }
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int kg = kb; kg < kb + kq; kg += kG) {
+      float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      slice_mma(rows, stride, kg, brow, ntiles, g, c, part, false);
+      slice_mma(rows, stride, kg + 64, brow, ntiles, g, c, part, false);
+      const float sgv = bf16_to_f32(s_gate[kg / kG]), suv = bf16_to_f32(s_up[kg / kG]);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        acc[nt][0] = fmaf(sgv, part[nt][0], acc[nt][0]);
+        acc[nt][1] = fmaf(sgv, part[nt][1], acc[nt][1]);
+        acc[nt][2] = fmaf(suv, part[nt][2], acc[nt][2]);
+        acc[nt][3] = fmaf(suv, part[nt][3], acc[nt][3]);
+      }
+    }
+    // reduce the four K quarters in a fixed order, then SwiGLU
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) S.u.red[q][wq][nt][lane][i] = acc[nt][i];
+    ptx::named_barrier(2 + q, 128);
+    if (wq < ntiles) {
+      const int nt = wq;
+      float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w2 = 0; w2 < 4; ++w2)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r4[i] += S.u.red[q][w2][nt][lane][i];
+#pragma unroll
+      for (int col = 0; col < 2; ++col) {
+        const int idx = tb + 8 * nt + 2 * c + col;
+        if (idx < n_tok) {
+          const uint16_t hv = f32_to_bf16(silu_mul(r4[col], r4[2 + col]));
+          if (sh) p.h_shared[static_cast<size_t>(idx) * p.Is + i0 + g] = hv;
+          else p.h_routed[static_cast<size_t>(p0 + idx) * p.I + i0 + g] = hv;
+        }
+      }
+    }
+    ptx::named_barrier(2 + q, 128);
+  }
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+}
+
+// Phase D consumer: down stage k (units k*U ..), by quad q; warp wq takes
+// units wq, wq + 4, ... of the stage, each over its full K (= I or Is).
+__device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p, const Work &wk,
+                                             int k, int wq, int lane, uint64_t budget) {
+  const int j = wk.n_local + k;
+  const int s = j % kFStages;
+  fwait(&S.full[s], (j / kFStages) & 1, S, budget);
+  const int u0 = k * wk.units_per_stage;
+  const int nu = min(wk.units_per_stage, wk.n_down_units - u0);
+  const int g = lane >> 2, c = lane & 3;
+  const int imax = p.I > p.Is ? p.I : p.Is;
+  const int ys_ld = p.T * (kK + 1);
+  for (int u = wq; u < nu; u += 4) {
+    const int e = down_unit(S, p, u0 + u);
+    const bool sh = e == kE;
+    const int Ii = sh ? p.Is : p.I;
+    const int ng = Ii / kG;
+    const int n_tok = sh ? p.T : S.counts[e];
+    const int p0 = sh ? 0 : S.offsets[e];
+    const moe_bf16 *sbase = sh ? p.ws2_s : p.w2_s + static_cast<size_t>(e) * p.H * ng;
+    const moe_bf16 *s_lo = sbase + static_cast<size_t>(wk.n0 + g) * ng;
+    const moe_bf16 *s_hi = sbase + static_cast<size_t>(wk.n0 + g + 8) * ng;
+    const uint8_t *rows = S.ring[s] + u * wk.unit_stride;
+    for (int tb = 0; tb < n_tok; tb += kFPass) {
+      const int ntiles = min(2, (n_tok - tb + 7) / 8);
+      const moe_bf16 *brow[2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int idx = tb + 8 * nt + g;
+        brow[nt] = nullptr;
+        if (idx < n_tok)
+          brow[nt] = sh ? p.h_shared + static_cast<size_t>(idx) * p.Is
+                        : p.h_routed + static_cast<size_t>(p0 + idx) * p.I;
+      }
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      for (int gi = 0; gi < ng; ++gi) {
+        float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        slice_mma(rows, imax + kFRowPad, gi * kG, brow, ntiles, g, c, part, true);
+        slice_mma(rows, imax + kFRowPad, gi * kG + 64, brow, ntiles, g, c, part, true);
+        const float slo = bf16_to_f32(s_lo[gi]), shi = bf16_to_f32(s_hi[gi]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          acc[nt][0] = fmaf(slo, part[nt][0], acc[nt][0]);
+          acc[nt][1] = fmaf(slo, part[nt][1], acc[nt][1]);
+          acc[nt][2] = fmaf(shi, part[nt][2], acc[nt][2]);
+          acc[nt][3] = fmaf(shi, part[nt][3], acc[nt][3]);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int col = 0; col < 2; ++col) {
+          const int idx = tb + 8 * nt + 2 * c + col;
+          if (nt < ntiles && idx < n_tok) {
+            const int slot = sh ? p.T * kK + idx : p0 + idx;
+            S.u.ys[g][slot] = acc[nt][col];
+            S.u.ys[g + 8][slot] = acc[nt][2 + col];
+          }
+        }
+    }
+  }
+  (void)ys_ld;
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+}
+
+// A7 for this CTA's 16 output rows: slots in rank order, then the shared
+// expert, fp32, one bf16 rounding.
+__device__ __forceinline__ void phase_combine(FusedSmem &S, const FusedParams &p, const Work &wk) {
+  if (wk.n0 < 0) return;
+  for (int i = threadIdx.x; i < 16 * p.T; i += kFConsumers) {
+    const int r = i & 15, t = i >> 4;
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kK; ++j) {
+      const int slot = S.slot_of[t][j];
+      const float w = S.wts[t][j];
+      if (slot >= 0 && w != 0.0f) acc = fmaf(w, S.u.ys[r][slot], acc);
+    }
+    if (p.Is > 0 && S.sg[t] != 0.0f) acc = fmaf(S.sg[t], S.u.ys[r][p.T * kK + t], acc);
+    p.out[static_cast<size_t>(t) * p.H + wk.n0 + r] = f32_to_bf16(acc);
+  }
+}
+
+__global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedParams p) {
+  extern __shared__ __align__(128) uint8_t fsmem_raw[];
+  FusedSmem &S = *reinterpret_cast<FusedSmem *>(fsmem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t budget = p.budget_ns;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kFStages; ++s) {
+      ptx::mbar_init(&S.full[s], 1);
+      ptx::mbar_init(&S.empty[s], 4);  // the four warps of the consuming quad
+    }
+    ptx::mbar_init(&S.routed, 1);
+    S.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kFConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = ptx::policy_evict_first();
+    // the shared expert's unit needs no routing: fetch it at once
+    const bool early = p.Is > 0 && static_cast<int>(blockIdx.x) < p.Is / 8;
+    if (early) produce_gu(S, p, 0, kE, 8 * blockIdx.x, pol, budget, lane);
+    if (lane == 0) fwait(&S.routed, 0, S, budget);
+    __syncwarp();
+    const Work wk = make_work(S, p);
+    int issued = early ? 1 : 0;
+    for (int j = issued; j < wk.n_local && !aborted(S); ++j, ++issued) {
+      int e, i0;
+      gu_unit(S, wk, blockIdx.x + j * gridDim.x, e, i0);
+      produce_gu(S, p, j, e, i0, pol, budget, lane);
+    }
+    for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k, ++issued)
+      produce_down(S, p, wk, k, pol, budget, lane);
+    // after an abort, let the copies already in flight land before exiting
+    if (aborted(S) && lane == 0) {
+      int never = 0;
+      for (int k = 0; k < kFStages && k < issued; ++k) {
+        const int j = issued - 1 - k;
+        ptx::mbar_wait(&S.full[j % kFStages], (j / kFStages) & 1, &never, budget);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- consumers
+    const int q = warp >> 2, wq = warp & 3;
+    phase_router(p, warp, lane);
+    grid_sync(p.grid_bar, S, budget);
+    phase_select(S, p, warp, lane);
+    if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
+    const Work wk = make_work(S, p);
+    for (int j = q; j < wk.n_local; j += kFQuads) consume_gu(S, p, wk, j, q, wq, lane, budget);
+    grid_sync(p.grid_bar, S, budget);
+    for (int k = q; k < wk.n_down_stages; k += kFQuads)
+      consume_down(S, p, wk, k, wq, lane, budget);
+    ptx::named_barrier(1, kFConsumers);
+    phase_combine(S, p, wk);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && aborted(S)) set_status(p.status, MOE_DEV_TIMEOUT);
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+unsigned long long fused_wait_budget_ns() {
+  static unsigned long long v = 0;
+  if (!v) {
+    const char *e = getenv("MOE_WAIT_BUDGET_NS");
+    v = e ? strtoull(e, nullptr, 10) : 2000000000ull;
+    if (!v) v = 1;
+  }
+  return v;
+}
+
+}  // namespace
+
+size_t fused_smem_bytes() { return sizeof(FusedSmem); }
+
+bool fused_decode_supported(int T, int H, int I, int Is) {
+  if (T < 1 || T > kFusedMaxT || H > kFusedMaxH || H % 256 != 0) return false;
+  if (I > kFusedMaxI || Is > kFusedMaxI || I % 128 != 0 || Is % 128 != 0) return false;
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return false;
+  if (!sms[dev]) {
+    // one resident CTA per SM is required for the grid barriers
+    int per_sm = 0;
+    if (cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(FusedSmem))) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel, kFThreads,
+                                                      sizeof(FusedSmem)) != cudaSuccess ||
+        per_sm < 1) {
+      sms[dev] = -1;
+    } else {
+      sms[dev] = device_sms();
+    }
+  }
+  return sms[dev] > 0 && sms[dev] * 16 >= H;
+}
+
+cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
+                                const moe_weights &w, float *rpart, moe_bf16 *h_routed,
+                                moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
+                                float *weights_out, float *logits_out, float *gate_logit_out,
+                                uint32_t *status, unsigned *grid_bar, cudaStream_t s) {
+  FusedParams p{};
+  p.x = x; p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 256;
+  p.w_router = w.w_router; p.w_gate = Is > 0 ? w.w_shared_gate : nullptr;
+  p.w13_q = w.w13_q; p.w13_s = w.w13_s; p.w2_q = w.w2_q; p.w2_s = w.w2_s;
+  p.ws13_q = w.ws13_q; p.ws13_s = w.ws13_s; p.ws2_q = w.ws2_q; p.ws2_s = w.ws2_s;
+  p.rpart = rpart; p.h_routed = h_routed; p.h_shared = h_shared; p.out = out;
+  p.ids_out = ids_out; p.weights_out = weights_out; p.logits_out = logits_out;
+  p.gate_logit_out = gate_logit_out; p.status = status; p.grid_bar = grid_bar;
+  p.budget_ns = fused_wait_budget_ns();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(device_sms());
+  cfg.blockDim = dim3(kFThreads);
+  cfg.dynamicSmemBytes = sizeof(FusedSmem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_fused_kernel, p);
+}
+
+}  // namespace moe

@@ -67,15 +67,12 @@ __device__ __forceinline__ void merge_level(uint64_t (&k)[8], int mask) {
   cx(k[0], k[1]); cx(k[2], k[3]); cx(k[4], k[5]); cx(k[6], k[7]);
 }
 
-// Select for one token with the whole warp.  `row` holds 256 fp32 logits
-// (16-byte aligned).  On return every lane holds the token's ids (rank
+// Select for one token with the whole warp, lane l holding the logits of
+// experts 8l .. 8l+7 in v.  On return every lane holds the token's ids (rank
 // order) and softmax weights; returns false for a non-finite row (ids -1,
 // weights 0).
-__device__ __forceinline__ bool select_top8_warp(const float *row, int lane, int (&ids)[8],
+__device__ __forceinline__ bool select_top8_regs(const float (&v)[8], int lane, int (&ids)[8],
                                                  float (&w)[8]) {
-  const float4 a = reinterpret_cast<const float4 *>(row)[2 * lane];
-  const float4 b = reinterpret_cast<const float4 *>(row)[2 * lane + 1];
-  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   bool finite = true;
   uint64_t k[8];
 #pragma unroll
@@ -106,6 +103,15 @@ __device__ __forceinline__ bool select_top8_warp(const float *row, int lane, int
     w[i] = e[i] * inv;
   }
   return true;
+}
+
+// As select_top8_regs, reading the 256 fp32 logits of `row` (16-byte aligned).
+__device__ __forceinline__ bool select_top8_warp(const float *row, int lane, int (&ids)[8],
+                                                 float (&w)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(row)[2 * lane];
+  const float4 b = reinterpret_cast<const float4 *>(row)[2 * lane + 1];
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  return select_top8_regs(v, lane, ids, w);
 }
 
 __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
