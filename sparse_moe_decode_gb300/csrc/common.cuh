@@ -76,7 +76,7 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p), "l"(evict_first_policy()));
   return r;
@@ -84,7 +84,7 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
 
 __device__ __forceinline__ uint4 ld_nc(const void *p) {
   uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;

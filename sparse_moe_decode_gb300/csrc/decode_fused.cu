@@ -107,8 +107,7 @@ __device__ __forceinline__ void i8x16_to_bf16(const uint4 q, uint32_t (&o)[8]) {
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulate (register fragments).
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -124,19 +123,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Loads of data written earlier in this launch by other CTAs: L2 only.
 __device__ __forceinline__ uint4 ld_cg16(const void *p) {
-  uint4 r;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
+  return __ldcg(reinterpret_cast<const uint4 *>(p));
 }
 
-__device__ __forceinline__ float ld_cg_f32(const float *p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
+__device__ __forceinline__ float ld_cg_f32(const float *p) { return __ldcg(p); }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
   unsigned v;
@@ -398,13 +390,32 @@ __device__ __forceinline__ void phase_select(FusedSmem &S, const FusedParams &p,
   ptx::named_barrier(1, kFConsumers);
 }
 
+// B fragments of one 64-wide K slice for up to two n8 token tiles: lane
+// (g, c) reads 16 consecutive bf16 of its token's row at k0 + 16c.
+__device__ __forceinline__ void load_b(const moe_bf16 *const (&brow)[2], int ntiles, int k0,
+                                       int c, bool cg, uint32_t (&xw)[2][8]) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    if (nt < ntiles && brow[nt]) {
+      const moe_bf16 *src = brow[nt] + k0 + 16 * c;
+      const uint4 x0 = cg ? ld_cg16(src) : ld_nc(src);
+      const uint4 x1 = cg ? ld_cg16(src + 8) : ld_nc(src + 8);
+      xw[nt][0] = x0.x; xw[nt][1] = x0.y; xw[nt][2] = x0.z; xw[nt][3] = x0.w;
+      xw[nt][4] = x1.x; xw[nt][5] = x1.y; xw[nt][6] = x1.z; xw[nt][7] = x1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xw[nt][i] = 0u;
+    }
+  }
+}
+
 // One 64-wide K slice of a 16-row unit against up to two n8 token tiles:
-// A rows g and g+8 from the staged rows (int8 -> bf16 in registers), B from
-// the tokens' activation rows.  Logical k (2c, 2c+1 | 2c+8, 2c+9) of MMA jj
-// maps to physical k 16c + 4jj + (0, 1 | 2, 3) for A and B alike.
-__device__ __forceinline__ void slice_mma(const uint8_t *rows, int stride, int k0,
-                                          const moe_bf16 *const (&brow)[2], int ntiles, int g,
-                                          int c, float (&part)[2][4], bool cg_loads) {
+// A rows g and g+8 from the staged rows (int8 -> bf16 in registers).
+// Logical k (2c, 2c+1 | 2c+8, 2c+9) of MMA jj maps to physical k
+// 16c + 4jj + (0, 1 | 2, 3) for A and B alike.
+__device__ __forceinline__ void mma_slice(const uint8_t *rows, int stride, int k0, int ntiles,
+                                          int g, int c, const uint32_t (&xw)[2][8],
+                                          float (&part)[2][4]) {
   const uint4 qa = *reinterpret_cast<const uint4 *>(rows + g * stride + k0 + 16 * c);
   const uint4 qb = *reinterpret_cast<const uint4 *>(rows + (g + 8) * stride + k0 + 16 * c);
   uint32_t a[8], b[8];
@@ -413,21 +424,36 @@ __device__ __forceinline__ void slice_mma(const uint8_t *rows, int stride, int k
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     if (nt >= ntiles) break;
-    uint32_t xw[8];
-    if (brow[nt]) {
-      const moe_bf16 *src = brow[nt] + k0 + 16 * c;
-      const uint4 x0 = cg_loads ? ld_cg16(src) : ld_nc(src);
-      const uint4 x1 = cg_loads ? ld_cg16(src + 8) : ld_nc(src + 8);
-      xw[0] = x0.x; xw[1] = x0.y; xw[2] = x0.z; xw[3] = x0.w;
-      xw[4] = x1.x; xw[5] = x1.y; xw[6] = x1.z; xw[7] = x1.w;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xw[i] = 0u;
-    }
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj)
-      mma16816(part[nt], a[2 * jj], b[2 * jj], a[2 * jj + 1], b[2 * jj + 1], xw[2 * jj],
-               xw[2 * jj + 1]);
+      mma16816(part[nt], a[2 * jj], b[2 * jj], a[2 * jj + 1], b[2 * jj + 1], xw[nt][2 * jj],
+               xw[nt][2 * jj + 1]);
+  }
+}
+
+// The K range [kb, kb + kn) of a 16-row unit in 128-wide groups (two
+// slices each), B fragments fetched one slice ahead; partial sums of each
+// group are promoted with the rows' group scales (lo: rows 0..7, hi: 8..15).
+__device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int kb, int kn,
+                                          const moe_bf16 *const (&brow)[2], int ntiles, int g,
+                                          int c, bool cg, const moe_bf16 *s_lo,
+                                          const moe_bf16 *s_hi, float (&acc)[2][4]) {
+  uint32_t xa[2][8], xb[2][8];
+  load_b(brow, ntiles, kb, c, cg, xa);
+  for (int kg = kb; kg < kb + kn; kg += kG) {
+    float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    load_b(brow, ntiles, kg + 64, c, cg, xb);
+    const float slo = bf16_to_f32(s_lo[kg / kG]), shi = bf16_to_f32(s_hi[kg / kG]);
+    mma_slice(rows, stride, kg, ntiles, g, c, xa, part);
+    if (kg + kG < kb + kn) load_b(brow, ntiles, kg + kG, c, cg, xa);
+    mma_slice(rows, stride, kg + 64, ntiles, g, c, xb, part);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      acc[nt][0] = fmaf(slo, part[nt][0], acc[nt][0]);
+      acc[nt][1] = fmaf(slo, part[nt][1], acc[nt][1]);
+      acc[nt][2] = fmaf(shi, part[nt][2], acc[nt][2]);
+      acc[nt][3] = fmaf(shi, part[nt][3], acc[nt][3]);
+    }
   }
 }
 
@@ -464,19 +490,7 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
       }
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    for (int kg = kb; kg < kb + kq; kg += kG) {
-      float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      slice_mma(rows, stride, kg, brow, ntiles, g, c, part, false);
-      slice_mma(rows, stride, kg + 64, brow, ntiles, g, c, part, false);
-      const float sgv = bf16_to_f32(s_gate[kg / kG]), suv = bf16_to_f32(s_up[kg / kG]);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        acc[nt][0] = fmaf(sgv, part[nt][0], acc[nt][0]);
-        acc[nt][1] = fmaf(sgv, part[nt][1], acc[nt][1]);
-        acc[nt][2] = fmaf(suv, part[nt][2], acc[nt][2]);
-        acc[nt][3] = fmaf(suv, part[nt][3], acc[nt][3]);
-      }
-    }
+    unit_gemm(rows, stride, kb, kq, brow, ntiles, g, c, false, s_gate, s_up, acc);
     // reduce the four K quarters in a fixed order, then SwiGLU
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -541,19 +555,7 @@ __device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p,
                         : p.h_routed + static_cast<size_t>(p0 + idx) * p.I;
       }
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int gi = 0; gi < ng; ++gi) {
-        float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        slice_mma(rows, imax + kFRowPad, gi * kG, brow, ntiles, g, c, part, true);
-        slice_mma(rows, imax + kFRowPad, gi * kG + 64, brow, ntiles, g, c, part, true);
-        const float slo = bf16_to_f32(s_lo[gi]), shi = bf16_to_f32(s_hi[gi]);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          acc[nt][0] = fmaf(slo, part[nt][0], acc[nt][0]);
-          acc[nt][1] = fmaf(slo, part[nt][1], acc[nt][1]);
-          acc[nt][2] = fmaf(shi, part[nt][2], acc[nt][2]);
-          acc[nt][3] = fmaf(shi, part[nt][3], acc[nt][3]);
-        }
-      }
+      unit_gemm(rows, imax + kFRowPad, 0, Ii, brow, ntiles, g, c, true, s_lo, s_hi, acc);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
