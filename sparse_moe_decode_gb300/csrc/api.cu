@@ -81,7 +81,7 @@ bool force_gemv() {
 
 Route route_of(const moe_dims *d, int T) {
   if (T >= kTcMinT) return kRouteTc;
-  if (!force_gemv() && T <= kFusedMaxT && d->hidden <= kFusedMaxH && d->hidden % 256 == 0 &&
+  if (!force_gemv() && T <= kFusedMaxT && d->hidden <= kFusedMaxH && d->hidden % 512 == 0 &&
       d->expert_inter <= kFusedMaxI && d->shared_inter <= kFusedMaxI)
     return kRouteFused;
   return kRouteGemv;
@@ -108,7 +108,7 @@ Layout layout(const moe_dims *d, int T) {
   L.h_shared = take(2 * t * (Is ? Is : 1));
   const Route r = route_of(d, T);
   if (r == kRouteGemv) L.y = take(4 * t * (kK + 1) * H);
-  if (r == kRouteFused) L.rpart = take(4 * t * (kE + 1) * (H / 256));
+  if (r == kRouteFused) L.rpart = take(4 * t * 260 * (H / 512));
   L.xstage = take(2 * t * H);
   L.ostage = take(2 * t * H);
   if (r == kRouteTc) {
@@ -190,8 +190,10 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   if (route == kRouteFused) {
     if (!fused_decode_supported(T, H, I, Is)) return MOE_ERR_UNSUPPORTED;
     unsigned *grid_bar = reinterpret_cast<unsigned *>(at<uint8_t>(ws, L.status) + 4);
-    MOE_TRY(launch_decode_fused(x, T, H, I, Is, *w, at<float>(ws, L.rpart), hr, hs, out, ids_out,
-                                weights_out, logits_out, gate_logit_out, status, grid_bar, s));
+    MOE_TRY(launch_decode_fused(x, T, H, I, Is, *w, at<float>(ws, L.rpart),
+                                at<int32_t>(ws, L.ids), at<float>(ws, L.weights),
+                                at<float>(ws, L.sgate), hr, hs, out, ids_out, weights_out,
+                                logits_out, gate_logit_out, status, grid_bar, s));
     MOE_TRY(rec());
     return MOE_OK;
   }

@@ -1,13 +1,15 @@
 // decode_fused.cu -- the whole block (A1..A7) for decode-size T in one
-// persistent cooperative kernel: one CTA per SM, phases separated by two
+// persistent cooperative kernel: one CTA per SM, phases separated by three
 // bounded grid barriers.
 //
-//   R  router: 257 rows x (H/256) K-slices of 256, one warp each, fp32
+//   R  router: 257 rows x (H/512) K-slices of 512, one warp each, fp32
 //      partials (the pages' S1 split of the router into K-slices);
 //   -- grid barrier 1 --
-//   S  every CTA folds the partials of every token, selects its top-8 with
-//      the warp merge network and builds the token -> expert lists in shared
-//      memory (redundant per CTA: cheaper than another grid barrier);
+//   S  one warp per token folds its partials in a fixed order and selects
+//      its top-8 with the warp merge network (softmax, shared sigmoid);
+//   -- grid barrier 2 --
+//   L  every CTA reads all selections and builds the token -> expert lists
+//      in shared memory;
 //   W  gate|up + SwiGLU: work unit = 8 gate rows + their 8 up rows of one
 //      expert (16 rows x H int8); units are dealt round-robin to the CTAs; a
 //      producer warp streams each unit's rows with bulk async copies into a
@@ -16,7 +18,7 @@
 //      quarter of K, as m16n8k16 bf16 tensor-core MMAs with the int8 weights
 //      converted exactly to bf16 in registers and the group scales promoted
 //      per 128-wide K group in fp32; h = bf16(silu(gate) * up) goes to global;
-//   -- grid barrier 2 --
+//   -- grid barrier 3 --
 //   D  down + combine: CTA c owns output rows 16c .. 16c+15 of every expert;
 //      the producer has been streaming those rows since its gate|up units
 //      were done; y for every (token, slot) of those rows stays in shared
@@ -38,18 +40,18 @@
 namespace moe {
 namespace {
 
-constexpr int kFQuads = 4;
+constexpr int kFQuads = 3;   // 13 warps: at most 4 per SM sub-partition, 128 registers
 constexpr int kFConsumerWarps = 4 * kFQuads;
 constexpr int kFConsumers = kFConsumerWarps * 32;
 constexpr int kFThreads = kFConsumers + 32;  // + one producer warp
 constexpr int kFStages = 5;
-constexpr int kFRowPad = 16;                 // bytes of padding per staged row
-constexpr int kFStageBytes = 16 * (kFusedMaxH + kFRowPad);
+constexpr int kFStageBytes = 16 * kFusedMaxH;  // one gate|up unit, or packed down units
 constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
+constexpr int kRP = 260;                     // router partial row: 257 used, 16-byte rows
 
 struct FusedParams {
   const moe_bf16 *x;
-  int T, H, I, Is, KS;  // KS = H / 256 router K-slices
+  int T, H, I, Is, KS;  // KS = H / 512 router K-slices
   const moe_bf16 *w_router, *w_gate;
   const int8_t *w13_q;
   const moe_bf16 *w13_s;
@@ -59,7 +61,10 @@ struct FusedParams {
   const moe_bf16 *ws13_s;
   const int8_t *ws2_q;
   const moe_bf16 *ws2_s;
-  float *rpart;        // [T][257][KS] router partial sums
+  float *rpart;        // [T][KS][kRP] router partial sums
+  int32_t *sel_ids;    // [T][K] selection of every token (scratch)
+  float *sel_w;        // [T][K]
+  float *sel_sg;       // [T]
   moe_bf16 *h_routed;  // [T*K][I], rows in list order
   moe_bf16 *h_shared;  // [T][Is]
   moe_bf16 *out;       // [T][H]
@@ -91,18 +96,6 @@ struct FusedSmem {
 };
 
 // ------------------------------------------------------------ helpers
-
-// 16 int8 -> 16 bf16 (8 packed words), exact: magic-number fp32 then the
-// upper halves.  Word m holds bytes 2m (low) and 2m+1 (high).
-__device__ __forceinline__ void i8x16_to_bf16(const uint4 q, uint32_t (&o)[8]) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const f4 f = i8x4_to_f32(w[i]);
-    o[2 * i] = __byte_perm(__float_as_uint(f.x), __float_as_uint(f.y), 0x7632);
-    o[2 * i + 1] = __byte_perm(__float_as_uint(f.z), __float_as_uint(f.w), 0x7632);
-  }
-}
 
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulate (register fragments).
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -173,8 +166,9 @@ __device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t 
 // Routing-derived work of this CTA (identical in every thread of the CTA).
 struct Work {
   int nSb, nIb;        // gate|up units of the shared expert, per routed expert
-  int n_units;         // gate|up units in the whole grid
-  int n_local;         // gate|up units of this CTA: global index blockIdx.x + j * gridDim.x
+  int has_shared;      // this CTA takes shared-expert unit blockIdx.x first
+  int r_begin;         // first routed unit of this CTA (contiguous range)
+  int n_local;         // gate|up units of this CTA
   int n0;              // first output row of this CTA in the down phase (-1: none)
   int n_down_units;    // shared expert + active experts (0 if n0 < 0)
   int unit_stride;     // bytes of one down unit (16 rows) in a ring stage
@@ -182,16 +176,19 @@ struct Work {
   int n_down_stages;
 };
 
-// gate|up unit b: the expert (kE = shared) and its first row pair i0
-__device__ __forceinline__ void gu_unit(const FusedSmem &S, const Work &wk, int b, int &e,
+// gate|up unit j of this CTA: the expert (kE = shared) and its first row
+// pair i0.  CTA c takes shared unit c (if any) first, then a contiguous run
+// of routed units, so consecutive units mostly share an expert (and its
+// tokens' activations).
+__device__ __forceinline__ void gu_unit(const FusedSmem &S, const Work &wk, int j, int &e,
                                         int &i0) {
-  if (b < wk.nSb) {
+  if (wk.has_shared && j == 0) {
     e = kE;
-    i0 = 8 * b;
+    i0 = 8 * static_cast<int>(blockIdx.x);
   } else {
-    const int a = (b - wk.nSb) / wk.nIb;
-    e = S.active[1 + a];
-    i0 = 8 * ((b - wk.nSb) % wk.nIb);
+    const int b = wk.r_begin + j - wk.has_shared;
+    e = S.active[1 + b / wk.nIb];
+    i0 = 8 * (b % wk.nIb);
   }
 }
 
@@ -206,14 +203,16 @@ __device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams 
   wk.nSb = p.Is / 8;
   wk.nIb = p.I / 8;
   const int n_active = S.active[0];
-  wk.n_units = wk.nSb + n_active * wk.nIb;
-  wk.n_local = blockIdx.x < wk.n_units
-                   ? (wk.n_units - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
-                   : 0;
+  const int R = n_active * wk.nIb;  // routed units in the grid
+  const int c = blockIdx.x, G = gridDim.x;
+  wk.has_shared = c < wk.nSb ? 1 : 0;
+  wk.r_begin = static_cast<int>((static_cast<long long>(R) * c) / G);
+  const int r_end = static_cast<int>((static_cast<long long>(R) * (c + 1)) / G);
+  wk.n_local = wk.has_shared + (r_end - wk.r_begin);
   wk.n0 = 16 * static_cast<int>(blockIdx.x) < p.H ? 16 * static_cast<int>(blockIdx.x) : -1;
   wk.n_down_units = wk.n0 >= 0 ? (p.Is > 0 ? 1 : 0) + n_active : 0;
   const int imax = p.I > p.Is ? p.I : p.Is;
-  wk.unit_stride = 16 * (imax + kFRowPad);
+  wk.unit_stride = 16 * imax;
   wk.units_per_stage = kFStageBytes / wk.unit_stride;
   wk.n_down_stages = (wk.n_down_units + wk.units_per_stage - 1) / wk.units_per_stage;
   return wk;
@@ -230,12 +229,14 @@ __device__ __forceinline__ void produce_gu(FusedSmem &S, const FusedParams &p, i
   }
   __syncwarp();
   if (aborted(S)) return;
-  if (lane < 16) {
+  if (lane < 2) {
+    // 8 consecutive gate rows (lane 0) or up rows (lane 1): one contiguous
+    // copy of 8 * H bytes each (bulk copies of >= 8 KB stream at full rate)
     const int half = e == kE ? p.Is : p.I;
-    const int row = lane < 8 ? i0 + lane : half + i0 + lane - 8;
+    const int row = lane == 0 ? i0 : half + i0;
     const int8_t *src = e == kE ? p.ws13_q + static_cast<size_t>(row) * p.H
                                 : p.w13_q + (static_cast<size_t>(e) * 2 * p.I + row) * p.H;
-    bulk_g2s(S.ring[s] + lane * (p.H + kFRowPad), src, p.H, &S.full[s], pol);
+    bulk_g2s(S.ring[s] + lane * 8 * p.H, src, 8u * p.H, &S.full[s], pol);
   }
   __syncwarp();
 }
@@ -255,89 +256,119 @@ __device__ __forceinline__ void produce_down(FusedSmem &S, const FusedParams &p,
   }
   __syncwarp();
   if (aborted(S)) return;
-  const int imax = p.I > p.Is ? p.I : p.Is;
-  for (int idx = lane; idx < nu * 16; idx += 32) {
-    const int u = idx >> 4, r = idx & 15;
-    const int e = down_unit(S, p, u0 + u);
+  if (lane < nu) {
+    // one contiguous copy of the unit's 16 rows (16 * Ii bytes)
+    const int e = down_unit(S, p, u0 + lane);
     const int Ii = e == kE ? p.Is : p.I;
-    const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(wk.n0 + r) * p.Is
-                                : p.w2_q + (static_cast<size_t>(e) * p.H + wk.n0 + r) * p.I;
-    bulk_g2s(S.ring[s] + u * wk.unit_stride + r * (imax + kFRowPad), src, Ii, &S.full[s], pol);
+    const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(wk.n0) * p.Is
+                                : p.w2_q + (static_cast<size_t>(e) * p.H + wk.n0) * p.I;
+    bulk_g2s(S.ring[s] + lane * wk.unit_stride, src, 16u * Ii, &S.full[s], pol);
   }
   __syncwarp();
 }
 
 // Phase R: router partials.  Task (r, ks): one warp dots row r (256 expert
-// rows, row 256 = shared gate) over K-slice ks with every token.
+// rows, row 256 = shared gate) over K-slice ks (512 wide) with every token.
 __device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, int lane) {
   const int rows = kE + (p.Is > 0 ? 1 : 0);
   const int n_tasks = rows * p.KS;
   for (int task = blockIdx.x * kFConsumerWarps + cwarp; task < n_tasks;
        task += gridDim.x * kFConsumerWarps) {
     const int r = task / p.KS, ks = task % p.KS;
-    const int k = ks * 256 + lane * 8;
+    const int k = ks * 512 + lane * 16;
     const moe_bf16 *wrow = r < kE ? p.w_router + static_cast<size_t>(r) * p.H : p.w_gate;
-    const uint4 wv = ld_nc(wrow + k);
-    const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                         bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
-    for (int t = 0; t < p.T; ++t) {
-      const uint4 xv = ld_nc(p.x + static_cast<size_t>(t) * p.H + k);
-      float a = wf[0] * bf16_lo(xv.x);
-      a = fmaf(wf[1], bf16_hi(xv.x), a); a = fmaf(wf[2], bf16_lo(xv.y), a);
-      a = fmaf(wf[3], bf16_hi(xv.y), a); a = fmaf(wf[4], bf16_lo(xv.z), a);
-      a = fmaf(wf[5], bf16_hi(xv.z), a); a = fmaf(wf[6], bf16_lo(xv.w), a);
-      a = fmaf(wf[7], bf16_hi(xv.w), a);
-      a = warp_sum(a);
-      if (lane == 0) p.rpart[(static_cast<size_t>(t) * (kE + 1) + r) * p.KS + ks] = a;
+    const uint4 wv0 = ld_nc(wrow + k), wv1 = ld_nc(wrow + k + 8);
+    const uint32_t wq[8] = {wv0.x, wv0.y, wv0.z, wv0.w, wv1.x, wv1.y, wv1.z, wv1.w};
+    for (int t0 = 0; t0 < p.T; t0 += 8) {
+      uint4 xa[8], xb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (t0 + u < p.T) {
+          xa[u] = ld_nc(p.x + static_cast<size_t>(t0 + u) * p.H + k);
+          xb[u] = ld_nc(p.x + static_cast<size_t>(t0 + u) * p.H + k + 8);
+        }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (t0 + u >= p.T) break;
+        const uint32_t xq[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w,
+                                xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          a = fmaf(bf16_lo(wq[i]), bf16_lo(xq[i]), a);
+          a = fmaf(bf16_hi(wq[i]), bf16_hi(xq[i]), a);
+        }
+        a = warp_sum(a);
+        if (lane == 0) p.rpart[(static_cast<size_t>(t0 + u) * p.KS + ks) * kRP + r] = a;
+      }
     }
   }
 }
 
-// Phase S: fold partials (fixed K-slice order), select, and build the lists.
-__device__ __forceinline__ void phase_select(FusedSmem &S, const FusedParams &p, int cwarp,
-                                             int lane) {
-  const bool out_cta = blockIdx.x == 0;
-  for (int t = cwarp; t < p.T; t += kFConsumerWarps) {
-    const float *rp = p.rpart + static_cast<size_t>(t) * (kE + 1) * p.KS;
-    float v[8];
+// Phase S1: one warp per token over the whole grid: fold the K-slice
+// partials (fixed order), select the top-8, softmax, shared gate; results go
+// to global (and to the caller's optional outputs).
+__device__ __forceinline__ void phase_select(const FusedParams &p, int cwarp, int lane) {
+  const int t = blockIdx.x * kFConsumerWarps + cwarp;
+  if (t >= p.T) return;
+  const float *rp = p.rpart + static_cast<size_t>(t) * p.KS * kRP;
+  float4 a0[kFusedMaxH / 512], a1[kFusedMaxH / 512];
+  float gp[kFusedMaxH / 512];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = 8 * lane + i;
-      float a = 0.0f;
-      for (int ks = 0; ks < p.KS; ++ks) a += ld_cg_f32(rp + e * p.KS + ks);
-      v[i] = a;
-    }
-    float g = 0.0f;
-    if (p.Is > 0)
-      for (int ks = 0; ks < p.KS; ++ks) g += ld_cg_f32(rp + kE * p.KS + ks);
-    int id[8];
-    float w[8];
-    const bool ok = select_top8_regs(v, lane, id, w);
-    if (lane < 8) {
-      int myid = id[0];
-      float myw = w[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i)
-        if (lane == i) { myid = id[i]; myw = w[i]; }
-      S.ids[t][lane] = myid;
-      S.wts[t][lane] = myw;
-      if (out_cta) {
-        if (p.ids_out) p.ids_out[t * kK + lane] = myid;
-        if (p.weights_out) p.weights_out[t * kK + lane] = myw;
-      }
-    }
-    if (lane == 0) {
-      S.sg[t] = p.Is > 0 ? sigmoidf_(g) : 0.0f;
-      if (out_cta && p.gate_logit_out && p.Is > 0) p.gate_logit_out[t] = g;
-      if (out_cta && !ok) set_status(p.status, MOE_DEV_NONFINITE);
-    }
-    if (out_cta && p.logits_out) {
-      float4 *dst = reinterpret_cast<float4 *>(p.logits_out + static_cast<size_t>(t) * kE + 8 * lane);
-      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  for (int ks = 0; ks < kFusedMaxH / 512; ++ks) {  // all loads in flight at once
+    if (ks < p.KS) {
+      const float4 *row = reinterpret_cast<const float4 *>(rp + ks * kRP + 8 * lane);
+      a0[ks] = __ldcg(row);
+      a1[ks] = __ldcg(row + 1);
+      gp[ks] = p.Is > 0 ? ld_cg_f32(rp + ks * kRP + kE) : 0.0f;
     }
   }
-  const int tid = threadIdx.x;  // consumer threads 0 .. 511
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float g = 0.0f;
+#pragma unroll
+  for (int ks = 0; ks < kFusedMaxH / 512; ++ks) {  // fixed K-slice order
+    if (ks < p.KS) {
+      v[0] += a0[ks].x; v[1] += a0[ks].y; v[2] += a0[ks].z; v[3] += a0[ks].w;
+      v[4] += a1[ks].x; v[5] += a1[ks].y; v[6] += a1[ks].z; v[7] += a1[ks].w;
+      g += gp[ks];
+    }
+  }
+  int id[8];
+  float w[8];
+  const bool ok = select_top8_regs(v, lane, id, w);
+  if (lane < 8) {
+    int myid = id[0];
+    float myw = w[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+      if (lane == i) { myid = id[i]; myw = w[i]; }
+    p.sel_ids[t * kK + lane] = myid;
+    p.sel_w[t * kK + lane] = myw;
+    if (p.ids_out) p.ids_out[t * kK + lane] = myid;
+    if (p.weights_out) p.weights_out[t * kK + lane] = myw;
+  }
+  if (lane == 0) {
+    p.sel_sg[t] = p.Is > 0 ? sigmoidf_(g) : 0.0f;
+    if (p.gate_logit_out && p.Is > 0) p.gate_logit_out[t] = g;
+    if (!ok) set_status(p.status, MOE_DEV_NONFINITE);
+  }
+  if (p.logits_out) {
+    float4 *dst = reinterpret_cast<float4 *>(p.logits_out + static_cast<size_t>(t) * kE + 8 * lane);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+// Phase S2 (every CTA): read the selection of every token and build the
+// token -> expert lists in shared memory.
+__device__ __forceinline__ void phase_lists(FusedSmem &S, const FusedParams &p, int cwarp,
+                                            int lane) {
+  const int tid = threadIdx.x;  // consumer threads
+  for (int i = tid; i < p.T * kK; i += kFConsumers) {
+    S.ids[i / kK][i % kK] = __ldcg(p.sel_ids + i);
+    S.wts[i / kK][i % kK] = __ldcg(p.sel_w + i);
+  }
+  for (int t = tid; t < p.T; t += kFConsumers) S.sg[t] = __ldcg(p.sel_sg + t);
   if (tid < kE) {
     S.counts[tid] = 0;
     S.mask[tid] = 0ull;
@@ -362,7 +393,7 @@ __device__ __forceinline__ void phase_select(FusedSmem &S, const FusedParams &p,
       if (lane >= o) { incl += n1; act += n2; }
     }
     if (lane == 31) S.scan_tmp[cwarp] = incl | (act << 20);
-    ptx::named_barrier(6, kE);  // ids 2..5 belong to the quads
+    ptx::named_barrier(6, kE);  // ids 2..4 belong to the quads
     int base = 0, abase = 0;
     for (int w2 = 0; w2 < cwarp; ++w2) {
       base += S.scan_tmp[w2] & 0xFFFFF;
@@ -390,69 +421,110 @@ __device__ __forceinline__ void phase_select(FusedSmem &S, const FusedParams &p,
   ptx::named_barrier(1, kFConsumers);
 }
 
-// B fragments of one 64-wide K slice for up to two n8 token tiles: lane
-// (g, c) reads 16 consecutive bf16 of its token's row at k0 + 16c.
-__device__ __forceinline__ void load_b(const moe_bf16 *const (&brow)[2], int ntiles, int k0,
-                                       int c, bool cg, uint32_t (&xw)[2][8]) {
+// One 64-wide K slice of a 16-row unit against one n8 token tile: A rows g
+// and g+8 from the staged rows (int8 -> bf16 in registers), B fragments xw.
+// Logical k (2c, 2c+1 | 2c+8, 2c+9) of MMA jj maps to physical k
+// 16c + 4jj + (0, 1 | 2, 3) for A and B alike.
+__device__ __forceinline__ void mma_slice(const uint8_t *rows, int stride, int k0, int g, int c,
+                                          const uint32_t (&xw)[8], float (&part)[4]) {
+  const uint4 qa = *reinterpret_cast<const uint4 *>(rows + g * stride + k0 + 16 * c);
+  const uint4 qb = *reinterpret_cast<const uint4 *>(rows + (g + 8) * stride + k0 + 16 * c);
+  const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    if (nt < ntiles && brow[nt]) {
-      const moe_bf16 *src = brow[nt] + k0 + 16 * c;
-      const uint4 x0 = cg ? ld_cg16(src) : ld_nc(src);
-      const uint4 x1 = cg ? ld_cg16(src + 8) : ld_nc(src + 8);
-      xw[nt][0] = x0.x; xw[nt][1] = x0.y; xw[nt][2] = x0.z; xw[nt][3] = x0.w;
-      xw[nt][4] = x1.x; xw[nt][5] = x1.y; xw[nt][6] = x1.z; xw[nt][7] = x1.w;
+  for (int jj = 0; jj < 4; ++jj) {
+    // bytes 4jj..4jj+3 of rows g and g+8, converted just before their MMA
+    const f4 fa = i8x4_to_f32(wa[jj]), fb = i8x4_to_f32(wb[jj]);
+    const uint32_t a0 = __byte_perm(__float_as_uint(fa.x), __float_as_uint(fa.y), 0x7632);
+    const uint32_t a2 = __byte_perm(__float_as_uint(fa.z), __float_as_uint(fa.w), 0x7632);
+    const uint32_t a1 = __byte_perm(__float_as_uint(fb.x), __float_as_uint(fb.y), 0x7632);
+    const uint32_t a3 = __byte_perm(__float_as_uint(fb.z), __float_as_uint(fb.w), 0x7632);
+    mma16816(part, a0, a1, a2, a3, xw[2 * jj], xw[2 * jj + 1]);
+  }
+}
+
+// Activation fragments of up to eight 64-wide slices starting at kb for
+// this lane's token row (zeros without a token).
+__device__ __forceinline__ void load_x8(const moe_bf16 *brow, int kb, int ns, int c,
+                                        uint32_t (&xw)[8][8]) {
+#pragma unroll
+  for (int sl = 0; sl < 8; ++sl) {
+    if (brow && sl < ns) {
+      const moe_bf16 *src = brow + kb + 64 * sl + 16 * c;
+      const uint4 x0 = ld_nc(src), x1 = ld_nc(src + 8);
+      xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
+      xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) xw[nt][i] = 0u;
+      for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
     }
   }
 }
 
-// One 64-wide K slice of a 16-row unit against up to two n8 token tiles:
-// A rows g and g+8 from the staged rows (int8 -> bf16 in registers).
-// Logical k (2c, 2c+1 | 2c+8, 2c+9) of MMA jj maps to physical k
-// 16c + 4jj + (0, 1 | 2, 3) for A and B alike.
-__device__ __forceinline__ void mma_slice(const uint8_t *rows, int stride, int k0, int ntiles,
-                                          int g, int c, const uint32_t (&xw)[2][8],
-                                          float (&part)[2][4]) {
-  const uint4 qa = *reinterpret_cast<const uint4 *>(rows + g * stride + k0 + 16 * c);
-  const uint4 qb = *reinterpret_cast<const uint4 *>(rows + (g + 8) * stride + k0 + 16 * c);
-  uint32_t a[8], b[8];
-  i8x16_to_bf16(qa, a);
-  i8x16_to_bf16(qb, b);
+// ns (<= 8) slices from kb (a multiple of 128) of a 16-row unit for one n8
+// tile with the B
+// fragments in xw; each slice's partial sums are promoted with its group's
+// scales (lo: rows 0..7, hi: rows 8..15).
+__device__ __forceinline__ void gemm_x8(const uint8_t *rows, int stride, int kb, int ns, int g,
+                                        int c, const uint32_t (&xw)[8][8],
+                                        const moe_bf16 *s_lo, const moe_bf16 *s_hi,
+                                        float (&acc)[4]) {
+  // kb is a multiple of 128: slices 2gi and 2gi+1 form group kb/128 + gi
+  float slo[4], shi[4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    if (nt >= ntiles) break;
+  for (int gi = 0; gi < 4; ++gi)
+    if (2 * gi < ns) {
+      slo[gi] = bf16_to_f32(s_lo[kb / kG + gi]);
+      shi[gi] = bf16_to_f32(s_hi[kb / kG + gi]);
+    }
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-      mma16816(part[nt], a[2 * jj], b[2 * jj], a[2 * jj + 1], b[2 * jj + 1], xw[nt][2 * jj],
-               xw[nt][2 * jj + 1]);
+  for (int sl = 0; sl < 8; ++sl) {
+    if (sl >= ns) break;
+    const int gi = sl >> 1;
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_slice(rows, stride, kb + 64 * sl, g, c, xw[sl], part);
+    acc[0] = fmaf(slo[gi], part[0], acc[0]);
+    acc[1] = fmaf(slo[gi], part[1], acc[1]);
+    acc[2] = fmaf(shi[gi], part[2], acc[2]);
+    acc[3] = fmaf(shi[gi], part[3], acc[3]);
   }
 }
 
-// The K range [kb, kb + kn) of a 16-row unit in 128-wide groups (two
-// slices each), B fragments fetched one slice ahead; partial sums of each
-// group are promoted with the rows' group scales (lo: rows 0..7, hi: 8..15).
+// The K range [kb, kb + kn) (a multiple of 64) of a 16-row unit for one n8
+// token tile.  The B fragments of up to eight slices (512 of K) are fetched
+// together before their MMAs, so each batch pays one memory latency; each
+// slice's partial sums are promoted with its group's scales (lo: rows 0..7,
+// hi: rows 8..15).  brow = this lane's token row or NULL.
 __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int kb, int kn,
-                                          const moe_bf16 *const (&brow)[2], int ntiles, int g,
-                                          int c, bool cg, const moe_bf16 *s_lo,
-                                          const moe_bf16 *s_hi, float (&acc)[2][4]) {
-  uint32_t xa[2][8], xb[2][8];
-  load_b(brow, ntiles, kb, c, cg, xa);
-  for (int kg = kb; kg < kb + kn; kg += kG) {
-    float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    load_b(brow, ntiles, kg + 64, c, cg, xb);
-    const float slo = bf16_to_f32(s_lo[kg / kG]), shi = bf16_to_f32(s_hi[kg / kG]);
-    mma_slice(rows, stride, kg, ntiles, g, c, xa, part);
-    if (kg + kG < kb + kn) load_b(brow, ntiles, kg + kG, c, cg, xa);
-    mma_slice(rows, stride, kg + 64, ntiles, g, c, xb, part);
+                                          const moe_bf16 *brow, int g, int c, bool cg,
+                                          const moe_bf16 *s_lo, const moe_bf16 *s_hi,
+                                          float (&acc)[4]) {
+  for (int kk = kb; kk < kb + kn; kk += 512) {
+    const int ns = min(8, (kb + kn - kk) / 64);
+    uint32_t xw[8][8];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      acc[nt][0] = fmaf(slo, part[nt][0], acc[nt][0]);
-      acc[nt][1] = fmaf(slo, part[nt][1], acc[nt][1]);
-      acc[nt][2] = fmaf(shi, part[nt][2], acc[nt][2]);
-      acc[nt][3] = fmaf(shi, part[nt][3], acc[nt][3]);
+    for (int sl = 0; sl < 8; ++sl) {
+      if (brow && sl < ns) {
+        const moe_bf16 *src = brow + kk + 64 * sl + 16 * c;
+        const uint4 x0 = cg ? ld_cg16(src) : ld_nc(src);
+        const uint4 x1 = cg ? ld_cg16(src + 8) : ld_nc(src + 8);
+        xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
+        xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
+      }
+    }
+#pragma unroll
+    for (int sl = 0; sl < 8; ++sl) {
+      if (sl >= ns) break;
+      const int k0 = kk + 64 * sl;
+      const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_slice(rows, stride, k0, g, c, xw[sl], part);
+      acc[0] = fmaf(slo, part[0], acc[0]);
+      acc[1] = fmaf(slo, part[1], acc[1]);
+      acc[2] = fmaf(shi, part[2], acc[2]);
+      acc[3] = fmaf(shi, part[3], acc[3]);
     }
   }
 }
@@ -460,11 +532,12 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 // Phase W consumer: gate|up unit j of this CTA, by quad q (warp wq of 4
 // takes K quarter wq).
 __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, const Work &wk,
-                                           int j, int q, int wq, int lane, uint64_t budget) {
+                                           int j, int q, int wq, int lane, uint64_t budget,
+                                           uint32_t (&xc)[8][8], int &xc_e) {
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
   int e, i0;
-  gu_unit(S, wk, blockIdx.x + j * gridDim.x, e, i0);
+  gu_unit(S, wk, j, e, i0);
   const bool sh = e == kE;
   const int half = sh ? p.Is : p.I;
   const int n_tok = sh ? p.T : S.counts[e];
@@ -476,7 +549,7 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
   const moe_bf16 *s_up = sbase + static_cast<size_t>(half + i0 + g) * ng;
   const int kq = p.H / 4, kb = wq * kq;
   const uint8_t *rows = S.ring[s];
-  const int stride = p.H + kFRowPad;
+  const int stride = p.H;
   for (int tb = 0; tb < n_tok; tb += kFPass) {
     const int ntiles = min(2, (n_tok - tb + 7) / 8);
     const moe_bf16 *brow[2];
@@ -490,7 +563,17 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
       }
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    unit_gemm(rows, stride, kb, kq, brow, ntiles, g, c, false, s_gate, s_up, acc);
+    const int ns = kq / 64;  // <= 8 since H <= 2048
+    for (int nt = 0; nt < ntiles; ++nt) {
+      // a routed expert with <= 8 tokens keeps its activation fragments in
+      // registers (xc) across its consecutive units
+      const bool cacheable = !sh && n_tok <= 8;
+      if (!cacheable || xc_e != e) {
+        load_x8(brow[nt], kb, ns, c, xc);
+        xc_e = cacheable ? e : -1;
+      }
+      gemm_x8(rows, stride, kb, ns, g, c, xc, s_gate, s_up, acc[nt]);
+    }
     // reduce the four K quarters in a fixed order, then SwiGLU
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -530,8 +613,6 @@ __device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p,
   const int u0 = k * wk.units_per_stage;
   const int nu = min(wk.units_per_stage, wk.n_down_units - u0);
   const int g = lane >> 2, c = lane & 3;
-  const int imax = p.I > p.Is ? p.I : p.Is;
-  const int ys_ld = p.T * (kK + 1);
   for (int u = wq; u < nu; u += 4) {
     const int e = down_unit(S, p, u0 + u);
     const bool sh = e == kE;
@@ -555,7 +636,8 @@ __device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p,
                         : p.h_routed + static_cast<size_t>(p0 + idx) * p.I;
       }
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      unit_gemm(rows, imax + kFRowPad, 0, Ii, brow, ntiles, g, c, true, s_lo, s_hi, acc);
+      for (int nt = 0; nt < ntiles; ++nt)
+        unit_gemm(rows, Ii, 0, Ii, brow[nt], g, c, true, s_lo, s_hi, acc[nt]);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -569,7 +651,6 @@ __device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p,
         }
     }
   }
-  (void)ys_ld;
   __syncwarp();
   if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
 }
@@ -620,7 +701,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     int issued = early ? 1 : 0;
     for (int j = issued; j < wk.n_local && !aborted(S); ++j, ++issued) {
       int e, i0;
-      gu_unit(S, wk, blockIdx.x + j * gridDim.x, e, i0);
+      gu_unit(S, wk, j, e, i0);
       produce_gu(S, p, j, e, i0, pol, budget, lane);
     }
     for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k, ++issued)
@@ -638,10 +719,15 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     const int q = warp >> 2, wq = warp & 3;
     phase_router(p, warp, lane);
     grid_sync(p.grid_bar, S, budget);
-    phase_select(S, p, warp, lane);
+    phase_select(p, warp, lane);
+    grid_sync(p.grid_bar, S, budget);
+    phase_lists(S, p, warp, lane);
     if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
-    for (int j = q; j < wk.n_local; j += kFQuads) consume_gu(S, p, wk, j, q, wq, lane, budget);
+    uint32_t xc[8][8];
+    int xc_e = -1;
+    for (int j = q; j < wk.n_local; j += kFQuads)
+      consume_gu(S, p, wk, j, q, wq, lane, budget, xc, xc_e);
     grid_sync(p.grid_bar, S, budget);
     for (int k = q; k < wk.n_down_stages; k += kFQuads)
       consume_down(S, p, wk, k, wq, lane, budget);
@@ -674,7 +760,7 @@ unsigned long long fused_wait_budget_ns() {
 size_t fused_smem_bytes() { return sizeof(FusedSmem); }
 
 bool fused_decode_supported(int T, int H, int I, int Is) {
-  if (T < 1 || T > kFusedMaxT || H > kFusedMaxH || H % 256 != 0) return false;
+  if (T < 1 || T > kFusedMaxT || H > kFusedMaxH || H % 512 != 0) return false;
   if (I > kFusedMaxI || Is > kFusedMaxI || I % 128 != 0 || Is % 128 != 0) return false;
   static int sms[64] = {0};
   int dev = 0;
@@ -697,16 +783,18 @@ bool fused_decode_supported(int T, int H, int I, int Is) {
 }
 
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
-                                const moe_weights &w, float *rpart, moe_bf16 *h_routed,
+                                const moe_weights &w, float *rpart, int32_t *sel_ids,
+                                float *sel_w, float *sel_sg, moe_bf16 *h_routed,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, cudaStream_t s) {
   FusedParams p{};
-  p.x = x; p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 256;
+  p.x = x; p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 512;
   p.w_router = w.w_router; p.w_gate = Is > 0 ? w.w_shared_gate : nullptr;
   p.w13_q = w.w13_q; p.w13_s = w.w13_s; p.w2_q = w.w2_q; p.w2_s = w.w2_s;
   p.ws13_q = w.ws13_q; p.ws13_s = w.ws13_s; p.ws2_q = w.ws2_q; p.ws2_s = w.ws2_s;
-  p.rpart = rpart; p.h_routed = h_routed; p.h_shared = h_shared; p.out = out;
+  p.rpart = rpart; p.sel_ids = sel_ids; p.sel_w = sel_w; p.sel_sg = sel_sg;
+  p.h_routed = h_routed; p.h_shared = h_shared; p.out = out;
   p.ids_out = ids_out; p.weights_out = weights_out; p.logits_out = logits_out;
   p.gate_logit_out = gate_logit_out; p.status = status; p.grid_bar = grid_bar;
   p.budget_ns = fused_wait_budget_ns();

@@ -53,7 +53,7 @@ cudaError_t launch_combine(int T, int H, const float *y, const float *weights,
 // ---- decode-size T: the fused persistent kernel (decode_fused.cu)
 
 constexpr int kFusedMaxT = 64;    // tokens
-constexpr int kFusedMaxH = 2048;  // hidden (multiple of 256)
+constexpr int kFusedMaxH = 2048;  // hidden (multiple of 512)
 constexpr int kFusedMaxI = 2048;  // expert / shared intermediate
 
 // Whether the fused kernel runs these sizes on the current device (one CTA
@@ -61,11 +61,13 @@ constexpr int kFusedMaxI = 2048;  // expert / shared intermediate
 bool fused_decode_supported(int T, int H, int I, int Is);
 size_t fused_smem_bytes();
 
-// A1..A7 in one cooperative launch.  rpart [T][257][H/256] fp32 scratch,
-// h_routed [T*K][I], h_shared [T][Is]; grid_bar is a 32-bit counter that must
-// be zero before the first launch (it restores itself after each launch).
+// A1..A7 in one cooperative launch.  rpart [T][H/512][260] fp32, sel_ids
+// [T][K], sel_w [T][K], sel_sg [T] scratch, h_routed [T*K][I], h_shared
+// [T][Is]; grid_bar is a 32-bit counter whose low 31 bits must be zero
+// before the first launch (each grid barrier leaves them unchanged).
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
-                                const moe_weights &w, float *rpart, moe_bf16 *h_routed,
+                                const moe_weights &w, float *rpart, int32_t *sel_ids,
+                                float *sel_w, float *sel_sg, moe_bf16 *h_routed,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, cudaStream_t s);
