@@ -46,6 +46,7 @@ constexpr int kFConsumers = kFConsumerWarps * 32;
 constexpr int kFThreads = kFConsumers + 32;  // + one producer warp
 constexpr int kFStages = 5;
 constexpr int kFStageBytes = 16 * kFusedMaxH;  // one gate|up unit, or packed down units
+constexpr int kFScaleBytes = 512;              // the group scales of a stage's rows
 constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
 constexpr int kRP = 260;                     // router partial row: 257 used, 16-byte rows
 
@@ -77,6 +78,7 @@ struct FusedParams {
 
 struct FusedSmem {
   uint8_t ring[kFStages][kFStageBytes];
+  uint8_t ring_s[kFStages][kFScaleBytes];  // bf16 scales of each stage's rows
   union {
     float red[kFQuads][4][2][32][4];         // gate|up: quad reduction
     float ys[16][kFusedMaxT * (kK + 1)];     // down: y of this CTA's 16 rows
@@ -172,6 +174,7 @@ struct Work {
   int n0;              // first output row of this CTA in the down phase (-1: none)
   int n_down_units;    // shared expert + active experts (0 if n0 < 0)
   int unit_stride;     // bytes of one down unit (16 rows) in a ring stage
+  int scale_stride;    // bytes of one down unit's scales in the stage's scale area
   int units_per_stage;
   int n_down_stages;
 };
@@ -213,6 +216,7 @@ __device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams 
   wk.n_down_units = wk.n0 >= 0 ? (p.Is > 0 ? 1 : 0) + n_active : 0;
   const int imax = p.I > p.Is ? p.I : p.Is;
   wk.unit_stride = 16 * imax;
+  wk.scale_stride = 2 * 16 * (imax / kG);
   wk.units_per_stage = kFStageBytes / wk.unit_stride;
   wk.n_down_stages = (wk.n_down_units + wk.units_per_stage - 1) / wk.units_per_stage;
   return wk;
@@ -225,18 +229,26 @@ __device__ __forceinline__ void produce_gu(FusedSmem &S, const FusedParams &p, i
   const int s = j % kFStages;
   if (lane == 0) {
     fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
-    if (!aborted(S)) ptx::mbar_expect_tx(&S.full[s], 16u * p.H);
+    if (!aborted(S)) ptx::mbar_expect_tx(&S.full[s], 16u * p.H + 2u * 8 * 2 * (p.H / kG));
   }
   __syncwarp();
   if (aborted(S)) return;
-  if (lane < 2) {
-    // 8 consecutive gate rows (lane 0) or up rows (lane 1): one contiguous
-    // copy of 8 * H bytes each (bulk copies of >= 8 KB stream at full rate)
+  if (lane < 4) {
+    // lanes 0/1: 8 consecutive gate / up rows, one contiguous copy of 8 * H
+    // bytes each (bulk copies of >= 8 KB stream at full rate); lanes 2/3:
+    // the bf16 group scales of those rows (8 * H/128 each)
     const int half = e == kE ? p.Is : p.I;
-    const int row = lane == 0 ? i0 : half + i0;
-    const int8_t *src = e == kE ? p.ws13_q + static_cast<size_t>(row) * p.H
-                                : p.w13_q + (static_cast<size_t>(e) * 2 * p.I + row) * p.H;
-    bulk_g2s(S.ring[s] + lane * 8 * p.H, src, 8u * p.H, &S.full[s], pol);
+    const int ng = p.H / kG;
+    const int row = (lane & 1) == 0 ? i0 : half + i0;
+    if (lane < 2) {
+      const int8_t *src = e == kE ? p.ws13_q + static_cast<size_t>(row) * p.H
+                                  : p.w13_q + (static_cast<size_t>(e) * 2 * p.I + row) * p.H;
+      bulk_g2s(S.ring[s] + lane * 8 * p.H, src, 8u * p.H, &S.full[s], pol);
+    } else {
+      const moe_bf16 *src = e == kE ? p.ws13_s + static_cast<size_t>(row) * ng
+                                    : p.w13_s + (static_cast<size_t>(e) * 2 * p.I + row) * ng;
+      bulk_g2s(S.ring_s[s] + (lane - 2) * 8 * ng * 2, src, 2u * 8 * ng, &S.full[s], pol);
+    }
   }
   __syncwarp();
 }
@@ -251,18 +263,30 @@ __device__ __forceinline__ void produce_down(FusedSmem &S, const FusedParams &p,
   if (lane == 0) {
     fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
     uint32_t tx = 0;
-    for (int u = 0; u < nu; ++u) tx += 16u * (down_unit(S, p, u0 + u) == kE ? p.Is : p.I);
+    for (int u = 0; u < nu; ++u) {
+      const int Ii = down_unit(S, p, u0 + u) == kE ? p.Is : p.I;
+      tx += 16u * Ii + 2u * 16 * (Ii / kG);
+    }
     if (!aborted(S)) ptx::mbar_expect_tx(&S.full[s], tx);
   }
   __syncwarp();
   if (aborted(S)) return;
-  if (lane < nu) {
-    // one contiguous copy of the unit's 16 rows (16 * Ii bytes)
-    const int e = down_unit(S, p, u0 + lane);
+  if (lane < 2 * nu) {
+    // lane u < nu: one contiguous copy of unit u's 16 rows (16 * Ii bytes);
+    // lane nu + u: their group scales (16 * Ii/128 bf16) into the scale area
+    const int u = lane < nu ? lane : lane - nu;
+    const int e = down_unit(S, p, u0 + u);
     const int Ii = e == kE ? p.Is : p.I;
-    const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(wk.n0) * p.Is
-                                : p.w2_q + (static_cast<size_t>(e) * p.H + wk.n0) * p.I;
-    bulk_g2s(S.ring[s] + lane * wk.unit_stride, src, 16u * Ii, &S.full[s], pol);
+    if (lane < nu) {
+      const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(wk.n0) * p.Is
+                                  : p.w2_q + (static_cast<size_t>(e) * p.H + wk.n0) * p.I;
+      bulk_g2s(S.ring[s] + u * wk.unit_stride, src, 16u * Ii, &S.full[s], pol);
+    } else {
+      const int ng = Ii / kG;
+      const moe_bf16 *src = e == kE ? p.ws2_s + static_cast<size_t>(wk.n0) * ng
+                                    : p.w2_s + (static_cast<size_t>(e) * p.H + wk.n0) * ng;
+      bulk_g2s(S.ring_s[s] + u * wk.scale_stride, src, 2u * 16 * ng, &S.full[s], pol);
+    }
   }
   __syncwarp();
 }
@@ -539,14 +563,13 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
   int e, i0;
   gu_unit(S, wk, j, e, i0);
   const bool sh = e == kE;
-  const int half = sh ? p.Is : p.I;
   const int n_tok = sh ? p.T : S.counts[e];
   const int p0 = sh ? 0 : S.offsets[e];
   const int g = lane >> 2, c = lane & 3;
   const int ng = p.H / kG;
-  const moe_bf16 *sbase = sh ? p.ws13_s : p.w13_s + static_cast<size_t>(e) * 2 * p.I * ng;
-  const moe_bf16 *s_gate = sbase + static_cast<size_t>(i0 + g) * ng;
-  const moe_bf16 *s_up = sbase + static_cast<size_t>(half + i0 + g) * ng;
+  // the stage's scale area holds the 8 gate rows' then the 8 up rows' scales
+  const moe_bf16 *s_gate = reinterpret_cast<const moe_bf16 *>(S.ring_s[s]) + g * ng;
+  const moe_bf16 *s_up = reinterpret_cast<const moe_bf16 *>(S.ring_s[s]) + (8 + g) * ng;
   const int kq = p.H / 4, kb = wq * kq;
   const uint8_t *rows = S.ring[s];
   const int stride = p.H;
@@ -620,9 +643,9 @@ __device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p,
     const int ng = Ii / kG;
     const int n_tok = sh ? p.T : S.counts[e];
     const int p0 = sh ? 0 : S.offsets[e];
-    const moe_bf16 *sbase = sh ? p.ws2_s : p.w2_s + static_cast<size_t>(e) * p.H * ng;
-    const moe_bf16 *s_lo = sbase + static_cast<size_t>(wk.n0 + g) * ng;
-    const moe_bf16 *s_hi = sbase + static_cast<size_t>(wk.n0 + g + 8) * ng;
+    const moe_bf16 *sbase = reinterpret_cast<const moe_bf16 *>(S.ring_s[s] + u * wk.scale_stride);
+    const moe_bf16 *s_lo = sbase + g * ng;
+    const moe_bf16 *s_hi = sbase + (g + 8) * ng;
     const uint8_t *rows = S.ring[s] + u * wk.unit_stride;
     for (int tb = 0; tb < n_tok; tb += kFPass) {
       const int ntiles = min(2, (n_tok - tb + 7) / 8);
