@@ -80,7 +80,7 @@ struct FusedSmem {
   uint8_t ring[kFStages][kFStageBytes];
   uint8_t ring_s[kFStages][kFScaleBytes];  // bf16 scales of each stage's rows
   union {
-    float red[kFQuads][4][2][32][4];         // gate|up: quad reduction
+    float red[kFQuads][2][4][2][32][4];      // gate|up: quad reduction, 2 buffers
     float ys[16][kFusedMaxT * (kK + 1)];     // down: y of this CTA's 16 rows
   } u;
   int32_t ids[kFusedMaxT][kK];
@@ -94,6 +94,7 @@ struct FusedSmem {
   unsigned long long mask[kE];
   int scan_tmp[8];
   uint64_t full[kFStages], empty[kFStages], routed;
+  uint64_t red_full[kFQuads][2], red_empty[kFQuads][2];
   int abort;
 };
 
@@ -557,7 +558,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 // takes K quarter wq).
 __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, const Work &wk,
                                            int j, int q, int wq, int lane, uint64_t budget,
-                                           uint32_t (&xc)[8][8], int &xc_e) {
+                                           uint32_t (&xc)[8][8], int &xc_e, uint32_t &npass) {
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
   int e, i0;
@@ -597,33 +598,47 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
       }
       gemm_x8(rows, stride, kb, ns, g, c, xc, s_gate, s_up, acc[nt]);
     }
-    // reduce the four K quarters in a fixed order, then SwiGLU
+    if (tb + kFPass >= n_tok) {  // the stage's rows are no longer needed
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+    }
+    // Hand the four K quarters to this pass's reducing warp (it rotates over
+    // the quad) through a double-buffered exchange; only the reducer waits.
+    const uint32_t u = npass++;
+    const int b = u & 1;
+    fwait(&S.red_empty[q][b], ((u >> 1) & 1) ^ 1, S, budget);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) S.u.red[q][wq][nt][lane][i] = acc[nt][i];
-    ptx::named_barrier(2 + q, 128);
-    if (wq < ntiles) {
-      const int nt = wq;
-      float r4[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int i = 0; i < 4; ++i) S.u.red[q][b][wq][nt][lane][i] = acc[nt][i];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.red_full[q][b]);
+    if (wq == static_cast<int>(u & 3)) {
+      fwait(&S.red_full[q][b], (u >> 1) & 1, S, budget);
+      for (int nt = 0; nt < ntiles; ++nt) {
+        float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int w2 = 0; w2 < 4; ++w2)
+        for (int w2 = 0; w2 < 4; ++w2)  // fixed order
 #pragma unroll
-        for (int i = 0; i < 4; ++i) r4[i] += S.u.red[q][w2][nt][lane][i];
+          for (int i = 0; i < 4; ++i) r4[i] += S.u.red[q][b][w2][nt][lane][i];
 #pragma unroll
-      for (int col = 0; col < 2; ++col) {
-        const int idx = tb + 8 * nt + 2 * c + col;
-        if (idx < n_tok) {
-          const uint16_t hv = f32_to_bf16(silu_mul(r4[col], r4[2 + col]));
-          if (sh) p.h_shared[static_cast<size_t>(idx) * p.Is + i0 + g] = hv;
-          else p.h_routed[static_cast<size_t>(p0 + idx) * p.I + i0 + g] = hv;
+        for (int col = 0; col < 2; ++col) {
+          const int idx = tb + 8 * nt + 2 * c + col;
+          if (idx < n_tok) {
+            const uint16_t hv = f32_to_bf16(silu_mul(r4[col], r4[2 + col]));
+            if (sh) p.h_shared[static_cast<size_t>(idx) * p.Is + i0 + g] = hv;
+            else p.h_routed[static_cast<size_t>(p0 + idx) * p.I + i0 + g] = hv;
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.red_empty[q][b]);
     }
-    ptx::named_barrier(2 + q, 128);
   }
-  __syncwarp();
-  if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+  if (n_tok == 0) {
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+  }
 }
 
 // Phase D consumer: down stage k (units k*U ..), by quad q; warp wq takes
@@ -707,6 +722,11 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       ptx::mbar_init(&S.empty[s], 4);  // the four warps of the consuming quad
     }
     ptx::mbar_init(&S.routed, 1);
+    for (int q = 0; q < kFQuads; ++q)
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(&S.red_full[q][b], 4);   // the quad's four warps
+        ptx::mbar_init(&S.red_empty[q][b], 1);  // the pass's reducing warp
+      }
     S.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -749,8 +769,9 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     const Work wk = make_work(S, p);
     uint32_t xc[8][8];
     int xc_e = -1;
+    uint32_t npass = 0;
     for (int j = q; j < wk.n_local; j += kFQuads)
-      consume_gu(S, p, wk, j, q, wq, lane, budget, xc, xc_e);
+      consume_gu(S, p, wk, j, q, wq, lane, budget, xc, xc_e, npass);
     grid_sync(p.grid_bar, S, budget);
     for (int k = q; k < wk.n_down_stages; k += kFQuads)
       consume_down(S, p, wk, k, wq, lane, budget);
