@@ -56,7 +56,7 @@ size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 struct Layout {
   size_t status, logits, gate_logit, ids, weights, sgate;
   size_t counts, offsets, active, perm, slot_of;
-  size_t h_routed, h_shared, y, rpart, xstage, ostage;
+  size_t h_routed, h_shared, y, rpart, x16, xscale, xstage, ostage;
   size_t xs, acc, items, counters, total;
 };
 
@@ -108,7 +108,11 @@ Layout layout(const moe_dims *d, int T) {
   L.h_shared = take(2 * t * (Is ? Is : 1));
   const Route r = route_of(d, T);
   if (r == kRouteGemv) L.y = take(4 * t * (kK + 1) * H);
-  if (r == kRouteFused) L.rpart = take(4 * t * 260 * (H / 512));
+  if (r == kRouteFused) {
+    L.rpart = take(4 * t * 260 * (H / 512));
+    L.x16 = take(2 * t * H);
+    L.xscale = take(4 * t);
+  }
   L.xstage = take(2 * t * H);
   L.ostage = take(2 * t * H);
   if (r == kRouteTc) {
@@ -190,7 +194,8 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   if (route == kRouteFused) {
     if (!fused_decode_supported(T, H, I, Is)) return MOE_ERR_UNSUPPORTED;
     unsigned *grid_bar = reinterpret_cast<unsigned *>(at<uint8_t>(ws, L.status) + 4);
-    MOE_TRY(launch_decode_fused(x, T, H, I, Is, *w, at<float>(ws, L.rpart),
+    MOE_TRY(launch_decode_fused(x, T, H, I, Is, *w, at<uint16_t>(ws, L.x16),
+                                at<float>(ws, L.xscale), at<float>(ws, L.rpart),
                                 at<int32_t>(ws, L.ids), at<float>(ws, L.weights),
                                 at<float>(ws, L.sgate), hr, hs, out, ids_out, weights_out,
                                 logits_out, gate_logit_out, status, grid_bar, s));

@@ -30,6 +30,7 @@
 // weights.  Every wait (mbarrier, grid barrier) is bounded by a %globaltimer
 // budget; a wait that gives up sets MOE_DEV_TIMEOUT and the kernel runs to
 // its end without waiting again.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -40,7 +41,7 @@
 namespace moe {
 namespace {
 
-constexpr int kFQuads = 3;   // 13 warps: at most 4 per SM sub-partition, 128 registers
+constexpr int kFQuads = 3;  // 13 warps: at most 4 per SM sub-partition, 128 registers
 constexpr int kFConsumerWarps = 4 * kFQuads;
 constexpr int kFConsumers = kFConsumerWarps * 32;
 constexpr int kFThreads = kFConsumers + 32;  // + one producer warp
@@ -52,6 +53,8 @@ constexpr int kRP = 260;                     // router partial row: 257 used, 16
 
 struct FusedParams {
   const moe_bf16 *x;
+  uint16_t *x16;        // [T][H] fp16: x * 2^-xexp[t], exact (see phase_router)
+  float *xscale;        // [T] 2^xexp[t]
   int T, H, I, Is, KS;  // KS = H / 512 router K-slices
   const moe_bf16 *w_router, *w_gate;
   const int8_t *w13_q;
@@ -86,6 +89,7 @@ struct FusedSmem {
   int32_t ids[kFusedMaxT][kK];
   float wts[kFusedMaxT][kK];
   float sg[kFusedMaxT];
+  float xs[kFusedMaxT];
   int32_t slot_of[kFusedMaxT][kK];
   int32_t perm[kFusedMaxT * kK];
   int32_t counts[kE];
@@ -107,6 +111,27 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k16, f16 inputs, fp32 accumulate (register fragments).
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                             uint32_t a2, uint32_t a3, uint32_t b0,
+                                             uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 4 int8 -> two f16x2, exact: each byte in offset binary (q + 128) becomes
+// the low mantissa byte of 1024.0 (f16 0x6400 | u), and 1152 = 1024 + 128 is
+// subtracted from both halves.  lo = bytes 0,1; hi = bytes 2,3.
+__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140);
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
 }
 
 // 1-D bulk copy global -> shared completing on an mbarrier, L2 evict-first.
@@ -295,6 +320,47 @@ __device__ __forceinline__ void produce_down(FusedSmem &S, const FusedParams &p,
 // Phase R: router partials.  Task (r, ks): one warp dots row r (256 expert
 // rows, row 256 = shared gate) over K-slice ks (512 wide) with every token.
 __device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, int lane) {
+  // Token scaling for the fp16 tensor-core path: warp gw < T writes token gw
+  // as x * 2^-s in fp16 with s = exponent(max |x_t|) - 14, so the largest
+  // magnitude lands in [2^14, 2^15).  A bf16 value (8 significant bits) is
+  // exact in fp16 whenever the scaled value is a normal fp16, i.e. for every
+  // element within 2^29 of the token's largest; smaller ones are off by less
+  // than 2^-40 of that largest.  2^s is undone on the fp32 results.
+  {
+    const int gw = blockIdx.x * kFConsumerWarps + cwarp;
+    if (gw < p.T) {
+      const moe_bf16 *xr = p.x + static_cast<size_t>(gw) * p.H;
+      float m = 0.0f;
+      for (int k = lane * 8; k < p.H; k += 256) {
+        const uint4 v = ld_nc(xr + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      int sexp = 0;
+      if (m > 0.0f && isfinite(m)) {
+        sexp = static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14;
+        sexp = max(-110, min(110, sexp));
+      }
+      const float down = __uint_as_float(static_cast<uint32_t>(127 - sexp) << 23);  // 2^-s
+      for (int k = lane * 8; k < p.H; k += 256) {
+        const uint4 v = ld_nc(xr + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 h = __floats2half2_rn(bf16_lo(w[i]) * down, bf16_hi(w[i]) * down);
+          o[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        *reinterpret_cast<uint4 *>(p.x16 + static_cast<size_t>(gw) * p.H + k) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if (lane == 0) p.xscale[gw] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
+    }
+  }
   const int rows = kE + (p.Is > 0 ? 1 : 0);
   const int n_tasks = rows * p.KS;
   for (int task = blockIdx.x * kFConsumerWarps + cwarp; task < n_tasks;
@@ -393,7 +459,10 @@ __device__ __forceinline__ void phase_lists(FusedSmem &S, const FusedParams &p, 
     S.ids[i / kK][i % kK] = __ldcg(p.sel_ids + i);
     S.wts[i / kK][i % kK] = __ldcg(p.sel_w + i);
   }
-  for (int t = tid; t < p.T; t += kFConsumers) S.sg[t] = __ldcg(p.sel_sg + t);
+  for (int t = tid; t < p.T; t += kFConsumers) {
+    S.sg[t] = __ldcg(p.sel_sg + t);
+    S.xs[t] = __ldcg(p.xscale + t);
+  }
   if (tid < kE) {
     S.counts[tid] = 0;
     S.mask[tid] = 0ull;
@@ -467,67 +536,37 @@ __device__ __forceinline__ void mma_slice(const uint8_t *rows, int stride, int k
   }
 }
 
-// Activation fragments of up to eight 64-wide slices starting at kb for
-// this lane's token row (zeros without a token).
-__device__ __forceinline__ void load_x8(const moe_bf16 *brow, int kb, int ns, int c,
-                                        uint32_t (&xw)[8][8]) {
+// As mma_slice with f16 operands: the int8 rows convert exactly to f16 and
+// the B fragments hold the token's scaled fp16 activations.
+__device__ __forceinline__ void mma_slice_f16(const uint8_t *rows, int stride, int k0, int g,
+                                              int c, const uint32_t (&xw)[8],
+                                              float (&part)[4]) {
+  const uint4 qa = *reinterpret_cast<const uint4 *>(rows + g * stride + k0 + 16 * c);
+  const uint4 qb = *reinterpret_cast<const uint4 *>(rows + (g + 8) * stride + k0 + 16 * c);
+  const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-  for (int sl = 0; sl < 8; ++sl) {
-    if (brow && sl < ns) {
-      const moe_bf16 *src = brow + kb + 64 * sl + 16 * c;
-      const uint4 x0 = ld_nc(src), x1 = ld_nc(src + 8);
-      xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
-      xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
-    }
-  }
-}
-
-// ns (<= 8) slices from kb (a multiple of 128) of a 16-row unit for one n8
-// tile with the B
-// fragments in xw; each slice's partial sums are promoted with its group's
-// scales (lo: rows 0..7, hi: rows 8..15).
-__device__ __forceinline__ void gemm_x8(const uint8_t *rows, int stride, int kb, int ns, int g,
-                                        int c, const uint32_t (&xw)[8][8],
-                                        const moe_bf16 *s_lo, const moe_bf16 *s_hi,
-                                        float (&acc)[4]) {
-  // kb is a multiple of 128: slices 2gi and 2gi+1 form group kb/128 + gi
-  float slo[4], shi[4];
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi)
-    if (2 * gi < ns) {
-      slo[gi] = bf16_to_f32(s_lo[kb / kG + gi]);
-      shi[gi] = bf16_to_f32(s_hi[kb / kG + gi]);
-    }
-#pragma unroll
-  for (int sl = 0; sl < 8; ++sl) {
-    if (sl >= ns) break;
-    const int gi = sl >> 1;
-    float part[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_slice(rows, stride, kb + 64 * sl, g, c, xw[sl], part);
-    acc[0] = fmaf(slo[gi], part[0], acc[0]);
-    acc[1] = fmaf(slo[gi], part[1], acc[1]);
-    acc[2] = fmaf(shi[gi], part[2], acc[2]);
-    acc[3] = fmaf(shi[gi], part[3], acc[3]);
+  for (int jj = 0; jj < 4; ++jj) {
+    uint32_t a0, a1, a2, a3;
+    i8x4_to_f16x2(wa[jj], a0, a2);
+    i8x4_to_f16x2(wb[jj], a1, a3);
+    mma16816_f16(part, a0, a1, a2, a3, xw[2 * jj], xw[2 * jj + 1]);
   }
 }
 
 // The K range [kb, kb + kn) (a multiple of 64) of a 16-row unit for one n8
-// token tile.  The B fragments of up to eight slices (512 of K) are fetched
-// together before their MMAs, so each batch pays one memory latency; each
-// slice's partial sums are promoted with its group's scales (lo: rows 0..7,
-// hi: rows 8..15).  brow = this lane's token row or NULL.
+// token tile, bf16 operands.  The B fragments of up to four slices (256 of
+// K) are fetched together before their MMAs, so each batch pays one memory
+// latency; each slice's partial sums are promoted with its group's scales
+// (lo: rows 0..7, hi: rows 8..15).  brow = this lane's token row or NULL.
 __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int kb, int kn,
                                           const moe_bf16 *brow, int g, int c, bool cg,
                                           const moe_bf16 *s_lo, const moe_bf16 *s_hi,
                                           float (&acc)[4]) {
-  for (int kk = kb; kk < kb + kn; kk += 512) {
-    const int ns = min(8, (kb + kn - kk) / 64);
-    uint32_t xw[8][8];
+  for (int kk = kb; kk < kb + kn; kk += 256) {
+    const int ns = min(4, (kb + kn - kk) / 64);
+    uint32_t xw[4][8];
 #pragma unroll
-    for (int sl = 0; sl < 8; ++sl) {
+    for (int sl = 0; sl < 4; ++sl) {
       if (brow && sl < ns) {
         const moe_bf16 *src = brow + kk + 64 * sl + 16 * c;
         const uint4 x0 = cg ? ld_cg16(src) : ld_nc(src);
@@ -540,7 +579,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
       }
     }
 #pragma unroll
-    for (int sl = 0; sl < 8; ++sl) {
+    for (int sl = 0; sl < 4; ++sl) {
       if (sl >= ns) break;
       const int k0 = kk + 64 * sl;
       const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
@@ -558,7 +597,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 // takes K quarter wq).
 __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, const Work &wk,
                                            int j, int q, int wq, int lane, uint64_t budget,
-                                           uint32_t (&xc)[8][8], int &xc_e, uint32_t &npass) {
+                                           uint32_t &npass) {
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
   int e, i0;
@@ -583,20 +622,41 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
       brow[nt] = nullptr;
       if (idx < n_tok) {
         const int t = sh ? idx : S.perm[p0 + idx] / kK;
-        brow[nt] = p.x + static_cast<size_t>(t) * p.H;
+        brow[nt] = reinterpret_cast<const moe_bf16 *>(p.x16) + static_cast<size_t>(t) * p.H;
       }
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const int ns = kq / 64;  // <= 8 since H <= 2048
     for (int nt = 0; nt < ntiles; ++nt) {
-      // a routed expert with <= 8 tokens keeps its activation fragments in
-      // registers (xc) across its consecutive units
-      const bool cacheable = !sh && n_tok <= 8;
-      if (!cacheable || xc_e != e) {
-        load_x8(brow[nt], kb, ns, c, xc);
-        xc_e = cacheable ? e : -1;
+      for (int kk = kb; kk < kb + kq; kk += 256) {  // batches of 4 slices (2 groups)
+        const int ns4 = min(4, (kb + kq - kk) / 64);
+        uint32_t xw[4][8];
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+          if (brow[nt] && sl < ns4) {  // fp16 rows written earlier in this launch
+            const moe_bf16 *src = brow[nt] + kk + 64 * sl + 16 * c;
+            const uint4 x0 = ld_cg16(src), x1 = ld_cg16(src + 8);
+            xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
+            xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
+          }
+        }
+        const float slo0 = bf16_to_f32(s_gate[kk / kG]), shi0 = bf16_to_f32(s_up[kk / kG]);
+        const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[kk / kG + 1]) : 0.0f;
+        const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[kk / kG + 1]) : 0.0f;
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+          if (sl >= ns4) break;
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part);
+          const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
+          acc[nt][0] = fmaf(slo, part[0], acc[nt][0]);
+          acc[nt][1] = fmaf(slo, part[1], acc[nt][1]);
+          acc[nt][2] = fmaf(shi, part[2], acc[nt][2]);
+          acc[nt][3] = fmaf(shi, part[3], acc[nt][3]);
+        }
       }
-      gemm_x8(rows, stride, kb, ns, g, c, xc, s_gate, s_up, acc[nt]);
     }
     if (tb + kFPass >= n_tok) {  // the stage's rows are no longer needed
       __syncwarp();
@@ -625,7 +685,8 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
         for (int col = 0; col < 2; ++col) {
           const int idx = tb + 8 * nt + 2 * c + col;
           if (idx < n_tok) {
-            const uint16_t hv = f32_to_bf16(silu_mul(r4[col], r4[2 + col]));
+            const float xsv = S.xs[sh ? idx : S.perm[p0 + idx] / kK];  // undo 2^-s
+            const uint16_t hv = f32_to_bf16(silu_mul(r4[col] * xsv, r4[2 + col] * xsv));
             if (sh) p.h_shared[static_cast<size_t>(idx) * p.Is + i0 + g] = hv;
             else p.h_routed[static_cast<size_t>(p0 + idx) * p.I + i0 + g] = hv;
           }
@@ -767,11 +828,9 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     phase_lists(S, p, warp, lane);
     if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
-    uint32_t xc[8][8];
-    int xc_e = -1;
     uint32_t npass = 0;
     for (int j = q; j < wk.n_local; j += kFQuads)
-      consume_gu(S, p, wk, j, q, wq, lane, budget, xc, xc_e, npass);
+      consume_gu(S, p, wk, j, q, wq, lane, budget, npass);
     grid_sync(p.grid_bar, S, budget);
     for (int k = q; k < wk.n_down_stages; k += kFQuads)
       consume_down(S, p, wk, k, wq, lane, budget);
@@ -827,13 +886,15 @@ bool fused_decode_supported(int T, int H, int I, int Is) {
 }
 
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
-                                const moe_weights &w, float *rpart, int32_t *sel_ids,
+                                const moe_weights &w, uint16_t *x16, float *xscale,
+                                float *rpart, int32_t *sel_ids,
                                 float *sel_w, float *sel_sg, moe_bf16 *h_routed,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, cudaStream_t s) {
   FusedParams p{};
-  p.x = x; p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 512;
+  p.x = x; p.x16 = x16; p.xscale = xscale;
+  p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 512;
   p.w_router = w.w_router; p.w_gate = Is > 0 ? w.w_shared_gate : nullptr;
   p.w13_q = w.w13_q; p.w13_s = w.w13_s; p.w2_q = w.w2_q; p.w2_s = w.w2_s;
   p.ws13_q = w.ws13_q; p.ws13_s = w.ws13_s; p.ws2_q = w.ws2_q; p.ws2_s = w.ws2_s;
