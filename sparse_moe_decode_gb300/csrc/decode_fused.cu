@@ -235,8 +235,17 @@ __device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams 
   const int R = n_active * wk.nIb;  // routed units in the grid
   const int c = blockIdx.x, G = gridDim.x;
   wk.has_shared = c < wk.nSb ? 1 : 0;
-  wk.r_begin = static_cast<int>((static_cast<long long>(R) * c) / G);
-  const int r_end = static_cast<int>((static_cast<long long>(R) * (c + 1)) / G);
+  // Balance by cost: a shared unit weighs its token tiles (T/8), a routed
+  // unit about one; CTA c's routed range starts at its cost prefix minus the
+  // shared units before it.
+  const long long ws = (p.T + 7) / 8;
+  const long long total = R + static_cast<long long>(wk.nSb) * ws;
+  auto start = [&](int cc) {
+    const long long v = total * cc / G - ws * min(cc, wk.nSb);
+    return static_cast<int>(v < 0 ? 0 : (v > R ? R : v));
+  };
+  wk.r_begin = start(c);
+  const int r_end = c + 1 == G ? R : max(wk.r_begin, start(c + 1));
   wk.n_local = wk.has_shared + (r_end - wk.r_begin);
   wk.n0 = 16 * static_cast<int>(blockIdx.x) < p.H ? 16 * static_cast<int>(blockIdx.x) : -1;
   wk.n_down_units = wk.n0 >= 0 ? (p.Is > 0 ? 1 : 0) + n_active : 0;
@@ -554,7 +563,7 @@ __device__ __forceinline__ void mma_slice_f16(const uint8_t *rows, int stride, i
 }
 
 // The K range [kb, kb + kn) (a multiple of 64) of a 16-row unit for one n8
-// token tile, bf16 operands.  The B fragments of up to four slices (256 of
+// token tile, bf16 operands.  The B fragments of up to eight slices (512 of
 // K) are fetched together before their MMAs, so each batch pays one memory
 // latency; each slice's partial sums are promoted with its group's scales
 // (lo: rows 0..7, hi: rows 8..15).  brow = this lane's token row or NULL.
@@ -562,11 +571,11 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
                                           const moe_bf16 *brow, int g, int c, bool cg,
                                           const moe_bf16 *s_lo, const moe_bf16 *s_hi,
                                           float (&acc)[4]) {
-  for (int kk = kb; kk < kb + kn; kk += 256) {
-    const int ns = min(4, (kb + kn - kk) / 64);
-    uint32_t xw[4][8];
+  for (int kk = kb; kk < kb + kn; kk += 512) {
+    const int ns = min(8, (kb + kn - kk) / 64);
+    uint32_t xw[8][8];
 #pragma unroll
-    for (int sl = 0; sl < 4; ++sl) {
+    for (int sl = 0; sl < 8; ++sl) {
       if (brow && sl < ns) {
         const moe_bf16 *src = brow + kk + 64 * sl + 16 * c;
         const uint4 x0 = cg ? ld_cg16(src) : ld_nc(src);
@@ -579,7 +588,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
       }
     }
 #pragma unroll
-    for (int sl = 0; sl < 4; ++sl) {
+    for (int sl = 0; sl < 8; ++sl) {
       if (sl >= ns) break;
       const int k0 = kk + 64 * sl;
       const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
@@ -597,7 +606,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 // takes K quarter wq).
 __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, const Work &wk,
                                            int j, int q, int wq, int lane, uint64_t budget,
-                                           uint32_t &npass) {
+                                           uint32_t &npass, uint32_t (&xc)[8][8], int &xc_e) {
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
   int e, i0;
@@ -626,36 +635,38 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
       }
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const int ns = kq / 64;  // <= 8 since H <= 2048
     for (int nt = 0; nt < ntiles; ++nt) {
-      for (int kk = kb; kk < kb + kq; kk += 256) {  // batches of 4 slices (2 groups)
-        const int ns4 = min(4, (kb + kq - kk) / 64);
-        uint32_t xw[4][8];
+      // The warp's activation fragments for its K quarter (8 slices, 64
+      // registers).  A routed expert with <= 8 tokens keeps them across its
+      // consecutive units (one expert spans many units of a CTA).
+      const bool cacheable = !sh && n_tok <= 8;
+      if (!cacheable || xc_e != e) {
 #pragma unroll
-        for (int sl = 0; sl < 4; ++sl) {
-          if (brow[nt] && sl < ns4) {  // fp16 rows written earlier in this launch
-            const moe_bf16 *src = brow[nt] + kk + 64 * sl + 16 * c;
+        for (int sl = 0; sl < 8; ++sl) {
+          if (brow[nt] && sl < ns) {  // fp16 rows written earlier in this launch
+            const moe_bf16 *src = brow[nt] + kb + 64 * sl + 16 * c;
             const uint4 x0 = ld_cg16(src), x1 = ld_cg16(src + 8);
-            xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
-            xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
+            xc[sl][0] = x0.x; xc[sl][1] = x0.y; xc[sl][2] = x0.z; xc[sl][3] = x0.w;
+            xc[sl][4] = x1.x; xc[sl][5] = x1.y; xc[sl][6] = x1.z; xc[sl][7] = x1.w;
           } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
+            for (int i = 0; i < 8; ++i) xc[sl][i] = 0u;
           }
         }
-        const float slo0 = bf16_to_f32(s_gate[kk / kG]), shi0 = bf16_to_f32(s_up[kk / kG]);
-        const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[kk / kG + 1]) : 0.0f;
-        const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[kk / kG + 1]) : 0.0f;
+        xc_e = cacheable ? e : -1;
+      }
 #pragma unroll
-        for (int sl = 0; sl < 4; ++sl) {
-          if (sl >= ns4) break;
-          float part[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part);
-          const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
-          acc[nt][0] = fmaf(slo, part[0], acc[nt][0]);
-          acc[nt][1] = fmaf(slo, part[1], acc[nt][1]);
-          acc[nt][2] = fmaf(shi, part[2], acc[nt][2]);
-          acc[nt][3] = fmaf(shi, part[3], acc[nt][3]);
-        }
+      for (int sl = 0; sl < 8; ++sl) {
+        if (sl >= ns) break;
+        const int k0 = kb + 64 * sl;  // kb is a multiple of 128
+        const float slo = bf16_to_f32(s_gate[k0 / kG]), shi = bf16_to_f32(s_up[k0 / kG]);
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_slice_f16(rows, stride, k0, g, c, xc[sl], part);
+        acc[nt][0] = fmaf(slo, part[0], acc[nt][0]);
+        acc[nt][1] = fmaf(slo, part[1], acc[nt][1]);
+        acc[nt][2] = fmaf(shi, part[2], acc[nt][2]);
+        acc[nt][3] = fmaf(shi, part[3], acc[nt][3]);
       }
     }
     if (tb + kFPass >= n_tok) {  // the stage's rows are no longer needed
@@ -829,8 +840,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
     uint32_t npass = 0;
+    uint32_t xc[8][8];
+    int xc_e = -1;
     for (int j = q; j < wk.n_local; j += kFQuads)
-      consume_gu(S, p, wk, j, q, wq, lane, budget, npass);
+      consume_gu(S, p, wk, j, q, wq, lane, budget, npass, xc, xc_e);
     grid_sync(p.grid_bar, S, budget);
     for (int k = q; k < wk.n_down_stages; k += kFQuads)
       consume_down(S, p, wk, k, wq, lane, budget);
@@ -882,7 +895,9 @@ bool fused_decode_supported(int T, int H, int I, int Is) {
       sms[dev] = device_sms();
     }
   }
-  return sms[dev] > 0 && sms[dev] * 16 >= H;
+  // the SMs must cover the H / 16 output-row blocks and the Is / 8 shared
+  // gate|up units (one per CTA)
+  return sms[dev] > 0 && sms[dev] * 16 >= H && sms[dev] * 8 >= Is;
 }
 
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
