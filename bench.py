@@ -129,6 +129,25 @@ def gateup_bytes(d: W.Dims, T: int, n_active: int):
     return n_active * per + sh + 2 * T * H + 2 * (T * 8 * I + T * Is)
 
 
+def down_bytes(d: W.Dims, T: int, n_active: int):
+    """Down projection + combine: each routed expert's down weights + scales
+    once, the shared expert's, the h rows in, the bf16 output out."""
+    H, I, Is, G = d.H, d.I, d.Is, d.G
+    per = H * I + 2 * H * (I // G)
+    sh = H * Is + 2 * H * (Is // G) if Is else 0
+    return n_active * per + sh + 2 * (T * 8 * I + T * Is) + 2 * T * H
+
+
+def kernel_bytes(kname: str, d: W.Dims, T: int, n_active: int):
+    """Algorithmic bytes of one launch of a block kernel, None for kernels
+    that run the whole block (the block's bytes apply)."""
+    if kname in ("gateup_swiglu", "gateup_swiglu_tc"):
+        return gateup_bytes(d, T, n_active)
+    if kname in ("down", "down_combine_tc"):
+        return down_bytes(d, T, n_active)
+    return None
+
+
 def algorithmic_flops(d: W.Dims, T: int):
     H, I, Is = d.H, d.I, d.Is
     return 2 * T * (8 * 3 * I * H + 3 * Is * H + 256 * H + H)
@@ -399,7 +418,7 @@ def main():
             "banks": banks,
         }
         if name == args.workload:
-            kb = gateup_bytes(d, T, n_act) if b.kernel_names[k_dom] == "gateup_swiglu" else None
+            kb = kernel_bytes(b.kernel_names[k_dom], d, T, n_act)
             r["_kernel"] = (b.kernel_names[k_dom], per_kernel[k_dom], kb)
             e2e_s, bi, bo = b.e2e(args.steps, args.warmup)
             e2e_s = max_all(e2e_s)

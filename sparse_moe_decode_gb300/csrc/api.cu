@@ -108,8 +108,8 @@ Layout layout(const moe_dims *d, int T) {
   L.h_shared = take(2 * t * (Is ? Is : 1));
   const Route r = route_of(d, T);
   if (r == kRouteGemv) L.y = take(4 * t * (kK + 1) * H);
-  if (r == kRouteFused) {
-    L.rpart = take(4 * t * 260 * (H / 512));
+  if (r == kRouteFused) L.rpart = take(4 * t * 260 * (H / 512));
+  if (r == kRouteFused || r == kRouteTc) {
     L.x16 = take(2 * t * H);
     L.xscale = take(4 * t);
   }
@@ -158,9 +158,9 @@ const char *const kStageNames[] = {"router_gemv", "select_top8", "expert_lists",
 constexpr int kStages = 6;
 const char *const kFusedStageNames[] = {"decode_fused"};
 const char *const kTcStageNames[] = {"router_tc", "router_gate_gemv", "select_top8",
-                                     "expert_lists", "build_items", "gather_rows", "zero_acc",
-                                     "gateup_swiglu_tc", "down_combine_tc", "acc_to_bf16"};
-constexpr int kTcStages = 10;
+                                     "lists_items", "scale_gather", "gateup_swiglu_tc",
+                                     "down_combine_tc", "acc_to_bf16"};
+constexpr int kTcStages = 8;
 
 // Records `ev[i]` after kernel i-1 when profiling (ev[0] before the first).
 struct Rec : StageRecorder {
@@ -230,10 +230,9 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   MOE_TRY(launch_select(logits, T, kE, wg ? glog : nullptr, ids, wts, wg ? sg : nullptr,
                         status, s));
   MOE_TRY(rec());
-  MOE_TRY(launch_lists(ids, T, lists, status, s));
-  MOE_TRY(rec());
-  MOE_TRY(launch_experts_tc(x, T, H, I, Is, *w, lists, lists.perm, wts, wg ? sg : nullptr,
-                            at<moe_bf16>(ws, L.xs), hr, hs, at<float>(ws, L.acc), out, items,
+  MOE_TRY(launch_experts_tc(x, T, H, I, Is, *w, ids, lists, wts, wg ? sg : nullptr,
+                            at<uint16_t>(ws, L.xs), at<uint16_t>(ws, L.x16),
+                            at<float>(ws, L.xscale), hr, hs, at<float>(ws, L.acc), out, items,
                             counters, status, s, rec));
   return MOE_OK;
 }

@@ -54,12 +54,42 @@ __device__ __forceinline__ f4 i8x4_to_f32(uint32_t w) {
   return r;
 }
 
+// 4 int8 -> two f16x2, exact: each byte in offset binary (q + 128) becomes
+// the low mantissa byte of 1024.0 (f16 0x6400 | u), and 1152 = 1024 + 128 is
+// subtracted from both halves.  lo = bytes 0,1; hi = bytes 2,3.
+__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140);
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
 // ----------------------------------------------------------- warp helpers
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   return v;
+}
+
+// Exclusive prefix sum over threads 0..255 of the block (all threads of the
+// block call it; tmp holds >= 8 ints of shared memory).
+__device__ __forceinline__ int block_exclusive_scan_256(int v, int *tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (threadIdx.x < 256 && lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  if (threadIdx.x < 256)
+    for (int w = 0; w < warp; ++w) base += tmp[w];
+  __syncthreads();
+  return base + incl - v;
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {

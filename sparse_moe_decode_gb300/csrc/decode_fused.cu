@@ -123,17 +123,6 @@ __device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 4 int8 -> two f16x2, exact: each byte in offset binary (q + 128) becomes
-// the low mantissa byte of 1024.0 (f16 0x6400 | u), and 1152 = 1024 + 128 is
-// subtracted from both halves.  lo = bytes 0,1; hi = bytes 2,3.
-__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  lo = __byte_perm(u, 0x64646464u, 0x4140);
-  hi = __byte_perm(u, 0x64646464u, 0x4342);
-  asm("sub.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
-  asm("sub.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
-}
-
 // 1-D bulk copy global -> shared completing on an mbarrier, L2 evict-first.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
                                          uint64_t *bar, uint64_t policy) {

@@ -1,6 +1,7 @@
 // kernels.h -- host-side launchers of the sm_103a kernels (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -74,7 +75,15 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, cudaStream_t s);
 
-// ---- prefill-size T: tcgen05 grouped GEMMs (tc_gemm.cu)
+// ---- prefill-size T: tcgen05 GEMMs (tc_gemm.cu: router; tc_expert.cu: experts)
+
+// 2-D row-major tensor [rows][cols] of `esize`-byte elements, box
+// [box_rows][box_cols], 128-byte swizzle, zero fill out of bounds.
+bool tc_make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
+                 uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols);
+int tc_sm_count();
+// Budget of every bounded wait in the tcgen05 kernels (MOE_WAIT_BUDGET_NS, default 2 s).
+unsigned long long tc_wait_budget_ns();
 
 // Bytes of the work-item lists for T tokens.
 size_t tc_items_bytes(int T, int I, int Is, int H);
@@ -84,12 +93,16 @@ size_t tc_items_bytes(int T, int I, int Is, int H);
 cudaError_t launch_router_tc(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
                              float *logits, uint32_t *status, cudaStream_t s);
 
-// A4..A7 for prefill-size T: gathers each expert's tokens (xs [T*K][H]),
-// runs gate|up + SwiGLU and down + weighted combine as grouped tcgen05 GEMMs
-// into out_acc [T][H] (fp32, zeroed here), then rounds out_acc to bf16.
+// A3..A7 for prefill-size T: builds the token -> expert lists of ids [T][K]
+// into L (counts, offsets, perm, slot_of; not active) with the work items,
+// the tokens' scaled fp16 copies (xs16 [T*K][H] in list order, x16 [T][H],
+// xscale [T]), runs gate|up + SwiGLU and down + weighted combine as grouped
+// tcgen05 GEMMs into out_acc [T][H] (fp32, zeroed here), then rounds out_acc
+// to bf16.
 cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
-                              const moe_weights &w, const Lists &L, const int32_t *perm,
-                              const float *weights, const float *sgate, moe_bf16 *xs,
+                              const moe_weights &w, const int32_t *ids, const Lists &L,
+                              const float *weights,
+                              const float *sgate, uint16_t *xs16, uint16_t *x16, float *xscale,
                               moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
                               moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
                               cudaStream_t s, StageRecorder &rec);

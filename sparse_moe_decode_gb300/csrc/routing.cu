@@ -54,10 +54,37 @@ router_gemv_kernel(const moe_bf16 *__restrict__ x, int T, int H,
   }
 }
 
+// The shared-expert gate row alone: one warp per token, the same lane
+// order and fp32 summation as the router kernel above.
+__global__ void __launch_bounds__(kRouterWarps * 32)
+gate_gemv_kernel(const moe_bf16 *__restrict__ x, int T, int H,
+                 const moe_bf16 *__restrict__ w_gate, float *__restrict__ gate_logit) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const moe_bf16 *xr = x + static_cast<size_t>(t) * H;
+  float a = 0.0f;
+  for (int k = lane * 8; k < H; k += 256) {
+    const uint4 wv = ld_nc(w_gate + k), xv = ld_nc(xr + k);
+    a = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), a); a = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), a);
+    a = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), a); a = fmaf(bf16_hi(wv.y), bf16_hi(xv.y), a);
+    a = fmaf(bf16_lo(wv.z), bf16_lo(xv.z), a); a = fmaf(bf16_hi(wv.z), bf16_hi(xv.z), a);
+    a = fmaf(bf16_lo(wv.w), bf16_lo(xv.w), a); a = fmaf(bf16_hi(wv.w), bf16_hi(xv.w), a);
+  }
+  a = warp_sum(a);
+  if (lane == 0) gate_logit[t] = a;
+}
+
 cudaError_t launch_router_gemv(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
                                const moe_bf16 *w_gate, float *logits, float *gate_logit,
                                cudaStream_t s, bool gate_only) {
-  const int row_begin = gate_only ? kE : 0;
+  if (gate_only) {
+    if (!w_gate || !gate_logit) return cudaSuccess;
+    gate_gemv_kernel<<<(T + kRouterWarps - 1) / kRouterWarps, kRouterWarps * 32, 0, s>>>(
+        x, T, H, w_gate, gate_logit);
+    return cudaGetLastError();
+  }
+  const int row_begin = 0;
   const int rows = kE + (w_gate && gate_logit ? 1 : 0) - row_begin;
   if (rows <= 0) return cudaSuccess;
   dim3 grid((rows + kRouterWarps - 1) / kRouterWarps, (T + kRouterTok - 1) / kRouterTok);
@@ -114,25 +141,9 @@ constexpr int kListThreads = 1024;
 constexpr int kListChunk = 2048;               // tokens per chunk
 constexpr int kListWords = kListChunk / 32;    // bitmap words per expert
 constexpr size_t kListSmem = sizeof(uint32_t) * kE * kListWords +   // bitmap
-                             sizeof(uint16_t) * kE * kListWords;    // word prefixes
-
-__device__ __forceinline__ int block_exclusive_scan_256(int v, int *tmp) {
-  // threads 0..255 participate with v; returns exclusive prefix; tmp >= 8 ints
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (threadIdx.x < 256 && lane == 31) tmp[warp] = incl;
-  __syncthreads();
-  int base = 0;
-  if (threadIdx.x < 256)
-    for (int w = 0; w < warp; ++w) base += tmp[w];
-  __syncthreads();
-  return base + incl - v;
-}
+                             sizeof(uint16_t) * kE * kListWords +   // word prefixes
+                             sizeof(int16_t) * kListChunk * kK;     // the chunk's ids
+constexpr int kListBatch = 8;  // independent loads in flight per thread
 
 __global__ void __launch_bounds__(kListThreads)
 lists_kernel(const int32_t *__restrict__ ids, int T, Lists L, uint32_t *status) {
@@ -140,15 +151,27 @@ lists_kernel(const int32_t *__restrict__ ids, int T, Lists L, uint32_t *status) 
   uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem);
   uint16_t *wpre = reinterpret_cast<uint16_t *>(smem + sizeof(uint32_t) * kE * kListWords);
   __shared__ int cnt[kE], base[kE], run[kE], scan_tmp[8];
+  int16_t *cids = reinterpret_cast<int16_t *>(smem + (sizeof(uint32_t) + sizeof(uint16_t)) *
+                                                          kE * kListWords);
   const int tid = threadIdx.x;
   const int n = T * kK;
   if (tid < kE) { cnt[tid] = 0; run[tid] = 0; }
   __syncthreads();
+  // Loads are batched (kListBatch per thread in flight) so that one CTA
+  // streams the ids at bandwidth rather than at one latency per entry.
   bool bad = false;
-  for (int i = tid; i < n; i += kListThreads) {
-    const int e = ids[i];
-    if (e >= kE) bad = true;
-    else if (e >= 0) atomicAdd(&cnt[e], 1);
+  for (int i0 = 0; i0 < n; i0 += kListThreads * kListBatch) {
+    int e[kListBatch];
+#pragma unroll
+    for (int u = 0; u < kListBatch; ++u) {
+      const int i = i0 + u * kListThreads + tid;
+      e[u] = i < n ? ids[i] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kListBatch; ++u) {
+      if (e[u] >= kE) bad = true;
+      else if (e[u] >= 0) atomicAdd(&cnt[e[u]], 1);
+    }
   }
   if (bad) set_status(status, MOE_DEV_BAD_EXPERT);
   __syncthreads();
@@ -169,10 +192,23 @@ lists_kernel(const int32_t *__restrict__ ids, int T, Lists L, uint32_t *status) 
     const int words = (tn + 31) / 32;
     for (int i = tid; i < kE * kListWords; i += kListThreads) bitmap[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < tn * kK; i += kListThreads) {
-      const int e = ids[static_cast<size_t>(t0) * kK + i];
-      const int tl = i / kK;
-      if (e >= 0 && e < kE) atomicOr(&bitmap[e * kListWords + tl / 32], 1u << (tl & 31));
+    for (int i0 = 0; i0 < tn * kK; i0 += kListThreads * kListBatch) {
+      int e[kListBatch];
+#pragma unroll
+      for (int u = 0; u < kListBatch; ++u) {
+        const int i = i0 + u * kListThreads + tid;
+        e[u] = i < tn * kK ? ids[static_cast<size_t>(t0) * kK + i] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kListBatch; ++u) {
+        const int i = i0 + u * kListThreads + tid;
+        if (i < tn * kK) {
+          const int ev = (e[u] >= 0 && e[u] < kE) ? e[u] : -1;  // out of range -> no slot
+          cids[i] = static_cast<int16_t>(ev);
+          const int tl = i / kK;
+          if (ev >= 0) atomicOr(&bitmap[ev * kListWords + tl / 32], 1u << (tl & 31));
+        }
+      }
     }
     __syncthreads();
     // per-expert exclusive prefix of popcounts over the chunk's words
@@ -194,8 +230,8 @@ lists_kernel(const int32_t *__restrict__ ids, int T, Lists L, uint32_t *status) 
     __syncthreads();
     for (int i = tid; i < tn * kK; i += kListThreads) {
       const size_t gi = static_cast<size_t>(t0) * kK + i;
-      const int e = ids[gi];
-      if (e < 0 || e >= kE) {
+      const int e = cids[i];
+      if (e < 0) {
         if (L.slot_of) L.slot_of[gi] = -1;
         continue;
       }

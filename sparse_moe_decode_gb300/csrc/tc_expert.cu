@@ -1,0 +1,791 @@
+// tc_expert.cu -- prefill-size T: the expert SwiGLU (gate|up, A4/A6) and the
+// down projection with the weighted combine (A5/A6/A7) as grouped GEMMs on
+// the 5th-generation tensor cores, with the dequantised weight operand held
+// in tensor memory.
+//
+// Orientation: D[row, token] = sum_k W[row, k] * X[token, k].  128 weight
+// rows are the M operand (one TMEM lane each), the tokens of one expert tile
+// are N (<= 128): each weight tile is streamed from HBM once for all of its
+// expert's tokens.
+//
+// Per 128-wide K group (one quantisation group):
+//   TMA         int8 tile 128 x 128 (128-byte swizzle) -> shared ring Q
+//   converters  Q row -> exact fp16 (gate|up) or bf16 (down) -> TMEM A stage
+//               (tcgen05.st; |q| <= 127 is exact in either type)
+//   TMA         activation tile N x 128 -> shared ring B
+//   MMA thread  P = A[TMEM] x B[smem]^T into one of three TMEM partial buffers
+//   promoters   acc[row][token] += s[row][group] * P (fp32 registers)
+// so the product q * s is never rounded ("scale promotion").  The gate|up
+// activations are each token's copy scaled by a power of two into fp16
+// (exact for every element within 2^29 of the token's largest), undone on the
+// fp32 results; the down activations h are bf16 as the SwiGLU rounds them.
+//
+// Warp roles (512 threads): warp 0 issues the weight TMA loads, warp 2 the
+// activation TMA loads (two producers, so that the weight ring runs ahead on
+// its own depth), warps 1 and 15 issue the MMAs of the even and the odd K
+// groups (one issuing thread sustains only about one MMA instruction per
+// hundred cycles, so two double the tensor rate at these N), warp 1 also
+// owns TMEM, warps 3..6 convert (one per TMEM lane quarter), warps 7..14
+// promote and run the epilogue (two per lane quarter, splitting the token
+// columns).  Every wait is bounded by a %globaltimer budget; on expiry
+// the CTA drains what it has in flight, frees TMEM, sets MOE_DEV_TIMEOUT and
+// returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kXThreads = 512;
+constexpr int kMma1 = 15;                  // second MMA issuing warp
+constexpr int kConv0 = 3;                  // first converter warp
+constexpr int kConv = 4;                   // converter warps
+constexpr int kProm = 8;                   // promoter warps
+constexpr int kXQS = 6, kXBS = 3;          // shared-memory ring depths
+constexpr int kXAS = 2;                    // TMEM A stages
+constexpr int kXPS = 3;                    // TMEM partial buffers
+constexpr int kXBRows = 32;                // rows per activation TMA box
+constexpr uint32_t kXQBytes = 128 * 128;   // int8 weight tile
+constexpr uint32_t kXBBytes = 2 * 128 * 128;  // 16-bit activation tile (<= 128 rows), two K halves
+constexpr uint32_t kXXchBytes = 128 * 64 * 4;  // gate|up exchange of the up rows
+constexpr uint32_t kXTmemCols = 512;       // A stages [0, 128), partials at 128, 256, 384
+constexpr uint32_t kXColP = kXAS * 64;
+static_assert(kXColP + kXPS * 128 <= kXTmemCols, "tensor memory columns");
+
+constexpr size_t kXOffQ = 0;
+constexpr size_t kXOffB = kXOffQ + kXQS * kXQBytes;
+constexpr size_t kXOffX = kXOffB + kXBS * kXBBytes;
+constexpr size_t kXOffBar = kXOffX + kXXchBytes;
+constexpr size_t kXSmem = kXOffBar + 512 + 1024;  // + barriers + alignment slack
+static_assert(kXSmem <= 232448, "shared memory per CTA");
+
+enum XMode : int { kXGateUp = 0, kXDown = 1 };
+
+struct XBars {
+  uint64_t q_full[kXQS], q_empty[kXQS], a_full[kXAS], a_empty[kXAS], b_full[kXBS],
+      b_empty[kXBS];
+  uint64_t p_full[kXPS], p_empty[kXPS], done[2], xch_full, xch_empty;
+  uint32_t tmem_holder;
+  int abort;
+};
+static_assert(sizeof(XBars) <= 512, "barrier block");
+
+struct XParams {
+  const int4 *items;                  // {expert (kE = shared), m tile, first B row, n}
+  const int *n_items;
+  int K_routed, K_shared;             // reduction lengths
+  int rows_routed, rows_shared;       // gate|up: I and Is; down: H for both
+  const moe_bf16 *s_routed, *s_shared;  // group scales [rows][K / 128]
+  // gate|up
+  const float *xscale;                // [T] 2^s of each token's fp16 copy
+  moe_bf16 *h_routed, *h_shared;      // [slots][I], [T][Is]
+  // down
+  float *out_acc;                     // [T][H] fp32
+  const float *weights, *sgate;
+  int H;
+  const int *perm;                    // list position -> entry t * K + j
+  uint32_t *status;
+  unsigned long long budget_ns;
+};
+
+// 16 int8 (one 16-byte chunk) -> 8 32-bit TMEM columns of two 16-bit values.
+template <int MODE>
+__device__ __forceinline__ void cvt_chunk(const uint4 q, uint32_t *o) {
+  if (MODE == kXGateUp) {
+    i8x4_to_f16x2(q.x, o[0], o[1]);
+    i8x4_to_f16x2(q.y, o[2], o[3]);
+    i8x4_to_f16x2(q.z, o[4], o[5]);
+    i8x4_to_f16x2(q.w, o[6], o[7]);
+  } else {
+    // exact fp32 values; bf16 keeps their upper halves (<= 8 significant bits)
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const f4 a = i8x4_to_f32(w[i]);
+      o[2 * i] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
+      o[2 * i + 1] = __byte_perm(__float_as_uint(a.z), __float_as_uint(a.w), 0x7632);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kXThreads, 1)
+tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
+                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
+                 const XParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  XBars *bars = reinterpret_cast<XBars *>(smem + kXOffBar);
+  volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *p.n_items;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kXQS; ++i) {
+      ptx::mbar_init(&bars->q_full[i], 1);
+      ptx::mbar_init(&bars->q_empty[i], kConv);
+    }
+    for (int i = 0; i < kXAS; ++i) {
+      ptx::mbar_init(&bars->a_full[i], kConv);
+      ptx::mbar_init(&bars->a_empty[i], 1);
+    }
+    for (int i = 0; i < kXBS; ++i) {
+      ptx::mbar_init(&bars->b_full[i], 1);
+      ptx::mbar_init(&bars->b_empty[i], 1);
+    }
+    for (int i = 0; i < kXPS; ++i) {
+      ptx::mbar_init(&bars->p_full[i], 1);
+      ptx::mbar_init(&bars->p_empty[i], kProm);
+    }
+    ptx::mbar_init(&bars->done[0], 1);
+    ptx::mbar_init(&bars->done[1], 1);
+    ptx::mbar_init(&bars->xch_full, kProm / 2);   // the warps holding up rows
+    ptx::mbar_init(&bars->xch_empty, kProm / 2);  // the warps holding gate rows
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_holder, kXTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_holder;
+  const uint64_t budget = p.budget_ns;
+  auto groups_of = [&](const int4 &itm) {
+    return (itm.x == kE ? p.K_shared : p.K_routed) / kG;
+  };
+
+  if (warp == 0 || warp == 2) {
+    // ----------------------------------- TMA producers: weights (warp 0),
+    // activations (warp 2)
+    if (lane == 0) {
+      const bool wq = warp == 0;
+      if (wq) {
+        ptx::tma_prefetch_desc(&tmA); ptx::tma_prefetch_desc(&tmAs);
+      } else {
+        ptx::tma_prefetch_desc(&tmB); ptx::tma_prefetch_desc(&tmBs);
+      }
+      const uint64_t pol = wq ? ptx::policy_evict_first() : ptx::policy_evict_last();
+      const int depth = wq ? kXQS : kXBS;
+      uint64_t *fullb = wq ? bars->q_full : bars->b_full;
+      uint64_t *emptyb = wq ? bars->q_empty : bars->b_empty;
+      uint32_t n = 0;  // stages issued on this ring
+      bool stop = false;
+      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+        const int4 itm = p.items[it];
+        const bool sh = itm.x == kE;
+        const int ng = groups_of(itm);
+        int rA0, rA1;
+        if (MODE == kXGateUp) {  // 64 gate rows, then the matching 64 up rows
+          const int half = sh ? p.rows_shared : p.rows_routed;
+          const int base = sh ? 0 : itm.x * 2 * half;
+          rA0 = base + itm.y * 64;
+          rA1 = base + half + itm.y * 64;
+        } else {
+          const int base = sh ? 0 : itm.x * p.rows_routed;
+          rA0 = base + itm.y * 128;
+          rA1 = rA0 + 64;
+        }
+        const int nb = (itm.w + kXBRows - 1) / kXBRows;
+        for (int g = 0; g < ng; ++g, ++n) {
+          const uint32_t s = n % depth;
+          if (!ptx::mbar_wait(&emptyb[s], ((n / depth) & 1) ^ 1, abort, budget)) { stop = true; break; }
+          if (wq) {
+            const void *ta = sh ? static_cast<const void *>(&tmAs) : static_cast<const void *>(&tmA);
+            uint8_t *dq = smem + kXOffQ + s * kXQBytes;
+            ptx::mbar_expect_tx(&fullb[s], kXQBytes);
+            ptx::tma_load_2d(dq, ta, g * 128, rA0, &fullb[s], pol);
+            ptx::tma_load_2d(dq + kXQBytes / 2, ta, g * 128, rA1, &fullb[s], pol);
+          } else {
+            const void *tb = sh ? static_cast<const void *>(&tmBs) : static_cast<const void *>(&tmB);
+            uint8_t *db = smem + kXOffB + s * kXBBytes;
+            ptx::mbar_expect_tx(&fullb[s], 2u * nb * kXBRows * 128);
+            for (int h = 0; h < 2; ++h)
+              for (int bb = 0; bb < nb; ++bb)
+                ptx::tma_load_2d(db + h * (kXBBytes / 2) + bb * kXBRows * 128, tb,
+                                 g * 128 + h * 64, itm.z + bb * kXBRows, &fullb[s], pol);
+          }
+        }
+      }
+      // After an abort, the copies still in flight must land before the CTA
+      // exits: wait (bounded) for the last stages issued on this ring.
+      if (*abort) {
+        int never = 0;
+        for (uint32_t k = 0; k < static_cast<uint32_t>(depth) && k < n; ++k) {
+          const uint32_t j = n - 1 - k;
+          ptx::mbar_wait(&fullb[j % depth], (j / depth) & 1, &never, budget);
+        }
+      }
+    }
+  } else if (warp == 1 || warp == kMma1) {
+    // -------------------------------------------- MMA issuers (even, odd)
+    if (lane == 0) {
+      const uint32_t par = warp == 1 ? 0 : 1;
+      uint32_t gs = 0;
+      bool issued = false;
+      for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
+        const int4 itm = p.items[it];
+        const int ng = groups_of(itm);
+        const int n16 = (itm.w + 15) & ~15;
+        const uint32_t idesc = MODE == kXGateUp ? ptx::idesc_f16_f32(128, n16)
+                                                : ptx::idesc_bf16_f32(128, n16);
+        for (int g = 0; g < ng; ++g, ++gs) {
+          if ((gs & 1) != par) continue;
+          const int sa = gs % kXAS, sb = gs % kXBS, pb = gs % kXPS;
+          if (!ptx::mbar_wait(&bars->a_full[sa], (gs / kXAS) & 1, abort, budget)) break;
+          if (!ptx::mbar_wait(&bars->b_full[sb], (gs / kXBS) & 1, abort, budget)) break;
+          if (!ptx::mbar_wait(&bars->p_empty[pb], ((gs / kXPS) & 1) ^ 1, abort, budget)) break;
+          ptx::tc_fence_after();
+          const uint32_t b0 = ptx::smem_u32(smem + kXOffB + sb * kXBBytes);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // K = 16 per instruction: 8 TMEM columns of A
+            const uint32_t boff = (k >> 2) * (kXBBytes / 2) + (k & 3) * 32;
+            ptx::mma_tmem_a(tmem + kXColP + pb * 128, tmem + sa * 64 + k * 8,
+                            ptx::sw128_desc(b0 + boff), idesc, k > 0);
+          }
+          ptx::mma_commit(&bars->a_empty[sa]);
+          ptx::mma_commit(&bars->b_empty[sb]);
+          ptx::mma_commit(&bars->p_full[pb]);
+          issued = true;
+        }
+      }
+      if (issued) {  // all MMAs complete before TMEM is released
+        ptx::mma_commit(&bars->done[par]);
+        int never = 0;
+        ptx::mbar_wait(&bars->done[par], 0, &never, budget);
+      }
+    }
+  } else if (warp < kConv0 + kConv) {
+    // ------------------------------------------------------- converters
+    const int quarter = warp & 3;  // TMEM lanes 32 * quarter .. + 31
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t gs = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int ng = groups_of(p.items[it]);
+      for (int g = 0; g < ng; ++g, ++gs) {
+        const int sq = gs % kXQS, sa = gs % kXAS;
+        if (!ptx::mbar_wait(&bars->q_full[sq], (gs / kXQS) & 1, abort, budget)) { ok = false; break; }
+        if (!ptx::mbar_wait(&bars->a_empty[sa], ((gs / kXAS) & 1) ^ 1, abort, budget)) { ok = false; break; }
+        ptx::tc_fence_after();
+        // row r of the swizzled tile: 16-byte chunk c sits at chunk c ^ (r & 7)
+        const uint8_t *src = smem + kXOffQ + sq * kXQBytes + r * 128;
+        uint4 q[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
+        const uint32_t ta = tmem + tl + sa * 64;
+        uint32_t v0[32], v1[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cvt_chunk<MODE>(q[c], v0 + 8 * c);
+        ptx::tmem_st32(ta, v0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cvt_chunk<MODE>(q[4 + c], v1 + 8 * c);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->q_empty[sq]);
+        ptx::tmem_st32(ta + 32, v1);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->a_full[sa]);
+      }
+    }
+  } else {
+    // --------------------------------------------- promoters + epilogue
+    const int quarter = warp & 3;
+    const int ch = (warp - kConv0 - kConv) >> 2;  // column blocks ch, ch + 2, ch + 4, ch + 6
+    const int r = quarter * 32 + lane;       // tile row of this thread
+    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
+    float acc[64];
+    uint32_t gs = 0, n_done = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++n_done) {
+      const int4 itm = p.items[it];
+      const bool sh = itm.x == kE;
+      const int ng = groups_of(itm);
+      const int n = itm.w, nblk = (n + 15) >> 4;
+      const moe_bf16 *srow;  // this row's group scales
+      if (MODE == kXGateUp) {
+        const int half = sh ? p.rows_shared : p.rows_routed;
+        const int rr = r < 64 ? itm.y * 64 + r : half + itm.y * 64 + (r - 64);
+        srow = (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * 2 * half * ng) +
+               static_cast<size_t>(rr) * ng;
+      } else {
+        const int rr = itm.y * 128 + r;
+        srow = (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * p.rows_routed * ng) +
+               static_cast<size_t>(rr) * ng;
+      }
+      // The row's group scales, 16 at a time, packed two per word and
+      // consumed from the low half; the per-column data of the epilogue.
+      // Both are loaded here so that their latency hides behind the groups.
+      uint32_t sw[8];
+      auto load_scales = [&](int g0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sw[i] = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (g0 + i < ng) sw[i >> 1] |= static_cast<uint32_t>(srow[g0 + i]) << (16 * (i & 1));
+      };
+      load_scales(0);
+      float cs[4];  // gate|up: 2^s of the column's token; down: combine weight
+      int ct[4];    // down: the column's token
+#pragma unroll
+      for (int jb = 0; jb < 4; ++jb) {
+        cs[jb] = 0.0f;
+        ct[jb] = 0;
+        const int cl = (ch + 2 * jb) * 16 + (lane & 15);
+        if (cl < n) {
+          if (MODE == kXGateUp) {
+            if (r < 64) cs[jb] = p.xscale[sh ? itm.z + cl : p.perm[itm.z + cl] / kK];
+          } else if (sh) {
+            ct[jb] = itm.z + cl;
+            cs[jb] = p.sgate ? p.sgate[itm.z + cl] : 0.0f;
+          } else {
+            const int ent = p.perm[itm.z + cl];
+            ct[jb] = ent / kK;
+            cs[jb] = p.weights[ent];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+      for (int g = 0; g < ng; ++g, ++gs) {
+        const int pb = gs % kXPS;
+        if (!ptx::mbar_wait(&bars->p_full[pb], (gs / kXPS) & 1, abort, budget)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const float sc = bf16_lo(sw[0]);
+        const uint32_t tb = tmem + tl + kXColP + pb * 128;
+#pragma unroll
+        for (int jb = 0; jb < 4; ++jb) {
+          const int b = ch + 2 * jb;
+          if (b < nblk) {
+            float v[16];
+            ptx::tmem_ld16(tb + b * 16, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[jb * 16 + j] = fmaf(sc, v[j], acc[jb * 16 + j]);
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->p_empty[pb]);
+        if ((g & 15) == 15) {
+          load_scales(g + 1);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 7; ++i) sw[i] = __funnelshift_r(sw[i], sw[i + 1], 16);
+          sw[7] >>= 16;
+        }
+      }
+      if (!ok) break;
+      // ------------------------------------------------------ epilogue
+      // acc[jb * 16 + j] is column (ch + 2 * jb) * 16 + j of this row
+      if (MODE == kXGateUp) {
+        float *xch = reinterpret_cast<float *>(smem + kXOffX);
+        const uint32_t par = n_done & 1;
+        if (r >= 64) {  // up rows hand their accumulators to the gate rows
+          if (!ptx::mbar_wait(&bars->xch_empty, par ^ 1, abort, budget)) break;
+#pragma unroll
+          for (int jb = 0; jb < 4; ++jb) {
+            const int b = ch + 2 * jb;
+            if (b < nblk) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) xch[(b * 16 + j) * 64 + (r - 64)] = acc[jb * 16 + j];
+            }
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bars->xch_full);
+        } else {
+          if (!ptx::mbar_wait(&bars->xch_full, par, abort, budget)) break;
+          const int Irows = sh ? p.rows_shared : p.rows_routed;
+          moe_bf16 *hout = sh ? p.h_shared : p.h_routed;
+          const int i = itm.y * 64 + r;
+#pragma unroll
+          for (int jb = 0; jb < 4; ++jb) {
+            const int b = ch + 2 * jb;
+            if (b < nblk) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int col = b * 16 + j;
+                const float sj = __shfl_sync(0xFFFFFFFFu, cs[jb], j);  // lane j holds column j's
+                if (col < n) {
+                  const float u = xch[col * 64 + r] * sj;
+                  hout[static_cast<size_t>(itm.z + col) * Irows + i] =
+                      f32_to_bf16(silu_mul(acc[jb * 16 + j] * sj, u));
+                }
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&bars->xch_empty);
+        }
+      } else {
+        // Weighted combine, out_acc[t][row] += w * acc: a 4 x 4 transpose
+        // among each four lanes leaves every lane four consecutive rows of
+        // one column, added with one 16-byte reduction.
+        const int q4 = lane & 3;
+        const bool lo2 = (q4 & 2) == 0, odd = (q4 & 1) != 0;
+        const int nrow4 = itm.y * 128 + quarter * 32 + (lane & ~3);
+#pragma unroll
+        for (int jb = 0; jb < 4; ++jb) {
+          const int b = ch + 2 * jb;
+          if (b < nblk) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float *v = &acc[jb * 16 + c4 * 4];  // this row, columns c4*4 .. +3
+              // lanes q and q ^ 2 swap 2 x 2 blocks
+              const float r0 = __shfl_xor_sync(0xFFFFFFFFu, lo2 ? v[2] : v[0], 2);
+              const float r1 = __shfl_xor_sync(0xFFFFFFFFu, lo2 ? v[3] : v[1], 2);
+              const float x0 = lo2 ? v[0] : r0, x1 = lo2 ? v[1] : r1;
+              const float x2 = lo2 ? r0 : v[2], x3 = lo2 ? r1 : v[3];
+              // lanes q and q ^ 1 swap single elements
+              const float p0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? x0 : x1, 1);
+              const float p1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? x2 : x3, 1);
+              const float y0 = odd ? p0 : x0, y1 = odd ? x1 : p0;
+              const float y2 = odd ? p1 : x2, y3 = odd ? x3 : p1;
+              // now: column c4 * 4 + q4, rows nrow4 .. nrow4 + 3
+              const int j = c4 * 4 + q4;
+              const int tj = __shfl_sync(0xFFFFFFFFu, ct[jb], j);  // lane j holds column j's
+              const float wj = __shfl_sync(0xFFFFFFFFu, cs[jb], j);
+              if (b * 16 + j < n && wj != 0.0f)
+                ptx::red_add_v4_f32(p.out_acc + static_cast<size_t>(tj) * p.H + nrow4, wj * y0,
+                                    wj * y1, wj * y2, wj * y3);
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kXTmemCols);
+  }
+  if (threadIdx.x == 0 && bars->abort) set_status(p.status, MOE_DEV_TIMEOUT);
+}
+
+// ------------------------------------ token -> expert lists, work items
+
+// One CTA per expert e (grid kE, kLiThreads threads).  Every CTA histograms
+// all T*K entries (so it knows the offsets of the experts before it), then
+// compacts the entries with ids == e in entry order, which yields the list
+// sorted by (e, t, j) as the one-CTA counting sort does, and lays out e's
+// work items: gate|up -> (e, 64-row pair tile m, first list row, n), down ->
+// (e, 128-row tile m, first, n).  CTA 0 also writes the shared expert's items
+// (e == kE, B rows indexed by token), the item totals and slot_of = -1 for
+// entries that name no expert.
+constexpr int kLiThreads = 1024;
+constexpr int kLiPer = 16;  // entries per thread and pass
+
+__global__ void __launch_bounds__(kLiThreads)
+lists_items_kernel(const int32_t *__restrict__ ids, int T, Lists L, int I, int Is, int H,
+                   int4 *__restrict__ gu, int *__restrict__ n_gu, int4 *__restrict__ dn,
+                   int *__restrict__ n_dn, uint32_t *status) {
+  __shared__ int hist[kE];
+  __shared__ int pre[kE], tpre[kE];
+  __shared__ int scan_tmp[32];
+  __shared__ int run;
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = T * kK;
+  if (tid < kE) hist[tid] = 0;
+  if (tid == 0) run = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int i0 = 0; i0 < n; i0 += kLiThreads * kLiPer) {
+    int v[kLiPer];
+#pragma unroll
+    for (int u = 0; u < kLiPer; ++u) {
+      const int i = i0 + u * kLiThreads + tid;
+      v[u] = i < n ? ids[i] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kLiPer; ++u) {
+      if (v[u] >= kE) bad = true;
+      if (v[u] >= 0 && v[u] < kE) atomicAdd(&hist[v[u]], 1);
+    }
+  }
+  if (bad && e == 0) set_status(status, MOE_DEV_BAD_EXPERT);
+  __syncthreads();
+  const int c = tid < kE ? hist[tid] : 0;
+  const int off = block_exclusive_scan_256(c, scan_tmp);
+  const int tl = block_exclusive_scan_256((c + 127) / 128, scan_tmp);
+  if (tid < kE) { pre[tid] = off; tpre[tid] = tl; }
+  __syncthreads();
+  const int cnt = hist[e], base = pre[e];
+  if (tid == 0) {
+    L.counts[e] = cnt;
+    L.offsets[e] = base;
+    if (e == kE - 1) L.offsets[kE] = base + cnt;
+  }
+  // ordered compaction: thread tid takes entries i0 + tid * kLiPer + u
+  for (int i0 = 0; i0 < n && cnt > 0; i0 += kLiThreads * kLiPer) {
+    int v[kLiPer];
+    int m = 0;
+#pragma unroll
+    for (int u = 0; u < kLiPer; ++u) {
+      const int i = i0 + tid * kLiPer + u;
+      v[u] = i < n ? ids[i] : -1;
+      m += v[u] == e;
+    }
+    // exclusive scan of m over the block, in thread order
+    int incl = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) scan_tmp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = scan_tmp[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+        if (lane >= o) w += y;
+      }
+      scan_tmp[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int pos = base + run + (warp > 0 ? scan_tmp[warp - 1] : 0) + incl - m;
+#pragma unroll
+    for (int u = 0; u < kLiPer; ++u) {
+      if (v[u] == e) {
+        const int i = i0 + tid * kLiPer + u;
+        L.perm[pos] = i;
+        if (L.slot_of) L.slot_of[i] = pos;
+        ++pos;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) run += scan_tmp[31];
+    __syncthreads();
+  }
+  if (e == 0 && L.slot_of) {  // entries that name no expert get no slot
+    for (int i = tid; i < n; i += kLiThreads) {
+      const int x = ids[i];
+      if (x < 0 || x >= kE) L.slot_of[i] = -1;
+    }
+  }
+  // work items of expert e
+  const int mg = I / 64, md = H / 128;
+  const int tiles = (cnt + 127) / 128, tb = tpre[e];
+  for (int k = tid; k < tiles * (mg + md); k += kLiThreads) {
+    const int nt = k / (mg + md), m = k % (mg + md);
+    const int first = base + nt * 128, nn = min(128, cnt - nt * 128);
+    if (m < mg) gu[(tb + nt) * mg + m] = make_int4(e, m, first, nn);
+    else dn[(tb + nt) * md + (m - mg)] = make_int4(e, m - mg, first, nn);
+  }
+  if (e == 0) {
+    const int nr = tpre[kE - 1] + (hist[kE - 1] + 127) / 128;  // all routed tiles
+    const int ts = Is > 0 ? (T + 127) / 128 : 0;
+    const int mgs = Is / 64;
+    for (int k = tid; k < ts * mgs; k += kLiThreads) {
+      const int nt = k / mgs, m = k % mgs;
+      gu[nr * mg + k] = make_int4(kE, m, nt * 128, min(128, T - nt * 128));
+    }
+    for (int k = tid; k < ts * md; k += kLiThreads) {
+      const int nt = k / md, m = k % md;
+      dn[nr * md + k] = make_int4(kE, m, nt * 128, min(128, T - nt * 128));
+    }
+    if (tid == 0) {
+      *n_gu = nr * mg + ts * mgs;
+      *n_dn = nr * md + ts * md;
+    }
+  }
+}
+
+// The gate|up activation operand in fp16, one warp per token t: the token
+// times 2^-s, with 2^s chosen per token so that its largest magnitude lands
+// in [2^14, 2^15) (every element within 2^29 of that largest is then exact
+// in fp16), written to x16[t] (the shared expert's operand) and to row p of
+// xs16 for each list position p = slot_of[t * K + j] of the token (the routed
+// experts' operand).  2^s is kept in xscale[t]; the token's fp32 output row
+// is zeroed for the combine's reductions.
+constexpr int kGatherMaxChunks = 8;  // 16-byte chunks per lane held in registers (H <= 2048)
+
+__global__ void scale_gather_kernel(const moe_bf16 *__restrict__ x, int T, int H,
+                                    const int32_t *__restrict__ slot_of, uint16_t *__restrict__ xs16,
+                                    uint16_t *__restrict__ x16, float *__restrict__ xscale,
+                                    float *__restrict__ out_acc) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const moe_bf16 *xr = x + static_cast<size_t>(t) * H;
+  const int nc = H / 256;  // chunks per lane
+  const bool in_regs = nc <= kGatherMaxChunks;
+  uint4 v[kGatherMaxChunks];
+  float m = 0.0f;
+  auto absmax = [&](const uint4 &q) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int c = 0; c < kGatherMaxChunks; ++c)
+      if (c < nc) v[c] = ld_nc(xr + c * 256 + lane * 8);
+#pragma unroll
+    for (int c = 0; c < kGatherMaxChunks; ++c)
+      if (c < nc) absmax(v[c]);
+  } else {
+    for (int c = 0; c < nc; ++c) absmax(ld_nc(xr + c * 256 + lane * 8));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  int sexp = 0;
+  if (m > 0.0f && isfinite(m)) {
+    sexp = static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14;
+    sexp = max(-110, min(110, sexp));
+  }
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - sexp) << 23);  // 2^-s
+  int pos[kK];
+#pragma unroll
+  for (int j = 0; j < kK; ++j) pos[j] = slot_of[static_cast<size_t>(t) * kK + j];
+  auto emit = [&](int c, const uint4 &q) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(bf16_lo(w[i]) * down, bf16_hi(w[i]) * down);
+      o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+    const int k = c * 256 + lane * 8;
+    *reinterpret_cast<uint4 *>(x16 + static_cast<size_t>(t) * H + k) = ov;
+#pragma unroll
+    for (int j = 0; j < kK; ++j)
+      if (pos[j] >= 0) *reinterpret_cast<uint4 *>(xs16 + static_cast<size_t>(pos[j]) * H + k) = ov;
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int c = 0; c < kGatherMaxChunks; ++c)
+      if (c < nc) emit(c, v[c]);
+  } else {
+    for (int c = 0; c < nc; ++c) emit(c, ld_nc(xr + c * 256 + lane * 8));
+  }
+  float4 *orow = reinterpret_cast<float4 *>(out_acc + static_cast<size_t>(t) * H);
+  for (int k = lane; k < H / 4; k += 32) orow[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (lane == 0) xscale[t] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
+}
+
+__global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
+                                   moe_bf16 *__restrict__ out) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n4;
+       i0 += 4 * stride) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * stride < n4) v[u] = __ldcg(reinterpret_cast<const float4 *>(acc) + i0 + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * stride < n4) {
+        uint2 o;
+        o.x = pack_bf16x2(v[u].x, v[u].y);
+        o.y = pack_bf16x2(v[u].z, v[u].w);
+        reinterpret_cast<uint2 *>(out)[i0 + u * stride] = o;
+      }
+  }
+}
+
+template <int MODE>
+cudaError_t launch_x(const CUtensorMap &a, const CUtensorMap &as, const CUtensorMap &b,
+                     const CUtensorMap &bs, const XParams &p, cudaStream_t s) {
+  static bool attr[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tc_expert_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kXSmem));
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  tc_expert_kernel<MODE><<<tc_sm_count(), kXThreads, kXSmem, s>>>(a, as, b, bs, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tc_items_bytes(int T, int I, int Is, int H) {
+  const size_t tiles = static_cast<size_t>(T) * kK / 128 + kE;
+  const size_t ts = (static_cast<size_t>(T) + 127) / 128;
+  const size_t gu = tiles * (I / 64) + ts * (Is / 64);
+  const size_t dn = tiles * (H / 128) + ts * (H / 128);
+  return (gu + dn + 16) * sizeof(int4);
+}
+
+cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
+                              const moe_weights &w, const int32_t *ids, const Lists &L,
+                              const float *weights,
+                              const float *sgate, uint16_t *xs16, uint16_t *x16, float *xscale,
+                              moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
+                              moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
+                              cudaStream_t s, StageRecorder &rec) {
+#define TC_STEP(expr)                          \
+  do {                                         \
+    cudaError_t e_ = (expr);                   \
+    if (e_ == cudaSuccess) e_ = rec();         \
+    if (e_ != cudaSuccess) return e_;          \
+  } while (0)
+  int4 *gu = items;
+  const size_t tiles = static_cast<size_t>(T) * kK / 128 + kE;
+  const size_t ts = (static_cast<size_t>(T) + 127) / 128;
+  int4 *dn = items + tiles * (I / 64) + ts * (Is / 64);
+  lists_items_kernel<<<kE, kLiThreads, 0, s>>>(ids, T, L, I, Is, H, gu, counters, dn,
+                                              counters + 1, status);
+  TC_STEP(cudaGetLastError());
+  scale_gather_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, L.slot_of, xs16, x16, xscale,
+                                                   out_acc);
+  TC_STEP(cudaGetLastError());
+  const size_t rows_r = static_cast<size_t>(T) * kK;
+  CUtensorMap a13, a13s, bx, bxs, a2, a2s, bh, bhs;
+  const bool shared = Is > 0;
+  bool ok = tc_make_map(&a13, w.w13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                        static_cast<uint64_t>(kE) * 2 * I, H, 64, 128) &&
+            tc_make_map(&bx, xs16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_r, H, kXBRows, 64) &&
+            tc_make_map(&a2, w.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                        static_cast<uint64_t>(kE) * H, I, 64, 128) &&
+            tc_make_map(&bh, h_routed, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_r, I, kXBRows, 64);
+  if (shared)
+    ok = ok && tc_make_map(&a13s, w.ws13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * Is, H, 64, 128) &&
+         tc_make_map(&bxs, x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, T, H, kXBRows, 64) &&
+         tc_make_map(&a2s, w.ws2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, Is, 64, 128) &&
+         tc_make_map(&bhs, h_shared, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, Is, kXBRows, 64);
+  else {
+    a13s = a13; bxs = bx; a2s = a2; bhs = bh;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  XParams p{};
+  p.items = gu; p.n_items = counters;
+  p.K_routed = H; p.K_shared = H;
+  p.rows_routed = I; p.rows_shared = Is;
+  p.s_routed = w.w13_s; p.s_shared = w.ws13_s;
+  p.xscale = xscale; p.perm = L.perm;
+  p.h_routed = h_routed; p.h_shared = h_shared;
+  p.status = status; p.budget_ns = tc_wait_budget_ns();
+  TC_STEP(launch_x<kXGateUp>(a13, a13s, bx, bxs, p, s));
+  XParams q{};
+  q.items = dn; q.n_items = counters + 1;
+  q.K_routed = I; q.K_shared = Is;
+  q.rows_routed = H; q.rows_shared = H;
+  q.s_routed = w.w2_s; q.s_shared = w.ws2_s;
+  q.out_acc = out_acc; q.perm = L.perm; q.weights = weights; q.sgate = sgate; q.H = H;
+  q.status = status; q.budget_ns = tc_wait_budget_ns();
+  TC_STEP(launch_x<kXDown>(a2, a2s, bh, bhs, q, s));
+  const size_t n4 = static_cast<size_t>(T) * H / 4;
+  acc_to_bf16_kernel<<<tc_sm_count() * 4, 256, 0, s>>>(out_acc, n4, out);
+  TC_STEP(cudaGetLastError());
+  return cudaSuccess;
+#undef TC_STEP
+}
+
+}  // namespace moe
