@@ -11,13 +11,17 @@
 //   L  every CTA reads all selections and builds the token -> expert lists
 //      in shared memory;
 //   W  gate|up + SwiGLU: work unit = 8 gate rows + their 8 up rows of one
-//      expert (16 rows x H int8); units are dealt round-robin to the CTAs; a
-//      producer warp streams each unit's rows with bulk async copies into a
-//      5-stage shared-memory ring (the shared expert's first unit is fetched
-//      before routing is known); four warp quads consume units, each warp a
-//      quarter of K, as m16n8k16 bf16 tensor-core MMAs with the int8 weights
-//      converted exactly to bf16 in registers and the group scales promoted
-//      per 128-wide K group in fp32; h = bf16(silu(gate) * up) goes to global;
+//      expert (16 rows x H int8); each CTA takes a contiguous, cost-balanced
+//      range of units; a producer warp streams each unit's rows (and their
+//      group scales) with bulk async copies into a 5-stage shared-memory ring
+//      (the shared expert's first units are fetched before routing is
+//      known); three warp quads consume units in turn, each warp a quarter
+//      of K, as m16n8k16 fp16 tensor-core MMAs: the int8 weights become fp16
+//      exactly in registers, the activations are each token's copy scaled
+//      by a power of two into fp16 (exact for every element within 2^29 of
+//      the token's largest), the group scales are promoted per 128-wide K
+//      group in fp32, a rotating reducer warp adds the four K quarters;
+//      h = bf16(silu(gate) * up) goes to global;
 //   -- grid barrier 3 --
 //   D  down + combine: CTA c owns output rows 16c .. 16c+15 of every expert;
 //      the producer has been streaming those rows since its gate|up units
