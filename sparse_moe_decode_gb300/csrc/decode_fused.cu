@@ -1,18 +1,19 @@
 // decode_fused.cu -- the whole block (A1..A7) for decode-size T in one
-// persistent cooperative kernel: one CTA per SM, phases separated by three
-// bounded grid barriers.
+// persistent cooperative kernel: one CTA per SM, phases separated by two
+// bounded grid barriers (three when T > 12).
 //
 //   R  router: 257 rows x (H/512) K-slices of 512, one warp each, fp32
 //      partials (the pages' S1 split of the router into K-slices);
 //   -- grid barrier 1 --
-//   S  one warp per token folds its partials in a fixed order and selects
-//      its top-8 with the warp merge network (softmax, shared sigmoid);
-//   -- grid barrier 2 --
-//   L  every CTA reads all selections and builds the token -> expert lists
-//      in shared memory;
+//   S  one warp per token folds the partials in a fixed order and selects
+//      the top-8 with the warp merge network (softmax, shared sigmoid); for
+//      T <= 12 every CTA selects every token itself, so every CTA holds the
+//      same selection; for larger T the grid shares the tokens and a grid
+//      barrier publishes the selections;
+//   L  every CTA builds the token -> expert lists in shared memory;
 //   W  gate|up + SwiGLU: work unit = 8 gate rows + their 8 up rows of one
-//      expert (16 rows x H int8); each CTA takes a contiguous, cost-balanced
-//      range of units; a producer warp streams each unit's rows (and their
+//      expert (16 rows x H int8); each CTA takes a contiguous, equal share
+//      of the routed units; a producer warp streams each unit's rows (and their
 //      group scales) with bulk async copies into a 5-stage shared-memory ring
 //      (the shared expert's first units are fetched before routing is
 //      known); three warp quads consume units in turn, each warp a quarter
@@ -22,7 +23,7 @@
 //      the token's largest), the group scales are promoted per 128-wide K
 //      group in fp32, a rotating reducer warp adds the four K quarters;
 //      h = bf16(silu(gate) * up) goes to global;
-//   -- grid barrier 3 --
+//   -- grid barrier 2 --
 //   D  down + combine: CTA c owns output rows 16c .. 16c+15 of every expert;
 //      the producer has been streaming those rows since its gate|up units
 //      were done; y for every (token, slot) of those rows stays in shared
@@ -54,6 +55,7 @@ constexpr int kFStageBytes = 16 * kFusedMaxH;  // one gate|up unit, or packed do
 constexpr int kFScaleBytes = 512;              // the group scales of a stage's rows
 constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
 constexpr int kRP = 260;                     // router partial row: 257 used, 16-byte rows
+constexpr int kFLocalSelT = kFConsumerWarps;  // tokens selected by every CTA itself
 
 struct FusedParams {
   const moe_bf16 *x;
@@ -70,7 +72,7 @@ struct FusedParams {
   const int8_t *ws2_q;
   const moe_bf16 *ws2_s;
   float *rpart;        // [T][KS][kRP] router partial sums
-  int32_t *sel_ids;    // [T][K] selection of every token (scratch)
+  int32_t *sel_ids;    // [T][K] selection of every token (T > kFLocalSelT)
   float *sel_w;        // [T][K]
   float *sel_sg;       // [T]
   moe_bf16 *h_routed;  // [T*K][I], rows in list order
@@ -140,6 +142,10 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // Loads of data written earlier in this launch by other CTAs: L2 only.
 __device__ __forceinline__ uint4 ld_cg16(const void *p) {
   return __ldcg(reinterpret_cast<const uint4 *>(p));
+}
+
+__device__ __forceinline__ uint4 ld_ca16(const void *p) {
+  return __ldca(reinterpret_cast<const uint4 *>(p));
 }
 
 __device__ __forceinline__ float ld_cg_f32(const float *p) { return __ldcg(p); }
@@ -228,17 +234,8 @@ __device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams 
   const int R = n_active * wk.nIb;  // routed units in the grid
   const int c = blockIdx.x, G = gridDim.x;
   wk.has_shared = c < wk.nSb ? 1 : 0;
-  // Balance by cost: a shared unit weighs its token tiles (T/8), a routed
-  // unit about one; CTA c's routed range starts at its cost prefix minus the
-  // shared units before it.
-  const long long ws = (p.T + 7) / 8;
-  const long long total = R + static_cast<long long>(wk.nSb) * ws;
-  auto start = [&](int cc) {
-    const long long v = total * cc / G - ws * min(cc, wk.nSb);
-    return static_cast<int>(v < 0 ? 0 : (v > R ? R : v));
-  };
-  wk.r_begin = start(c);
-  const int r_end = c + 1 == G ? R : max(wk.r_begin, start(c + 1));
+  wk.r_begin = static_cast<int>((static_cast<long long>(R) * c) / G);
+  const int r_end = static_cast<int>((static_cast<long long>(R) * (c + 1)) / G);
   wk.n_local = wk.has_shared + (r_end - wk.r_begin);
   wk.n0 = 16 * static_cast<int>(blockIdx.x) < p.H ? 16 * static_cast<int>(blockIdx.x) : -1;
   wk.n_down_units = wk.n0 >= 0 ? (p.Is > 0 ? 1 : 0) + n_active : 0;
@@ -398,12 +395,13 @@ __device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, in
   }
 }
 
-// Phase S1: one warp per token over the whole grid: fold the K-slice
-// partials (fixed order), select the top-8, softmax, shared gate; results go
-// to global (and to the caller's optional outputs).
-__device__ __forceinline__ void phase_select(const FusedParams &p, int cwarp, int lane) {
-  const int t = blockIdx.x * kFConsumerWarps + cwarp;
-  if (t >= p.T) return;
+// Token t's selection: fold the K-slice partials (fixed order), select the
+// top-8, softmax, shared gate.  Local: into this CTA's shared memory (every
+// CTA selects every token; CTA 0 writes the optional outputs).  Otherwise
+// into the global selection arrays, by the one warp that owns token t.
+__device__ __forceinline__ void select_token(FusedSmem &S, const FusedParams &p, int t,
+                                             int lane, bool local) {
+  const bool first = !local || blockIdx.x == 0;  // writes the optional outputs
   const float *rp = p.rpart + static_cast<size_t>(t) * p.KS * kRP;
   float4 a0[kFusedMaxH / 512], a1[kFusedMaxH / 512];
   float gp[kFusedMaxH / 512];
@@ -435,36 +433,52 @@ __device__ __forceinline__ void phase_select(const FusedParams &p, int cwarp, in
 #pragma unroll
     for (int i = 1; i < 8; ++i)
       if (lane == i) { myid = id[i]; myw = w[i]; }
-    p.sel_ids[t * kK + lane] = myid;
-    p.sel_w[t * kK + lane] = myw;
-    if (p.ids_out) p.ids_out[t * kK + lane] = myid;
-    if (p.weights_out) p.weights_out[t * kK + lane] = myw;
+    if (local) {
+      S.ids[t][lane] = myid;
+      S.wts[t][lane] = myw;
+    } else {
+      p.sel_ids[t * kK + lane] = myid;
+      p.sel_w[t * kK + lane] = myw;
+    }
+    if (first && p.ids_out) p.ids_out[t * kK + lane] = myid;
+    if (first && p.weights_out) p.weights_out[t * kK + lane] = myw;
   }
   if (lane == 0) {
-    p.sel_sg[t] = p.Is > 0 ? sigmoidf_(g) : 0.0f;
-    if (p.gate_logit_out && p.Is > 0) p.gate_logit_out[t] = g;
-    if (!ok) set_status(p.status, MOE_DEV_NONFINITE);
+    const float sg = p.Is > 0 ? sigmoidf_(g) : 0.0f;
+    if (local) S.sg[t] = sg;
+    else p.sel_sg[t] = sg;
+    if (first && p.gate_logit_out && p.Is > 0) p.gate_logit_out[t] = g;
+    if (first && !ok) set_status(p.status, MOE_DEV_NONFINITE);
   }
-  if (p.logits_out) {
+  if (first && p.logits_out) {
     float4 *dst = reinterpret_cast<float4 *>(p.logits_out + static_cast<size_t>(t) * kE + 8 * lane);
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
     dst[1] = make_float4(v[4], v[5], v[6], v[7]);
   }
 }
 
-// Phase S2 (every CTA): read the selection of every token and build the
+// Phases S and L.  T <= kFLocalSelT: every CTA selects all T tokens itself
+// (one warp per token, the same fold order and merge network in every CTA,
+// so every CTA holds the same selection), with no grid barrier between
+// selection and lists.  Larger T: one warp of the grid per token, a grid
+// barrier, and every CTA reads all selections.  Then every CTA builds the
 // token -> expert lists in shared memory.
-__device__ __forceinline__ void phase_lists(FusedSmem &S, const FusedParams &p, int cwarp,
-                                            int lane) {
+__device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedParams &p, int cwarp,
+                                                   int lane, uint64_t budget) {
   const int tid = threadIdx.x;  // consumer threads
-  for (int i = tid; i < p.T * kK; i += kFConsumers) {
-    S.ids[i / kK][i % kK] = __ldcg(p.sel_ids + i);
-    S.wts[i / kK][i % kK] = __ldcg(p.sel_w + i);
+  if (p.T <= kFLocalSelT) {
+    if (cwarp < p.T) select_token(S, p, cwarp, lane, true);
+  } else {
+    const int t = blockIdx.x * kFConsumerWarps + cwarp;
+    if (t < p.T) select_token(S, p, t, lane, false);
+    grid_sync(p.grid_bar, S, budget);
+    for (int i = tid; i < p.T * kK; i += kFConsumers) {
+      S.ids[i / kK][i % kK] = __ldcg(p.sel_ids + i);
+      S.wts[i / kK][i % kK] = __ldcg(p.sel_w + i);
+    }
+    for (int t2 = tid; t2 < p.T; t2 += kFConsumers) S.sg[t2] = __ldcg(p.sel_sg + t2);
   }
-  for (int t = tid; t < p.T; t += kFConsumers) {
-    S.sg[t] = __ldcg(p.sel_sg + t);
-    S.xs[t] = __ldcg(p.xscale + t);
-  }
+  for (int t2 = tid; t2 < p.T; t2 += kFConsumers) S.xs[t2] = __ldcg(p.xscale + t2);
   if (tid < kE) {
     S.counts[tid] = 0;
     S.mask[tid] = 0ull;
@@ -556,7 +570,7 @@ __device__ __forceinline__ void mma_slice_f16(const uint8_t *rows, int stride, i
 }
 
 // The K range [kb, kb + kn) (a multiple of 64) of a 16-row unit for one n8
-// token tile, bf16 operands.  The B fragments of up to eight slices (512 of
+// token tile, bf16 operands.  The B fragments of up to four slices (256 of
 // K) are fetched together before their MMAs, so each batch pays one memory
 // latency; each slice's partial sums are promoted with its group's scales
 // (lo: rows 0..7, hi: rows 8..15).  brow = this lane's token row or NULL.
@@ -564,11 +578,11 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
                                           const moe_bf16 *brow, int g, int c, bool cg,
                                           const moe_bf16 *s_lo, const moe_bf16 *s_hi,
                                           float (&acc)[4]) {
-  for (int kk = kb; kk < kb + kn; kk += 512) {
-    const int ns = min(8, (kb + kn - kk) / 64);
-    uint32_t xw[8][8];
+  for (int kk = kb; kk < kb + kn; kk += 256) {
+    const int ns = min(4, (kb + kn - kk) / 64);
+    uint32_t xw[4][8];
 #pragma unroll
-    for (int sl = 0; sl < 8; ++sl) {
+    for (int sl = 0; sl < 4; ++sl) {
       if (brow && sl < ns) {
         const moe_bf16 *src = brow + kk + 64 * sl + 16 * c;
         const uint4 x0 = cg ? ld_cg16(src) : ld_nc(src);
@@ -581,7 +595,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
       }
     }
 #pragma unroll
-    for (int sl = 0; sl < 8; ++sl) {
+    for (int sl = 0; sl < 4; ++sl) {
       if (sl >= ns) break;
       const int k0 = kk + 64 * sl;
       const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
@@ -599,7 +613,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 // takes K quarter wq).
 __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, const Work &wk,
                                            int j, int q, int wq, int lane, uint64_t budget,
-                                           uint32_t &npass, uint32_t (&xc)[8][8], int &xc_e) {
+                                           uint32_t &npass) {
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
   int e, i0;
@@ -628,38 +642,39 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
       }
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const int ns = kq / 64;  // <= 8 since H <= 2048
     for (int nt = 0; nt < ntiles; ++nt) {
-      // The warp's activation fragments for its K quarter (8 slices, 64
-      // registers).  A routed expert with <= 8 tokens keeps them across its
-      // consecutive units (one expert spans many units of a CTA).
-      const bool cacheable = !sh && n_tok <= 8;
-      if (!cacheable || xc_e != e) {
+      for (int kk = kb; kk < kb + kq; kk += 256) {  // batches of 4 slices (2 groups)
+        const int ns4 = min(4, (kb + kq - kk) / 64);
+        uint32_t xw[4][8];
 #pragma unroll
-        for (int sl = 0; sl < 8; ++sl) {
-          if (brow[nt] && sl < ns) {  // fp16 rows written earlier in this launch
-            const moe_bf16 *src = brow[nt] + kb + 64 * sl + 16 * c;
-            const uint4 x0 = ld_cg16(src), x1 = ld_cg16(src + 8);
-            xc[sl][0] = x0.x; xc[sl][1] = x0.y; xc[sl][2] = x0.z; xc[sl][3] = x0.w;
-            xc[sl][4] = x1.x; xc[sl][5] = x1.y; xc[sl][6] = x1.z; xc[sl][7] = x1.w;
+        for (int sl = 0; sl < 4; ++sl) {
+          if (brow[nt] && sl < ns4) {
+            // fp16 rows written before grid barrier 1 of this launch: no SM
+            // reads them earlier, so L1 holds no stale copy, and caching
+            // them in L1 serves this CTA's many units of the same expert
+            const moe_bf16 *src = brow[nt] + kk + 64 * sl + 16 * c;
+            const uint4 x0 = ld_ca16(src), x1 = ld_ca16(src + 8);
+            xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
+            xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
           } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xc[sl][i] = 0u;
+            for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
           }
         }
-        xc_e = cacheable ? e : -1;
-      }
+        const float slo0 = bf16_to_f32(s_gate[kk / kG]), shi0 = bf16_to_f32(s_up[kk / kG]);
+        const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[kk / kG + 1]) : 0.0f;
+        const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[kk / kG + 1]) : 0.0f;
 #pragma unroll
-      for (int sl = 0; sl < 8; ++sl) {
-        if (sl >= ns) break;
-        const int k0 = kb + 64 * sl;  // kb is a multiple of 128
-        const float slo = bf16_to_f32(s_gate[k0 / kG]), shi = bf16_to_f32(s_up[k0 / kG]);
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_slice_f16(rows, stride, k0, g, c, xc[sl], part);
-        acc[nt][0] = fmaf(slo, part[0], acc[nt][0]);
-        acc[nt][1] = fmaf(slo, part[1], acc[nt][1]);
-        acc[nt][2] = fmaf(shi, part[2], acc[nt][2]);
-        acc[nt][3] = fmaf(shi, part[3], acc[nt][3]);
+        for (int sl = 0; sl < 4; ++sl) {
+          if (sl >= ns4) break;
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part);
+          const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
+          acc[nt][0] = fmaf(slo, part[0], acc[nt][0]);
+          acc[nt][1] = fmaf(slo, part[1], acc[nt][1]);
+          acc[nt][2] = fmaf(shi, part[2], acc[nt][2]);
+          acc[nt][3] = fmaf(shi, part[3], acc[nt][3]);
+        }
       }
     }
     if (tb + kFPass >= n_tok) {  // the stage's rows are no longer needed
@@ -827,16 +842,12 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     const int q = warp >> 2, wq = warp & 3;
     phase_router(p, warp, lane);
     grid_sync(p.grid_bar, S, budget);
-    phase_select(p, warp, lane);
-    grid_sync(p.grid_bar, S, budget);
-    phase_lists(S, p, warp, lane);
+    phase_select_lists(S, p, warp, lane, budget);
     if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
     uint32_t npass = 0;
-    uint32_t xc[8][8];
-    int xc_e = -1;
     for (int j = q; j < wk.n_local; j += kFQuads)
-      consume_gu(S, p, wk, j, q, wq, lane, budget, npass, xc, xc_e);
+      consume_gu(S, p, wk, j, q, wq, lane, budget, npass);
     grid_sync(p.grid_bar, S, budget);
     for (int k = q; k < wk.n_down_stages; k += kFQuads)
       consume_down(S, p, wk, k, wq, lane, budget);
@@ -895,8 +906,8 @@ bool fused_decode_supported(int T, int H, int I, int Is) {
 
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 const moe_weights &w, uint16_t *x16, float *xscale,
-                                float *rpart, int32_t *sel_ids,
-                                float *sel_w, float *sel_sg, moe_bf16 *h_routed,
+                                float *rpart, int32_t *sel_ids, float *sel_w,
+                                float *sel_sg, moe_bf16 *h_routed,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, cudaStream_t s) {

@@ -63,14 +63,14 @@ bool fused_decode_supported(int T, int H, int I, int Is);
 size_t fused_smem_bytes();
 
 // A1..A7 in one cooperative launch.  x16 [T][H] fp16 and xscale [T] (the
-// tokens' scaled fp16 copies), rpart [T][H/512][260] fp32, sel_ids
-// [T][K], sel_w [T][K], sel_sg [T] scratch, h_routed [T*K][I], h_shared
-// [T][Is]; grid_bar is a 32-bit counter whose low 31 bits must be zero
-// before the first launch (each grid barrier leaves them unchanged).
+// tokens' scaled fp16 copies), rpart [T][H/512][260] fp32, sel_ids [T][K],
+// sel_w [T][K], sel_sg [T], h_routed [T*K][I], h_shared [T][Is] scratch; grid_bar is a 32-bit counter whose
+// low 31 bits must be zero before the first launch (each grid barrier leaves
+// them unchanged).
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 const moe_weights &w, uint16_t *x16, float *xscale,
-                                float *rpart, int32_t *sel_ids,
-                                float *sel_w, float *sel_sg, moe_bf16 *h_routed,
+                                float *rpart, int32_t *sel_ids, float *sel_w,
+                                float *sel_sg, moe_bf16 *h_routed,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, cudaStream_t s);
