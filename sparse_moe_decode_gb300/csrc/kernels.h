@@ -81,6 +81,10 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
 // [box_rows][box_cols], 128-byte swizzle, zero fill out of bounds.
 bool tc_make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
                  uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols);
+// 3-D tensor of `esize`-byte elements: dims innermost first, strides (bytes)
+// of dims 1 and 2, box innermost first; 128-byte swizzle, zero fill.
+bool tc_make_map3(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
+                  const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]);
 int tc_sm_count();
 // Budget of every bounded wait in the tcgen05 kernels (MOE_WAIT_BUDGET_NS, default 2 s).
 unsigned long long tc_wait_budget_ns();

@@ -5,14 +5,14 @@
 //
 // Orientation: D[row, token] = sum_k W[row, k] * X[token, k].  128 weight
 // rows are the M operand (one TMEM lane each), the tokens of one expert tile
-// are N (<= 128): each weight tile is streamed from HBM once for all of its
-// expert's tokens.
+// are N (<= 96): each weight tile is streamed from HBM once for all of its
+// expert's tokens (an expert with more than 96 tokens gets several tiles).
 //
 // Per 128-wide K group (one quantisation group):
 //   TMA         int8 tile 128 x 128 (128-byte swizzle) -> shared ring Q
 //   converters  Q row -> exact fp16 (gate|up) or bf16 (down) -> TMEM A stage
 //               (tcgen05.st; |q| <= 127 is exact in either type)
-//   TMA         activation tile N x 128 -> shared ring B
+//   TMA         activation tile N x 128 -> shared ring B (4 stages)
 //   MMA thread  P = A[TMEM] x B[smem]^T into one of three TMEM partial buffers
 //   promoters   acc[row][token] += s[row][group] * P (fp32 registers)
 // so the product q * s is never rounded ("scale promotion").  The gate|up
@@ -20,14 +20,13 @@
 // (exact for every element within 2^29 of the token's largest), undone on the
 // fp32 results; the down activations h are bf16 as the SwiGLU rounds them.
 //
-// Warp roles (512 threads): warp 0 issues the weight TMA loads, warp 2 the
-// activation TMA loads (two producers, so that the weight ring runs ahead on
-// its own depth), warps 1 and 15 issue the MMAs of the even and the odd K
-// groups (one issuing thread sustains only about one MMA instruction per
-// hundred cycles, so two double the tensor rate at these N), warp 1 also
-// owns TMEM, warps 3..6 convert (one per TMEM lane quarter), warps 7..14
-// promote and run the epilogue (two per lane quarter, splitting the token
-// columns).  Every wait is bounded by a %globaltimer budget; on expiry
+// Warp roles (512 threads): warp 0 issues the TMA loads (one copy of the
+// weight tile and one of the activation tile per K group), warps 1, 2 and
+// 15 issue the MMAs of the K groups g with g mod 3 = 0, 1, 2 (one issuing
+// thread sustains only about one tcgen05 instruction per hundred cycles, so
+// several multiply the tensor rate at these N), warp 1 also owns TMEM, warps
+// 3..6 convert (one per TMEM lane quarter), warps 7..14 promote and run the
+// epilogue (two per lane quarter, splitting the token columns).  Every wait is bounded by a %globaltimer budget; on expiry
 // the CTA drains what it has in flight, frees TMEM, sets MOE_DEV_TIMEOUT and
 // returns.
 #include <cuda.h>
@@ -42,20 +41,30 @@ namespace moe {
 namespace {
 
 constexpr int kXThreads = 512;
-constexpr int kMma1 = 15;                  // second MMA issuing warp
+constexpr int kMma1 = 2, kMma2 = 15;       // second and third MMA issuing warps
+constexpr int kIssuers = 3;
 constexpr int kConv0 = 3;                  // first converter warp
 constexpr int kConv = 4;                   // converter warps
 constexpr int kProm = 8;                   // promoter warps
-constexpr int kXQS = 6, kXBS = 3;          // shared-memory ring depths
-constexpr int kXAS = 2;                    // TMEM A stages
+constexpr int kXTile = 96;                 // tokens per work item at most (N)
+constexpr int kXQS = 6, kXBS = 4;          // shared-memory ring depths
+constexpr int kXAS = 3;                    // TMEM A stages
 constexpr int kXPS = 3;                    // TMEM partial buffers
 constexpr int kXBRows = 32;                // rows per activation TMA box
 constexpr uint32_t kXQBytes = 128 * 128;   // int8 weight tile
-constexpr uint32_t kXBBytes = 2 * 128 * 128;  // 16-bit activation tile (<= 128 rows), two K halves
-constexpr uint32_t kXXchBytes = 128 * 64 * 4;  // gate|up exchange of the up rows
-constexpr uint32_t kXTmemCols = 512;       // A stages [0, 128), partials at 128, 256, 384
-constexpr uint32_t kXColP = kXAS * 64;
-static_assert(kXColP + kXPS * 128 <= kXTmemCols, "tensor memory columns");
+constexpr uint32_t kXBBytes = 2 * kXTile * 128;  // 16-bit activation tile (<= 96 rows), two K halves
+constexpr uint32_t kXXchBytes = kXTile * 64 * 4;  // gate|up exchange of the up rows
+// TMEM columns: partial buffer pb at 128 * (pb + 1) (96 wide); A stage sa in
+// two 32-column halves (K 0..63 and 64..127 of the group) in the gaps.
+constexpr uint32_t kXTmemCols = 512;
+__host__ __device__ constexpr uint32_t x_pcol(int pb) { return 128u * (pb + 1); }
+__host__ __device__ constexpr uint32_t x_acol(int sa, int half) {
+  return sa < 2 ? 64u * sa + 32u * half : (half == 0 ? 224u : 352u);
+}
+static_assert(x_pcol(kXPS - 1) + kXTile <= kXTmemCols, "tensor memory columns");
+static_assert(x_pcol(0) + kXTile <= x_acol(2, 0) && x_acol(2, 0) + 32 <= x_pcol(1) &&
+                  x_pcol(1) + kXTile <= x_acol(2, 1) && x_acol(2, 1) + 32 <= x_pcol(2),
+              "A stages and partials overlap");
 
 constexpr size_t kXOffQ = 0;
 constexpr size_t kXOffB = kXOffQ + kXQS * kXQBytes;
@@ -69,11 +78,20 @@ enum XMode : int { kXGateUp = 0, kXDown = 1 };
 struct XBars {
   uint64_t q_full[kXQS], q_empty[kXQS], a_full[kXAS], a_empty[kXAS], b_full[kXBS],
       b_empty[kXBS];
-  uint64_t p_full[kXPS], p_empty[kXPS], done[2], xch_full, xch_empty;
+  uint64_t p_full[kXPS], p_empty[kXPS], done[kIssuers], xch_full, xch_empty;
   uint32_t tmem_holder;
   int abort;
 };
 static_assert(sizeof(XBars) <= 512, "barrier block");
+
+// Tensor maps: weights (gate|up: 3-D, the 64 gate rows and the matching 64
+// up rows of a group in one copy; down: 128 rows), and activations as 3-D
+// (64 elements, rows, K chunks of 64) with boxes of 32, 64 or 96 rows and two
+// K chunks, so that one copy brings a group's whole activation tile.
+struct XMaps {
+  CUtensorMap a[2];     // routed, shared
+  CUtensorMap b[2][3];  // routed, shared x box rows 32, 64, 96
+};
 
 struct XParams {
   const int4 *items;                  // {expert (kE = shared), m tile, first B row, n}
@@ -115,9 +133,7 @@ __device__ __forceinline__ void cvt_chunk(const uint4 q, uint32_t *o) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kXThreads, 1)
-tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
-                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
-                 const XParams p) {
+tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -143,8 +159,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       ptx::mbar_init(&bars->p_full[i], 1);
       ptx::mbar_init(&bars->p_empty[i], kProm);
     }
-    ptx::mbar_init(&bars->done[0], 1);
-    ptx::mbar_init(&bars->done[1], 1);
+    for (int i = 0; i < kIssuers; ++i) ptx::mbar_init(&bars->done[i], 1);
     ptx::mbar_init(&bars->xch_full, kProm / 2);   // the warps holding up rows
     ptx::mbar_init(&bars->xch_empty, kProm / 2);  // the warps holding gate rows
     bars->abort = 0;
@@ -163,82 +178,76 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     return (itm.x == kE ? p.K_shared : p.K_routed) / kG;
   };
 
-  if (warp == 0 || warp == 2) {
-    // ----------------------------------- TMA producers: weights (warp 0),
-    // activations (warp 2)
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const bool wq = warp == 0;
-      if (wq) {
-        ptx::tma_prefetch_desc(&tmA); ptx::tma_prefetch_desc(&tmAs);
-      } else {
-        ptx::tma_prefetch_desc(&tmB); ptx::tma_prefetch_desc(&tmBs);
+      ptx::tma_prefetch_desc(&maps.a[0]); ptx::tma_prefetch_desc(&maps.a[1]);
+      for (int i = 0; i < 3; ++i) {
+        ptx::tma_prefetch_desc(&maps.b[0][i]); ptx::tma_prefetch_desc(&maps.b[1][i]);
       }
-      const uint64_t pol = wq ? ptx::policy_evict_first() : ptx::policy_evict_last();
-      const int depth = wq ? kXQS : kXBS;
-      uint64_t *fullb = wq ? bars->q_full : bars->b_full;
-      uint64_t *emptyb = wq ? bars->q_empty : bars->b_empty;
-      uint32_t n = 0;  // stages issued on this ring
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      uint32_t nq = 0, nb = 0;  // stages issued on the Q and B rings
       bool stop = false;
       for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
         const int4 itm = p.items[it];
         const bool sh = itm.x == kE;
         const int ng = groups_of(itm);
-        int rA0, rA1;
-        if (MODE == kXGateUp) {  // 64 gate rows, then the matching 64 up rows
-          const int half = sh ? p.rows_shared : p.rows_routed;
-          const int base = sh ? 0 : itm.x * 2 * half;
-          rA0 = base + itm.y * 64;
-          rA1 = base + half + itm.y * 64;
+        int rA;
+        if (MODE == kXGateUp) {  // first gate row; the up rows follow I (Is) rows later
+          rA = (sh ? 0 : itm.x * 2 * p.rows_routed) + itm.y * 64;
         } else {
-          const int base = sh ? 0 : itm.x * p.rows_routed;
-          rA0 = base + itm.y * 128;
-          rA1 = rA0 + 64;
+          rA = (sh ? 0 : itm.x * p.rows_routed) + itm.y * 128;
         }
-        const int nb = (itm.w + kXBRows - 1) / kXBRows;
-        for (int g = 0; g < ng; ++g, ++n) {
-          const uint32_t s = n % depth;
-          if (!ptx::mbar_wait(&emptyb[s], ((n / depth) & 1) ^ 1, abort, budget)) { stop = true; break; }
-          if (wq) {
-            const void *ta = sh ? static_cast<const void *>(&tmAs) : static_cast<const void *>(&tmA);
-            uint8_t *dq = smem + kXOffQ + s * kXQBytes;
-            ptx::mbar_expect_tx(&fullb[s], kXQBytes);
-            ptx::tma_load_2d(dq, ta, g * 128, rA0, &fullb[s], pol);
-            ptx::tma_load_2d(dq + kXQBytes / 2, ta, g * 128, rA1, &fullb[s], pol);
-          } else {
-            const void *tb = sh ? static_cast<const void *>(&tmBs) : static_cast<const void *>(&tmB);
-            uint8_t *db = smem + kXOffB + s * kXBBytes;
-            ptx::mbar_expect_tx(&fullb[s], 2u * nb * kXBRows * 128);
-            for (int h = 0; h < 2; ++h)
-              for (int bb = 0; bb < nb; ++bb)
-                ptx::tma_load_2d(db + h * (kXBBytes / 2) + bb * kXBRows * 128, tb,
-                                 g * 128 + h * 64, itm.z + bb * kXBRows, &fullb[s], pol);
-          }
+        const int nbx = (itm.w + kXBRows - 1) / kXBRows;  // activation box: 32 * nbx rows
+        for (int g = 0; g < ng; ++g) {
+          const uint32_t sq = nq % kXQS;
+          if (!ptx::mbar_wait(&bars->q_empty[sq], ((nq / kXQS) & 1) ^ 1, abort, budget)) { stop = true; break; }
+          uint8_t *dq = smem + kXOffQ + sq * kXQBytes;
+          ptx::mbar_expect_tx(&bars->q_full[sq], kXQBytes);
+          if (MODE == kXGateUp)
+            ptx::tma_load_3d(dq, &maps.a[sh ? 1 : 0], g * 128, rA, 0, &bars->q_full[sq], pol_w);
+          else
+            ptx::tma_load_2d(dq, &maps.a[sh ? 1 : 0], g * 128, rA, &bars->q_full[sq], pol_w);
+          ++nq;
+          const uint32_t sb = nb % kXBS;
+          if (!ptx::mbar_wait(&bars->b_empty[sb], ((nb / kXBS) & 1) ^ 1, abort, budget)) { stop = true; break; }
+          uint8_t *db = smem + kXOffB + sb * kXBBytes;
+          ptx::mbar_expect_tx(&bars->b_full[sb], 2u * nbx * kXBRows * 128);
+          ptx::tma_load_3d(db, &maps.b[sh ? 1 : 0][nbx - 1], 0, itm.z, 2 * g, &bars->b_full[sb],
+                           pol_x);
+          ++nb;
         }
       }
       // After an abort, the copies still in flight must land before the CTA
-      // exits: wait (bounded) for the last stages issued on this ring.
+      // exits: wait (bounded) for the last stages issued on each ring.
       if (*abort) {
         int never = 0;
-        for (uint32_t k = 0; k < static_cast<uint32_t>(depth) && k < n; ++k) {
-          const uint32_t j = n - 1 - k;
-          ptx::mbar_wait(&fullb[j % depth], (j / depth) & 1, &never, budget);
+        for (uint32_t k = 0; k < kXQS && k < nq; ++k) {
+          const uint32_t j = nq - 1 - k;
+          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, budget);
+        }
+        for (uint32_t k = 0; k < kXBS && k < nb; ++k) {
+          const uint32_t j = nb - 1 - k;
+          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, budget);
         }
       }
     }
-  } else if (warp == 1 || warp == kMma1) {
-    // -------------------------------------------- MMA issuers (even, odd)
+  } else if (warp == 1 || warp == kMma1 || warp == kMma2) {
+    // ------------------------------------ MMA issuers (groups mod kIssuers)
     if (lane == 0) {
-      const uint32_t par = warp == 1 ? 0 : 1;
+      const uint32_t par = warp == 1 ? 0 : warp == kMma1 ? 1 : 2;
       uint32_t gs = 0;
       bool issued = false;
       for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
         const int4 itm = p.items[it];
         const int ng = groups_of(itm);
         const int n16 = (itm.w + 15) & ~15;
+        const uint32_t bhalf = static_cast<uint32_t>((itm.w + kXBRows - 1) / kXBRows) * kXBRows * 128;
         const uint32_t idesc = MODE == kXGateUp ? ptx::idesc_f16_f32(128, n16)
                                                 : ptx::idesc_bf16_f32(128, n16);
         for (int g = 0; g < ng; ++g, ++gs) {
-          if ((gs & 1) != par) continue;
+          if (gs % kIssuers != par) continue;
           const int sa = gs % kXAS, sb = gs % kXBS, pb = gs % kXPS;
           if (!ptx::mbar_wait(&bars->a_full[sa], (gs / kXAS) & 1, abort, budget)) break;
           if (!ptx::mbar_wait(&bars->b_full[sb], (gs / kXBS) & 1, abort, budget)) break;
@@ -247,8 +256,8 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           const uint32_t b0 = ptx::smem_u32(smem + kXOffB + sb * kXBBytes);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {  // K = 16 per instruction: 8 TMEM columns of A
-            const uint32_t boff = (k >> 2) * (kXBBytes / 2) + (k & 3) * 32;
-            ptx::mma_tmem_a(tmem + kXColP + pb * 128, tmem + sa * 64 + k * 8,
+            const uint32_t boff = (k >> 2) * bhalf + (k & 3) * 32;
+            ptx::mma_tmem_a(tmem + x_pcol(pb), tmem + x_acol(sa, k >> 2) + (k & 3) * 8,
                             ptx::sw128_desc(b0 + boff), idesc, k > 0);
           }
           ptx::mma_commit(&bars->a_empty[sa]);
@@ -282,16 +291,16 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint4 q[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
-        const uint32_t ta = tmem + tl + sa * 64;
+        const uint32_t ta0 = tmem + tl + x_acol(sa, 0), ta1 = tmem + tl + x_acol(sa, 1);
         uint32_t v0[32], v1[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) cvt_chunk<MODE>(q[c], v0 + 8 * c);
-        ptx::tmem_st32(ta, v0);
+        ptx::tmem_st32(ta0, v0);
 #pragma unroll
         for (int c = 0; c < 4; ++c) cvt_chunk<MODE>(q[4 + c], v1 + 8 * c);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bars->q_empty[sq]);
-        ptx::tmem_st32(ta + 32, v1);
+        ptx::tmem_st32(ta1, v1);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
@@ -301,10 +310,10 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   } else {
     // --------------------------------------------- promoters + epilogue
     const int quarter = warp & 3;
-    const int ch = (warp - kConv0 - kConv) >> 2;  // column blocks ch, ch + 2, ch + 4, ch + 6
+    const int ch = (warp - kConv0 - kConv) >> 2;  // column blocks ch, ch + 2, ch + 4
     const int r = quarter * 32 + lane;       // tile row of this thread
     const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
-    float acc[64];
+    float acc[48];
     uint32_t gs = 0, n_done = 0;
     bool ok = true;
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++n_done) {
@@ -335,10 +344,10 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           if (g0 + i < ng) sw[i >> 1] |= static_cast<uint32_t>(srow[g0 + i]) << (16 * (i & 1));
       };
       load_scales(0);
-      float cs[4];  // gate|up: 2^s of the column's token; down: combine weight
-      int ct[4];    // down: the column's token
+      float cs[3];  // gate|up: 2^s of the column's token; down: combine weight
+      int ct[3];    // down: the column's token
 #pragma unroll
-      for (int jb = 0; jb < 4; ++jb) {
+      for (int jb = 0; jb < 3; ++jb) {
         cs[jb] = 0.0f;
         ct[jb] = 0;
         const int cl = (ch + 2 * jb) * 16 + (lane & 15);
@@ -356,15 +365,15 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
       }
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < 48; ++j) acc[j] = 0.0f;
       for (int g = 0; g < ng; ++g, ++gs) {
         const int pb = gs % kXPS;
         if (!ptx::mbar_wait(&bars->p_full[pb], (gs / kXPS) & 1, abort, budget)) { ok = false; break; }
         ptx::tc_fence_after();
         const float sc = bf16_lo(sw[0]);
-        const uint32_t tb = tmem + tl + kXColP + pb * 128;
+        const uint32_t tb = tmem + tl + x_pcol(pb);
 #pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
+        for (int jb = 0; jb < 3; ++jb) {
           const int b = ch + 2 * jb;
           if (b < nblk) {
             float v[16];
@@ -394,7 +403,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if (r >= 64) {  // up rows hand their accumulators to the gate rows
           if (!ptx::mbar_wait(&bars->xch_empty, par ^ 1, abort, budget)) break;
 #pragma unroll
-          for (int jb = 0; jb < 4; ++jb) {
+          for (int jb = 0; jb < 3; ++jb) {
             const int b = ch + 2 * jb;
             if (b < nblk) {
 #pragma unroll
@@ -409,7 +418,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           moe_bf16 *hout = sh ? p.h_shared : p.h_routed;
           const int i = itm.y * 64 + r;
 #pragma unroll
-          for (int jb = 0; jb < 4; ++jb) {
+          for (int jb = 0; jb < 3; ++jb) {
             const int b = ch + 2 * jb;
             if (b < nblk) {
 #pragma unroll
@@ -435,7 +444,7 @@ tc_expert_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const bool lo2 = (q4 & 2) == 0, odd = (q4 & 1) != 0;
         const int nrow4 = itm.y * 128 + quarter * 32 + (lane & ~3);
 #pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
+        for (int jb = 0; jb < 3; ++jb) {
           const int b = ch + 2 * jb;
           if (b < nblk) {
 #pragma unroll
@@ -516,7 +525,7 @@ lists_items_kernel(const int32_t *__restrict__ ids, int T, Lists L, int I, int I
   __syncthreads();
   const int c = tid < kE ? hist[tid] : 0;
   const int off = block_exclusive_scan_256(c, scan_tmp);
-  const int tl = block_exclusive_scan_256((c + 127) / 128, scan_tmp);
+  const int tl = block_exclusive_scan_256((c + kXTile - 1) / kXTile, scan_tmp);
   if (tid < kE) { pre[tid] = off; tpre[tid] = tl; }
   __syncthreads();
   const int cnt = hist[e], base = pre[e];
@@ -576,24 +585,24 @@ lists_items_kernel(const int32_t *__restrict__ ids, int T, Lists L, int I, int I
   }
   // work items of expert e
   const int mg = I / 64, md = H / 128;
-  const int tiles = (cnt + 127) / 128, tb = tpre[e];
+  const int tiles = (cnt + kXTile - 1) / kXTile, tb = tpre[e];
   for (int k = tid; k < tiles * (mg + md); k += kLiThreads) {
     const int nt = k / (mg + md), m = k % (mg + md);
-    const int first = base + nt * 128, nn = min(128, cnt - nt * 128);
+    const int first = base + nt * kXTile, nn = min(kXTile, cnt - nt * kXTile);
     if (m < mg) gu[(tb + nt) * mg + m] = make_int4(e, m, first, nn);
     else dn[(tb + nt) * md + (m - mg)] = make_int4(e, m - mg, first, nn);
   }
   if (e == 0) {
-    const int nr = tpre[kE - 1] + (hist[kE - 1] + 127) / 128;  // all routed tiles
-    const int ts = Is > 0 ? (T + 127) / 128 : 0;
+    const int nr = tpre[kE - 1] + (hist[kE - 1] + kXTile - 1) / kXTile;  // all routed tiles
+    const int ts = Is > 0 ? (T + kXTile - 1) / kXTile : 0;
     const int mgs = Is / 64;
     for (int k = tid; k < ts * mgs; k += kLiThreads) {
       const int nt = k / mgs, m = k % mgs;
-      gu[nr * mg + k] = make_int4(kE, m, nt * 128, min(128, T - nt * 128));
+      gu[nr * mg + k] = make_int4(kE, m, nt * kXTile, min(kXTile, T - nt * kXTile));
     }
     for (int k = tid; k < ts * md; k += kLiThreads) {
       const int nt = k / md, m = k % md;
-      dn[nr * md + k] = make_int4(kE, m, nt * 128, min(128, T - nt * 128));
+      dn[nr * md + k] = make_int4(kE, m, nt * kXTile, min(kXTile, T - nt * kXTile));
     }
     if (tid == 0) {
       *n_gu = nr * mg + ts * mgs;
@@ -697,8 +706,7 @@ __global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
 }
 
 template <int MODE>
-cudaError_t launch_x(const CUtensorMap &a, const CUtensorMap &as, const CUtensorMap &b,
-                     const CUtensorMap &bs, const XParams &p, cudaStream_t s) {
+cudaError_t launch_x(const XMaps &maps, const XParams &p, cudaStream_t s) {
   static bool attr[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -709,15 +717,15 @@ cudaError_t launch_x(const CUtensorMap &a, const CUtensorMap &as, const CUtensor
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
-  tc_expert_kernel<MODE><<<tc_sm_count(), kXThreads, kXSmem, s>>>(a, as, b, bs, p);
+  tc_expert_kernel<MODE><<<tc_sm_count(), kXThreads, kXSmem, s>>>(maps, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t tc_items_bytes(int T, int I, int Is, int H) {
-  const size_t tiles = static_cast<size_t>(T) * kK / 128 + kE;
-  const size_t ts = (static_cast<size_t>(T) + 127) / 128;
+  const size_t tiles = static_cast<size_t>(T) * kK / kXTile + kE;
+  const size_t ts = (static_cast<size_t>(T) + kXTile - 1) / kXTile;
   const size_t gu = tiles * (I / 64) + ts * (Is / 64);
   const size_t dn = tiles * (H / 128) + ts * (H / 128);
   return (gu + dn + 16) * sizeof(int4);
@@ -737,8 +745,8 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
     if (e_ != cudaSuccess) return e_;          \
   } while (0)
   int4 *gu = items;
-  const size_t tiles = static_cast<size_t>(T) * kK / 128 + kE;
-  const size_t ts = (static_cast<size_t>(T) + 127) / 128;
+  const size_t tiles = static_cast<size_t>(T) * kK / kXTile + kE;
+  const size_t ts = (static_cast<size_t>(T) + kXTile - 1) / kXTile;
   int4 *dn = items + tiles * (I / 64) + ts * (Is / 64);
   lists_items_kernel<<<kE, kLiThreads, 0, s>>>(ids, T, L, I, Is, H, gu, counters, dn,
                                               counters + 1, status);
@@ -747,21 +755,44 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                                                    out_acc);
   TC_STEP(cudaGetLastError());
   const size_t rows_r = static_cast<size_t>(T) * kK;
-  CUtensorMap a13, a13s, bx, bxs, a2, a2s, bh, bhs;
+  // Activation maps: (64 elements, rows, K / 64 chunks), chunk stride 128 B,
+  // boxes (64, 32 * i, 2).
+  auto act_maps = [&](CUtensorMap (&m)[3], const void *base, CUtensorMapDataType dt,
+                      uint64_t rows, uint64_t K) {
+    const uint64_t dims[3] = {64, rows, K / 64};
+    const uint64_t strides[2] = {K * 2, 128};
+    bool ok = true;
+    for (int i = 0; i < 3; ++i) {
+      const uint32_t box[3] = {64, static_cast<uint32_t>(kXBRows * (i + 1)), 2};
+      ok = ok && tc_make_map3(&m[i], base, dt, 2, dims, strides, box);
+    }
+    return ok;
+  };
+  XMaps gm{}, dm{};
   const bool shared = Is > 0;
-  bool ok = tc_make_map(&a13, w.w13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                        static_cast<uint64_t>(kE) * 2 * I, H, 64, 128) &&
-            tc_make_map(&bx, xs16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_r, H, kXBRows, 64) &&
-            tc_make_map(&a2, w.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                        static_cast<uint64_t>(kE) * H, I, 64, 128) &&
-            tc_make_map(&bh, h_routed, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows_r, I, kXBRows, 64);
-  if (shared)
-    ok = ok && tc_make_map(&a13s, w.ws13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * Is, H, 64, 128) &&
-         tc_make_map(&bxs, x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, T, H, kXBRows, 64) &&
-         tc_make_map(&a2s, w.ws2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, Is, 64, 128) &&
-         tc_make_map(&bhs, h_shared, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, Is, kXBRows, 64);
-  else {
-    a13s = a13; bxs = bx; a2s = a2; bhs = bh;
+  bool ok;
+  {  // gate|up weights: (H, rows, gate|up) with the up rows I rows after the gate rows
+    const uint64_t dims[3] = {static_cast<uint64_t>(H), static_cast<uint64_t>(kE) * 2 * I, 2};
+    const uint64_t strides[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(I) * H};
+    const uint32_t box[3] = {128, 64, 2};
+    ok = tc_make_map3(&gm.a[0], w.w13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dims, strides, box);
+  }
+  ok = ok && act_maps(gm.b[0], xs16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rows_r, H) &&
+       tc_make_map(&dm.a[0], w.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                   static_cast<uint64_t>(kE) * H, I, 128, 128) &&
+       act_maps(dm.b[0], h_routed, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows_r, I);
+  if (shared) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(H), 2 * static_cast<uint64_t>(Is), 2};
+    const uint64_t strides[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Is) * H};
+    const uint32_t box[3] = {128, 64, 2};
+    ok = ok && tc_make_map3(&gm.a[1], w.ws13_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dims, strides,
+                            box) &&
+         act_maps(gm.b[1], x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, T, H) &&
+         tc_make_map(&dm.a[1], w.ws2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, Is, 128, 128) &&
+         act_maps(dm.b[1], h_shared, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, T, Is);
+  } else {
+    gm.a[1] = gm.a[0]; dm.a[1] = dm.a[0];
+    for (int i = 0; i < 3; ++i) { gm.b[1][i] = gm.b[0][i]; dm.b[1][i] = dm.b[0][i]; }
   }
   if (!ok) return cudaErrorInvalidValue;
   XParams p{};
@@ -772,7 +803,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   p.xscale = xscale; p.perm = L.perm;
   p.h_routed = h_routed; p.h_shared = h_shared;
   p.status = status; p.budget_ns = tc_wait_budget_ns();
-  TC_STEP(launch_x<kXGateUp>(a13, a13s, bx, bxs, p, s));
+  TC_STEP(launch_x<kXGateUp>(gm, p, s));
   XParams q{};
   q.items = dn; q.n_items = counters + 1;
   q.K_routed = I; q.K_shared = Is;
@@ -780,7 +811,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   q.s_routed = w.w2_s; q.s_shared = w.ws2_s;
   q.out_acc = out_acc; q.perm = L.perm; q.weights = weights; q.sgate = sgate; q.H = H;
   q.status = status; q.budget_ns = tc_wait_budget_ns();
-  TC_STEP(launch_x<kXDown>(a2, a2s, bh, bhs, q, s));
+  TC_STEP(launch_x<kXDown>(dm, q, s));
   const size_t n4 = static_cast<size_t>(T) * H / 4;
   acc_to_bf16_kernel<<<tc_sm_count() * 4, 256, 0, s>>>(out_acc, n4, out);
   TC_STEP(cudaGetLastError());

@@ -196,6 +196,21 @@ bool tc_make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tc_make_map3(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
+                  const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]) {
+  EncodeTiledFn enc = encoder();
+  if (!enc || !base) return false;
+  const cuuint64_t gdim[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t gstride[2] = {strides[0], strides[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  (void)esize;
+  return enc(m, dt, 3, const_cast<void *>(base), gdim, gstride, bx, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_sm_count() {
   static int n[64] = {0};
   int dev = 0;
