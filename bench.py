@@ -26,6 +26,7 @@ the same workload on its own GPU and `value` sums the ranks' tokens.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -35,6 +36,8 @@ import tempfile
 import time
 
 import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -136,6 +139,38 @@ def down_bytes(d: W.Dims, T: int, n_active: int):
     per = H * I + 2 * H * (I // G)
     sh = H * Is + 2 * H * (Is // G) if Is else 0
     return n_active * per + sh + 2 * (T * 8 * I + T * Is) + 2 * T * H
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
+# one ncu capture of each kernel (summaries under profiles/), valid only while
+# the kernel's sources hash to the value recorded with the capture.
+MEASURED_TRAFFIC = {
+    "decode_fused": {"bytes": 529.0e6, "workload": "verify_T32",
+                     "sources": ["decode_fused.cu", "common.cuh", "select.cuh", "sm100_ptx.cuh"],
+                     "sha256_16": "20609ec655a8ff00",
+                     "profile": "profiles/decode_fused_verify_T32.md"},
+    "gateup_swiglu_tc": {"bytes": 645.0e6, "workload": "prefill_T2048",
+                         "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],
+                         "sha256_16": "e9de3cd0acd53d86",
+                         "profile": "profiles/tc_expert_prefill_T2048.md"},
+    "down_combine_tc": {"bytes": 314.5e6, "workload": "prefill_T2048",
+                        "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],
+                        "sha256_16": "e9de3cd0acd53d86",
+                        "profile": "profiles/tc_expert_prefill_T2048.md"},
+}
+
+
+def measured_traffic(kname: str, workload: str):
+    """The captured traffic of kname on this workload, or None when there is
+    no capture or the kernel's sources changed since it was taken."""
+    m = MEASURED_TRAFFIC.get(kname)
+    if not m or m["workload"] != workload:
+        return None
+    h = hashlib.sha256()
+    for f in m["sources"]:
+        with open(os.path.join(HERE, "sparse_moe_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return m["bytes"] if h.hexdigest()[:16] == m["sha256_16"] else None
 
 
 def kernel_bytes(kname: str, d: W.Dims, T: int, n_active: int):
@@ -336,6 +371,9 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOAD_T), default="verify")
     ap.add_argument("--only", action="store_true", help="time only --workload")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--banks", type=int, default=0,
+                    help="weight banks (default 16 for T <= 32, else 2); fewer keep a "
+                         "profiler capture small, and a bench line taken with them says so")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -393,7 +431,7 @@ def main():
     head = None
     for name in order:
         T = WORKLOAD_T[name]
-        banks = 16 if T <= 32 else 2
+        banks = args.banks if args.banks > 0 else (16 if T <= 32 else 2)
         b = Bench(name, moe, torch, dev, banks)
         ms, wall, per_kernel, clk = b.run(args.steps, args.warmup, barrier, local)
         ms = max_all(ms)
@@ -437,7 +475,8 @@ def main():
         kbytes = head["algorithmic_bytes"]
     achieved = kbytes / (kms * 1e-3) / 1e9
     roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+            "traffic": measured_traffic(kname, LABEL[args.workload]),
             "peak_src": pk["src"] + " (copy, burst)", "kernel_ms": kms,
             "algorithmic_bytes_per_launch": kbytes}
     cb = cpu_baseline(args.workload, budget_s=args.cpu_budget) if world == 1 or rank == 0 else None
