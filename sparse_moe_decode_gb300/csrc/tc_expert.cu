@@ -1,34 +1,30 @@
-// tc_expert.cu -- prefill-size T: the expert SwiGLU (gate|up, A4/A6) and the
-// down projection with the weighted combine (A5/A6/A7) as grouped GEMMs on
-// the 5th-generation tensor cores, with the dequantised weight operand held
-// in tensor memory.
+// tc_expert.cu -- prefill-size T: the expert gate|up projections with the
+// SwiGLU (A4/A6), the down projection with the weighted combine (A5/A6/A7),
+// the token -> expert lists and work items (A3) and the tokens' fp16 copies,
+// as grouped GEMMs on the 5th-generation tensor cores with the dequantised
+// weight operand held in tensor memory.
 //
 // Orientation: D[row, token] = sum_k W[row, k] * X[token, k].  128 weight
 // rows are the M operand (one TMEM lane each), the tokens of one expert tile
 // are N (<= 96): each weight tile is streamed from HBM once for all of its
 // expert's tokens (an expert with more than 96 tokens gets several tiles).
 //
-// Per 128-wide K group (one quantisation group):
-//   TMA         int8 tile 128 x 128 (128-byte swizzle) -> shared ring Q
-//   converters  Q row -> exact fp16 (gate|up) or bf16 (down) -> TMEM A stage
-//               (tcgen05.st; |q| <= 127 is exact in either type)
-//   TMA         activation tile N x 128 -> shared ring B (4 stages)
-//   MMA thread  P = A[TMEM] x B[smem]^T into one of three TMEM partial buffers
-//   promoters   acc[row][token] += s[row][group] * P (fp32 registers)
-// so the product q * s is never rounded ("scale promotion").  The gate|up
-// activations are each token's copy scaled by a power of two into fp16
-// (exact for every element within 2^29 of the token's largest), undone on the
-// fp32 results; the down activations h are bf16 as the SwiGLU rounds them.
+// gate|up (gateup_split_kernel): the weights become two exact fp16 operands
+// (the group scale split in two, below) and the MMAs sum the whole reduction
+// in TMEM.
 //
-// Warp roles (512 threads): warp 0 issues the TMA loads (one copy of the
-// weight tile and one of the activation tile per K group), warps 1, 2 and
-// 15 issue the MMAs of the K groups g with g mod 3 = 0, 1, 2 (one issuing
-// thread sustains only about one tcgen05 instruction per hundred cycles, so
-// several multiply the tensor rate at these N), warp 1 also owns TMEM, warps
-// 3..6 convert (one per TMEM lane quarter), warps 7..14 promote and run the
-// epilogue (two per lane quarter, splitting the token columns).  Every wait is bounded by a %globaltimer budget; on expiry
-// the CTA drains what it has in flight, frees TMEM, sets MOE_DEV_TIMEOUT and
-// returns.
+// down (down_tc_kernel), per 128-wide K group (one quantisation group):
+//   TMA         int8 tile 128 x 128 (128-byte swizzle) -> shared ring Q
+//   converters  Q row -> exact bf16 -> TMEM A stage (tcgen05.st; |q| <= 127
+//               is exact in bf16)
+//   TMA         activation tile N x 128 -> shared ring B (4 stages)
+//   MMA         P = A[TMEM] x B[smem]^T into one of three TMEM partial buffers
+//   promoters   acc[row][token] += s[row][group] * P (fp32 registers)
+// so the product q * s is never rounded ("scale promotion"); the epilogue
+// adds w * acc to the fp32 output rows with vector reductions.
+//
+// Every wait is bounded by a %globaltimer budget; on expiry the CTA drains
+// what it has in flight, frees TMEM, sets MOE_DEV_TIMEOUT and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -73,8 +69,6 @@ constexpr size_t kXOffBar = kXOffX + kXXchBytes;
 constexpr size_t kXSmem = kXOffBar + 512 + 1024;  // + barriers + alignment slack
 static_assert(kXSmem <= 232448, "shared memory per CTA");
 
-enum XMode : int { kXGateUp = 0, kXDown = 1 };
-
 struct XBars {
   uint64_t q_full[kXQS], q_empty[kXQS], a_full[kXAS], a_empty[kXAS], b_full[kXBS],
       b_empty[kXBS];
@@ -111,29 +105,28 @@ struct XParams {
   unsigned long long budget_ns;
 };
 
-// 16 int8 (one 16-byte chunk) -> 8 32-bit TMEM columns of two 16-bit values.
-template <int MODE>
-__device__ __forceinline__ void cvt_chunk(const uint4 q, uint32_t *o) {
-  if (MODE == kXGateUp) {
-    i8x4_to_f16x2(q.x, o[0], o[1]);
-    i8x4_to_f16x2(q.y, o[2], o[3]);
-    i8x4_to_f16x2(q.z, o[4], o[5]);
-    i8x4_to_f16x2(q.w, o[6], o[7]);
-  } else {
-    // exact fp32 values; bf16 keeps their upper halves (<= 8 significant bits)
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// 16 int8 (one 16-byte chunk) -> 8 32-bit TMEM columns of two bf16 values:
+// exact fp32 values, of which bf16 keeps the upper halves (<= 8 significant
+// bits).
+__device__ __forceinline__ void cvt_chunk_bf16(const uint4 q, uint32_t *o) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const f4 a = i8x4_to_f32(w[i]);
-      o[2 * i] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
-      o[2 * i + 1] = __byte_perm(__float_as_uint(a.z), __float_as_uint(a.w), 0x7632);
-    }
+  for (int i = 0; i < 4; ++i) {
+    const f4 a = i8x4_to_f32(w[i]);
+    o[2 * i] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
+    o[2 * i + 1] = __byte_perm(__float_as_uint(a.z), __float_as_uint(a.w), 0x7632);
   }
 }
 
-template <int MODE>
+// Warp roles (512 threads): warp 0 issues the TMA copies (one of the weight
+// tile and one of the activation tile per K group), warps 1, 2 and 15 issue
+// the MMAs of the K groups g with g mod 3 = 0, 1, 2 (one issuing thread
+// sustains only about one tcgen05 instruction per hundred cycles), warp 1
+// also owns TMEM, warps 3..6 convert (one per TMEM lane quarter), warps 7..14
+// promote and run the epilogue (two per lane quarter, splitting the token
+// columns).
 __global__ void __launch_bounds__(kXThreads, 1)
-tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
+down_tc_kernel(const __grid_constant__ XMaps maps, const XParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -193,22 +186,14 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
         const int4 itm = p.items[it];
         const bool sh = itm.x == kE;
         const int ng = groups_of(itm);
-        int rA;
-        if (MODE == kXGateUp) {  // first gate row; the up rows follow I (Is) rows later
-          rA = (sh ? 0 : itm.x * 2 * p.rows_routed) + itm.y * 64;
-        } else {
-          rA = (sh ? 0 : itm.x * p.rows_routed) + itm.y * 128;
-        }
+        const int rA = (sh ? 0 : itm.x * p.rows_routed) + itm.y * 128;
         const int nbx = (itm.w + kXBRows - 1) / kXBRows;  // activation box: 32 * nbx rows
         for (int g = 0; g < ng; ++g) {
           const uint32_t sq = nq % kXQS;
           if (!ptx::mbar_wait(&bars->q_empty[sq], ((nq / kXQS) & 1) ^ 1, abort, budget)) { stop = true; break; }
           uint8_t *dq = smem + kXOffQ + sq * kXQBytes;
           ptx::mbar_expect_tx(&bars->q_full[sq], kXQBytes);
-          if (MODE == kXGateUp)
-            ptx::tma_load_3d(dq, &maps.a[sh ? 1 : 0], g * 128, rA, 0, &bars->q_full[sq], pol_w);
-          else
-            ptx::tma_load_2d(dq, &maps.a[sh ? 1 : 0], g * 128, rA, &bars->q_full[sq], pol_w);
+          ptx::tma_load_2d(dq, &maps.a[sh ? 1 : 0], g * 128, rA, &bars->q_full[sq], pol_w);
           ++nq;
           const uint32_t sb = nb % kXBS;
           if (!ptx::mbar_wait(&bars->b_empty[sb], ((nb / kXBS) & 1) ^ 1, abort, budget)) { stop = true; break; }
@@ -244,8 +229,7 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
         const int ng = groups_of(itm);
         const int n16 = (itm.w + 15) & ~15;
         const uint32_t bhalf = static_cast<uint32_t>((itm.w + kXBRows - 1) / kXBRows) * kXBRows * 128;
-        const uint32_t idesc = MODE == kXGateUp ? ptx::idesc_f16_f32(128, n16)
-                                                : ptx::idesc_bf16_f32(128, n16);
+        const uint32_t idesc = ptx::idesc_bf16_f32(128, n16);
         for (int g = 0; g < ng; ++g, ++gs) {
           if (gs % kIssuers != par) continue;
           const int sa = gs % kXAS, sb = gs % kXBS, pb = gs % kXPS;
@@ -294,10 +278,10 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
         const uint32_t ta0 = tmem + tl + x_acol(sa, 0), ta1 = tmem + tl + x_acol(sa, 1);
         uint32_t v0[32], v1[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cvt_chunk<MODE>(q[c], v0 + 8 * c);
+        for (int c = 0; c < 4; ++c) cvt_chunk_bf16(q[c], v0 + 8 * c);
         ptx::tmem_st32(ta0, v0);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cvt_chunk<MODE>(q[4 + c], v1 + 8 * c);
+        for (int c = 0; c < 4; ++c) cvt_chunk_bf16(q[4 + c], v1 + 8 * c);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&bars->q_empty[sq]);
         ptx::tmem_st32(ta1, v1);
@@ -321,17 +305,10 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
       const bool sh = itm.x == kE;
       const int ng = groups_of(itm);
       const int n = itm.w, nblk = (n + 15) >> 4;
-      const moe_bf16 *srow;  // this row's group scales
-      if (MODE == kXGateUp) {
-        const int half = sh ? p.rows_shared : p.rows_routed;
-        const int rr = r < 64 ? itm.y * 64 + r : half + itm.y * 64 + (r - 64);
-        srow = (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * 2 * half * ng) +
-               static_cast<size_t>(rr) * ng;
-      } else {
-        const int rr = itm.y * 128 + r;
-        srow = (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * p.rows_routed * ng) +
-               static_cast<size_t>(rr) * ng;
-      }
+      // this row's group scales
+      const moe_bf16 *srow =
+          (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * p.rows_routed * ng) +
+          static_cast<size_t>(itm.y * 128 + r) * ng;
       // The row's group scales, 16 at a time, packed two per word and
       // consumed from the low half; the per-column data of the epilogue.
       // Both are loaded here so that their latency hides behind the groups.
@@ -344,7 +321,7 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
           if (g0 + i < ng) sw[i >> 1] |= static_cast<uint32_t>(srow[g0 + i]) << (16 * (i & 1));
       };
       load_scales(0);
-      float cs[3];  // gate|up: 2^s of the column's token; down: combine weight
+      float cs[3];  // the column's combine weight
       int ct[3];    // down: the column's token
 #pragma unroll
       for (int jb = 0; jb < 3; ++jb) {
@@ -352,9 +329,7 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
         ct[jb] = 0;
         const int cl = (ch + 2 * jb) * 16 + (lane & 15);
         if (cl < n) {
-          if (MODE == kXGateUp) {
-            if (r < 64) cs[jb] = p.xscale[sh ? itm.z + cl : p.perm[itm.z + cl] / kK];
-          } else if (sh) {
+          if (sh) {
             ct[jb] = itm.z + cl;
             cs[jb] = p.sgate ? p.sgate[itm.z + cl] : 0.0f;
           } else {
@@ -397,46 +372,7 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
       if (!ok) break;
       // ------------------------------------------------------ epilogue
       // acc[jb * 16 + j] is column (ch + 2 * jb) * 16 + j of this row
-      if (MODE == kXGateUp) {
-        float *xch = reinterpret_cast<float *>(smem + kXOffX);
-        const uint32_t par = n_done & 1;
-        if (r >= 64) {  // up rows hand their accumulators to the gate rows
-          if (!ptx::mbar_wait(&bars->xch_empty, par ^ 1, abort, budget)) break;
-#pragma unroll
-          for (int jb = 0; jb < 3; ++jb) {
-            const int b = ch + 2 * jb;
-            if (b < nblk) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) xch[(b * 16 + j) * 64 + (r - 64)] = acc[jb * 16 + j];
-            }
-          }
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&bars->xch_full);
-        } else {
-          if (!ptx::mbar_wait(&bars->xch_full, par, abort, budget)) break;
-          const int Irows = sh ? p.rows_shared : p.rows_routed;
-          moe_bf16 *hout = sh ? p.h_shared : p.h_routed;
-          const int i = itm.y * 64 + r;
-#pragma unroll
-          for (int jb = 0; jb < 3; ++jb) {
-            const int b = ch + 2 * jb;
-            if (b < nblk) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int col = b * 16 + j;
-                const float sj = __shfl_sync(0xFFFFFFFFu, cs[jb], j);  // lane j holds column j's
-                if (col < n) {
-                  const float u = xch[col * 64 + r] * sj;
-                  hout[static_cast<size_t>(itm.z + col) * Irows + i] =
-                      f32_to_bf16(silu_mul(acc[jb * 16 + j] * sj, u));
-                }
-              }
-            }
-          }
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&bars->xch_empty);
-        }
-      } else {
+      {
         // Weighted combine, out_acc[t][row] += w * acc: a 4 x 4 transpose
         // among each four lanes leaves every lane four consecutive rows of
         // one column, added with one 16-byte reduction.
@@ -470,6 +406,367 @@ tc_expert_kernel(const __grid_constant__ XMaps maps, const XParams p) {
             }
           }
         }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kXTmemCols);
+  }
+  if (threadIdx.x == 0 && bars->abort) set_status(p.status, MOE_DEV_TIMEOUT);
+}
+
+// ------------------------------ gate|up with the scales split (no promotion)
+//
+// Every bf16 group scale s = m * 2^E (m an 8-bit integer significand) is
+// split as s = s_a + s_b, s_a = (m & 0xF0) * 2^E, s_b = (m & 0x0F) * 2^E.
+// Then q * s_a and q * s_b (|q| <= 127) have at most 11 significant bits each
+// and, scaled by a per-row power of two 2^-e (e from the row's largest group
+// exponent), are exact fp16 values for every group whose scale is within
+// 2^21 of the row's largest.  The weight row becomes two fp16 rows A1 = q *
+// s_a * 2^-e and A2 = q * s_b * 2^-e, and the MMAs accumulate A1 x B and
+// A2 x B over the whole reduction in TMEM: the products are exact and the
+// scales need no promotion.  2^e (per row) and 2^s (per token) are applied to
+// the fp32 sums in the epilogue.  The conversion is one fp16 FMA per pair of
+// weights: with u = q + 128 placed in the mantissa of 1024 (1024 + u exact),
+// (1024 + u) * s' - 1152 * s' = q * s' is rounded once, and is exact.
+//
+// Warp roles (480 threads): warp 0 issues the TMA copies, warp 1 the MMAs of
+// A1 and warp 2 those of A2 of every K group, each into its own accumulator
+// (the epilogue adds the two), warps 3..6 convert (one per TMEM lane
+// quarter), warps 7..14 run the epilogue (two per lane quarter, splitting the
+// token columns).
+constexpr int kGThreads = 480;
+constexpr int kGConv0 = 3;  // converter warps 3..6; epilogue warps 7..14
+constexpr int kGAS = 2;     // TMEM A stages (one per issuer)
+constexpr int kGEpi = 8;
+
+// TMEM: A stage sa at [128 sa, 128 sa + 128): A1 in its first 64 columns, A2
+// in the next 64; accumulator of issuer i at 256 + 128 i (96 wide).
+__host__ __device__ constexpr uint32_t g_acol(int sa, int part) { return 128u * sa + 64u * part; }
+__host__ __device__ constexpr uint32_t g_dcol(int i) { return 256u + 128u * i; }
+static_assert(g_dcol(1) + kXTile <= kXTmemCols, "tensor memory columns");
+
+struct GBars {
+  uint64_t q_full[kXQS], q_empty[kXQS], a_full[kGAS], a_empty[kGAS], b_full[kXBS],
+      b_empty[kXBS];
+  uint64_t d_full[2], d_empty[2], done[2], xch_full, xch_empty;
+  uint32_t tmem_holder;
+  int abort;
+};
+static_assert(sizeof(GBars) <= 512, "barrier block");
+
+// Exponent field of the largest nonzero |scale| among the row's ng groups,
+// clamped so that 2^-e and 2^e below are normal floats.
+__device__ __forceinline__ int row_scale_exp(const moe_bf16 *srow, int ng) {
+  int ef = 0;
+  for (int g = 0; g < ng; ++g) ef = max(ef, static_cast<int>((srow[g] >> 7) & 0xFF));
+  return max(8, min(254, ef));
+}
+
+__global__ void __launch_bounds__(kGThreads, 1)
+gateup_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  GBars *bars = reinterpret_cast<GBars *>(smem + kXOffBar);
+  volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *p.n_items;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kXQS; ++i) {
+      ptx::mbar_init(&bars->q_full[i], 1);
+      ptx::mbar_init(&bars->q_empty[i], kConv);
+    }
+    for (int i = 0; i < kGAS; ++i) {
+      ptx::mbar_init(&bars->a_full[i], kConv);
+      ptx::mbar_init(&bars->a_empty[i], 2);  // both issuers
+    }
+    for (int i = 0; i < kXBS; ++i) {
+      ptx::mbar_init(&bars->b_full[i], 1);
+      ptx::mbar_init(&bars->b_empty[i], 2);  // both issuers
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->d_full[i], 1);
+      ptx::mbar_init(&bars->d_empty[i], kGEpi);
+      ptx::mbar_init(&bars->done[i], 1);
+    }
+    ptx::mbar_init(&bars->xch_full, kGEpi / 2);   // the warps holding up rows
+    ptx::mbar_init(&bars->xch_empty, kGEpi / 2);  // the warps holding gate rows
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_holder, kXTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_holder;
+  const uint64_t budget = p.budget_ns;
+  auto groups_of = [&](const int4 &itm) {
+    return (itm.x == kE ? p.K_shared : p.K_routed) / kG;
+  };
+  // the scales of weight row r (0..63 gate, 64..127 up) of item itm
+  auto scale_row = [&](const int4 &itm, int r, int ng) {
+    const bool sh = itm.x == kE;
+    const int half = sh ? p.rows_shared : p.rows_routed;
+    const int rr = r < 64 ? itm.y * 64 + r : half + itm.y * 64 + (r - 64);
+    return (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * 2 * half * ng) +
+           static_cast<size_t>(rr) * ng;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&maps.a[0]); ptx::tma_prefetch_desc(&maps.a[1]);
+      for (int i = 0; i < 3; ++i) {
+        ptx::tma_prefetch_desc(&maps.b[0][i]); ptx::tma_prefetch_desc(&maps.b[1][i]);
+      }
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      uint32_t nq = 0, nb = 0;
+      bool stop = false;
+      int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+        const int4 itm = nxt;  // descriptors are read one item ahead
+        if (it + static_cast<int>(gridDim.x) < n_items) nxt = p.items[it + gridDim.x];
+        const bool sh = itm.x == kE;
+        const int ng = groups_of(itm);
+        const int rA = (sh ? 0 : itm.x * 2 * p.rows_routed) + itm.y * 64;
+        const int nbx = (itm.w + kXBRows - 1) / kXBRows;
+        for (int g = 0; g < ng; ++g) {
+          const uint32_t sq = nq % kXQS;
+          if (!ptx::mbar_wait(&bars->q_empty[sq], ((nq / kXQS) & 1) ^ 1, abort, budget)) { stop = true; break; }
+          ptx::mbar_expect_tx(&bars->q_full[sq], kXQBytes);
+          ptx::tma_load_3d(smem + kXOffQ + sq * kXQBytes, &maps.a[sh ? 1 : 0], g * 128, rA, 0,
+                           &bars->q_full[sq], pol_w);
+          ++nq;
+          const uint32_t sb = nb % kXBS;
+          if (!ptx::mbar_wait(&bars->b_empty[sb], ((nb / kXBS) & 1) ^ 1, abort, budget)) { stop = true; break; }
+          ptx::mbar_expect_tx(&bars->b_full[sb], 2u * nbx * kXBRows * 128);
+          ptx::tma_load_3d(smem + kXOffB + sb * kXBBytes, &maps.b[sh ? 1 : 0][nbx - 1], 0, itm.z,
+                           2 * g, &bars->b_full[sb], pol_x);
+          ++nb;
+        }
+      }
+      if (*abort) {  // let the copies in flight land before exiting
+        int never = 0;
+        for (uint32_t k = 0; k < kXQS && k < nq; ++k) {
+          const uint32_t j = nq - 1 - k;
+          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, budget);
+        }
+        for (uint32_t k = 0; k < kXBS && k < nb; ++k) {
+          const uint32_t j = nb - 1 - k;
+          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, budget);
+        }
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // --------------------------------- MMA issuers (A1 part, A2 part)
+    if (lane == 0) {
+      const int me = warp - 1;
+      uint32_t gs = 0, nit = 0;
+      bool issued = false;
+      int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+      for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x, ++nit) {
+        const int4 itm = nxt;  // descriptors are read one item ahead
+        if (it + static_cast<int>(gridDim.x) < n_items) nxt = p.items[it + gridDim.x];
+        const int ng = groups_of(itm);
+        const int n16 = (itm.w + 15) & ~15;
+        const uint32_t bhalf = static_cast<uint32_t>((itm.w + kXBRows - 1) / kXBRows) * kXBRows * 128;
+        const uint32_t idesc = ptx::idesc_f16_f32(128, n16);
+        // the accumulator must have been read by the previous item's epilogue
+        if (!ptx::mbar_wait(&bars->d_empty[me], (nit & 1) ^ 1, abort, budget)) break;
+        ptx::tc_fence_after();
+        bool first = true;
+        for (int g = 0; g < ng; ++g, ++gs) {
+          const int sa = gs % kGAS, sb = gs % kXBS;
+          if (!ptx::mbar_wait(&bars->a_full[sa], (gs / kGAS) & 1, abort, budget)) break;
+          if (!ptx::mbar_wait(&bars->b_full[sb], (gs / kXBS) & 1, abort, budget)) break;
+          ptx::tc_fence_after();
+          const uint32_t b0 = ptx::smem_u32(smem + kXOffB + sb * kXBBytes);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // K = 16 per instruction: 8 TMEM columns of A
+            const uint64_t bd = ptx::sw128_desc(b0 + (k >> 2) * bhalf + (k & 3) * 32);
+            ptx::mma_tmem_a(tmem + g_dcol(me), tmem + g_acol(sa, me) + k * 8, bd, idesc,
+                            !(first && k == 0));
+          }
+          first = false;
+          ptx::mma_commit(&bars->a_empty[sa]);
+          ptx::mma_commit(&bars->b_empty[sb]);
+          issued = true;
+        }
+        if (*abort) break;
+        ptx::mma_commit(&bars->d_full[me]);  // this item's sums are complete
+      }
+      if (issued) {  // all MMAs complete before TMEM is released
+        ptx::mma_commit(&bars->done[me]);
+        int never = 0;
+        ptx::mbar_wait(&bars->done[me], 0, &never, budget);
+      }
+    }
+  } else if (warp < kGConv0 + kConv) {
+    // ------------------------------------------------------- converters
+    const int quarter = warp & 3;  // TMEM lanes 32 * quarter .. + 31
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t gs = 0;
+    bool ok = true;
+    int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int4 itm = nxt;  // descriptors are read one item ahead
+      const int ng = groups_of(itm);
+      const moe_bf16 *srow = scale_row(itm, r, ng);
+      if (it + static_cast<int>(gridDim.x) < n_items) {  // the next item's scales into L1
+        nxt = p.items[it + gridDim.x];
+        const moe_bf16 *ns = scale_row(nxt, r, groups_of(nxt));
+        asm volatile("prefetch.L1 [%0];" ::"l"(ns));
+      }
+      const int ef = row_scale_exp(srow, ng);
+      const float down = __uint_as_float(static_cast<uint32_t>(258 - ef) << 23);  // 2^-e
+      for (int g = 0; g < ng; ++g, ++gs) {
+        const int sq = gs % kXQS, sa = gs % kGAS;
+        // s = s_a + s_b: s_a keeps the top four significand bits of s
+        const uint16_t sbits = srow[g];
+        const float s_a = bf16_to_f32(static_cast<uint16_t>(sbits & 0xFFF0u));
+        const float s_b = bf16_to_f32(sbits) - s_a;
+        // multipliers s' and the constants -1152 s' (all exact in fp16)
+        const __half2 ha = __float2half2_rn(s_a * down), hb = __float2half2_rn(s_b * down);
+        const __half2 ca = __float2half2_rn(-1152.0f * s_a * down);
+        const __half2 cb = __float2half2_rn(-1152.0f * s_b * down);
+        const uint32_t ha2 = *reinterpret_cast<const uint32_t *>(&ha);
+        const uint32_t hb2 = *reinterpret_cast<const uint32_t *>(&hb);
+        const uint32_t ca2 = *reinterpret_cast<const uint32_t *>(&ca);
+        const uint32_t cb2 = *reinterpret_cast<const uint32_t *>(&cb);
+        if (!ptx::mbar_wait(&bars->q_full[sq], (gs / kXQS) & 1, abort, budget)) { ok = false; break; }
+        if (!ptx::mbar_wait(&bars->a_empty[sa], ((gs / kGAS) & 1) ^ 1, abort, budget)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint8_t *src = smem + kXOffQ + sq * kXQBytes + r * 128;
+        uint4 q[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v1[32], v2[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 qc = q[4 * hf + c];
+            const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t u = w[i] ^ 0x80808080u;  // q + 128 per byte
+              const uint32_t m[2] = {__byte_perm(u, 0x64646464u, 0x4140),   // 1024 + u
+                                     __byte_perm(u, 0x64646464u, 0x4342)};
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(v1[8 * c + 2 * i + h])
+                    : "r"(m[h]), "r"(ha2), "r"(ca2));
+                asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(v2[8 * c + 2 * i + h])
+                    : "r"(m[h]), "r"(hb2), "r"(cb2));
+              }
+            }
+          }
+          if (hf == 1) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars->q_empty[sq]);
+          }
+          ptx::tmem_st32(tmem + tl + g_acol(sa, 0) + 32 * hf, v1);
+          ptx::tmem_st32(tmem + tl + g_acol(sa, 1) + 32 * hf, v2);
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->a_full[sa]);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int ch = (warp - kGConv0 - kConv) >> 2;  // column blocks ch, ch + 2, ch + 4
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
+    float acc[48];
+    uint32_t nit = 0;
+    int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++nit) {
+      const int4 itm = nxt;  // descriptors are read one item ahead
+      if (it + static_cast<int>(gridDim.x) < n_items) nxt = p.items[it + gridDim.x];
+      const bool sh = itm.x == kE;
+      const int ng = groups_of(itm);
+      const int n = itm.w, nblk = (n + 15) >> 4;
+      const float up = __uint_as_float(
+          static_cast<uint32_t>(row_scale_exp(scale_row(itm, r, ng), ng) - 4) << 23);  // 2^e
+      float cs[3];  // gate rows: 2^s of the columns' tokens (lane j: column j of each block)
+#pragma unroll
+      for (int jb = 0; jb < 3; ++jb) {
+        cs[jb] = 0.0f;
+        const int cl = (ch + 2 * jb) * 16 + (lane & 15);
+        if (r < 64 && cl < n) cs[jb] = p.xscale[sh ? itm.z + cl : p.perm[itm.z + cl] / kK];
+      }
+      if (!ptx::mbar_wait(&bars->d_full[0], nit & 1, abort, budget)) break;
+      if (!ptx::mbar_wait(&bars->d_full[1], nit & 1, abort, budget)) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int jb = 0; jb < 3; ++jb) {
+        const int b = ch + 2 * jb;
+        if (b < nblk) {
+          float v[16], w[16];
+          ptx::tmem_ld16(tmem + tl + g_dcol(0) + b * 16, v);
+          ptx::tmem_ld16(tmem + tl + g_dcol(1) + b * 16, w);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[jb * 16 + j] = (v[j] + w[j]) * up;
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&bars->d_empty[0]);
+        ptx::mbar_arrive(&bars->d_empty[1]);
+      }
+      // SwiGLU: the up rows hand their sums to the gate rows through shared
+      // memory; acc[jb * 16 + j] is column (ch + 2 * jb) * 16 + j of this row
+      float *xch = reinterpret_cast<float *>(smem + kXOffX);
+      const uint32_t par = nit & 1;
+      if (r >= 64) {
+        if (!ptx::mbar_wait(&bars->xch_empty, par ^ 1, abort, budget)) break;
+#pragma unroll
+        for (int jb = 0; jb < 3; ++jb) {
+          const int b = ch + 2 * jb;
+          if (b < nblk) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xch[(b * 16 + j) * 64 + (r - 64)] = acc[jb * 16 + j];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->xch_full);
+      } else {
+        if (!ptx::mbar_wait(&bars->xch_full, par, abort, budget)) break;
+        const int Irows = sh ? p.rows_shared : p.rows_routed;
+        moe_bf16 *hout = sh ? p.h_shared : p.h_routed;
+        const int i = itm.y * 64 + r;
+#pragma unroll
+        for (int jb = 0; jb < 3; ++jb) {
+          const int b = ch + 2 * jb;
+          if (b < nblk) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = b * 16 + j;
+              const float sj = __shfl_sync(0xFFFFFFFFu, cs[jb], j);  // lane j holds column j's
+              if (col < n) {
+                const float u = xch[col * 64 + r] * sj;
+                hout[static_cast<size_t>(itm.z + col) * Irows + i] =
+                    f32_to_bf16(silu_mul(acc[jb * 16 + j] * sj, u));
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->xch_empty);
       }
     }
   }
@@ -705,19 +1002,33 @@ __global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
   }
 }
 
-template <int MODE>
-cudaError_t launch_x(const XMaps &maps, const XParams &p, cudaStream_t s) {
+cudaError_t launch_down(const XMaps &maps, const XParams &p, cudaStream_t s) {
   static bool attr[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_expert_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(down_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kXSmem));
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
-  tc_expert_kernel<MODE><<<tc_sm_count(), kXThreads, kXSmem, s>>>(maps, p);
+  down_tc_kernel<<<tc_sm_count(), kXThreads, kXSmem, s>>>(maps, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gateup_split(const XMaps &maps, const XParams &p, cudaStream_t s) {
+  static bool attr[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gateup_split_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kXSmem));
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  gateup_split_kernel<<<tc_sm_count(), kGThreads, kXSmem, s>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -803,7 +1114,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   p.xscale = xscale; p.perm = L.perm;
   p.h_routed = h_routed; p.h_shared = h_shared;
   p.status = status; p.budget_ns = tc_wait_budget_ns();
-  TC_STEP(launch_x<kXGateUp>(gm, p, s));
+  TC_STEP(launch_gateup_split(gm, p, s));
   XParams q{};
   q.items = dn; q.n_items = counters + 1;
   q.K_routed = I; q.K_shared = Is;
@@ -811,7 +1122,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   q.s_routed = w.w2_s; q.s_shared = w.ws2_s;
   q.out_acc = out_acc; q.perm = L.perm; q.weights = weights; q.sgate = sgate; q.H = H;
   q.status = status; q.budget_ns = tc_wait_budget_ns();
-  TC_STEP(launch_x<kXDown>(dm, q, s));
+  TC_STEP(launch_down(dm, q, s));
   const size_t n4 = static_cast<size_t>(T) * H / 4;
   acc_to_bf16_kernel<<<tc_sm_count() * 4, 256, 0, s>>>(out_acc, n4, out);
   TC_STEP(cudaGetLastError());
