@@ -56,7 +56,7 @@ size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 struct Layout {
   size_t status, logits, gate_logit, ids, weights, sgate;
   size_t counts, offsets, active, perm, slot_of;
-  size_t h_routed, h_shared, y, rpart, x16, xscale, xstage, ostage;
+  size_t h_routed, h_shared, y, rpart, x16, xscale, hscale, xstage, ostage;
   size_t xs, acc, items, counters, total;
 };
 
@@ -113,6 +113,9 @@ Layout layout(const moe_dims *d, int T) {
     L.x16 = take(2 * t * H);
     L.xscale = take(4 * t);
   }
+  if (r == kRouteTc) {
+    L.hscale = take(4 * t * (kK + 1));
+  }
   L.xstage = take(2 * t * H);
   L.ostage = take(2 * t * H);
   if (r == kRouteTc) {
@@ -159,8 +162,8 @@ constexpr int kStages = 6;
 const char *const kFusedStageNames[] = {"decode_fused"};
 const char *const kTcStageNames[] = {"router_tc", "router_gate_gemv", "select_top8",
                                      "lists_items", "scale_gather", "gateup_swiglu_tc",
-                                     "down_combine_tc", "acc_to_bf16"};
-constexpr int kTcStages = 8;
+                                     "h_scale", "down_combine_tc", "acc_to_bf16"};
+constexpr int kTcStages = 9;
 
 // Records `ev[i]` after kernel i-1 when profiling (ev[0] before the first).
 struct Rec : StageRecorder {
@@ -232,7 +235,7 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   MOE_TRY(rec());
   MOE_TRY(launch_experts_tc(x, T, H, I, Is, *w, ids, lists, wts, wg ? sg : nullptr,
                             at<uint16_t>(ws, L.xs), at<uint16_t>(ws, L.x16),
-                            at<float>(ws, L.xscale), hr, hs, at<float>(ws, L.acc), out, items,
+                            at<float>(ws, L.xscale), at<float>(ws, L.hscale), hr, hs, at<float>(ws, L.acc), out, items,
                             counters, status, s, rec));
   return MOE_OK;
 }

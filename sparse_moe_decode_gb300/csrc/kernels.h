@@ -100,13 +100,14 @@ cudaError_t launch_router_tc(const moe_bf16 *x, int T, int H, const moe_bf16 *w_
 // A3..A7 for prefill-size T: builds the token -> expert lists of ids [T][K]
 // into L (counts, offsets, perm, slot_of; not active) with the work items,
 // the tokens' scaled fp16 copies (xs16 [T*K][H] in list order, x16 [T][H],
-// xscale [T]), runs gate|up + SwiGLU and down + weighted combine as grouped
-// tcgen05 GEMMs into out_acc [T][H] (fp32, zeroed here), then rounds out_acc
-// to bf16.
+// xscale [T]), runs gate|up + SwiGLU (h in bf16), converts h in place to
+// per-row scaled fp16 (2^s of each row in hscale [T*K + T]), runs down + weighted combine into out_acc [T][H] (fp32, zeroed
+// here), then rounds out_acc to bf16.
 cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                               const moe_weights &w, const int32_t *ids, const Lists &L,
                               const float *weights,
                               const float *sgate, uint16_t *xs16, uint16_t *x16, float *xscale,
+                              float *hscale,
                               moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
                               moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
                               cudaStream_t s, StageRecorder &rec);

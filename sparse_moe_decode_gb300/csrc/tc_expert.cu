@@ -9,19 +9,12 @@
 // are N (<= 96): each weight tile is streamed from HBM once for all of its
 // expert's tokens (an expert with more than 96 tokens gets several tiles).
 //
-// gate|up (gateup_split_kernel): the weights become two exact fp16 operands
-// (the group scale split in two, below) and the MMAs sum the whole reduction
-// in TMEM.
-//
-// down (down_tc_kernel), per 128-wide K group (one quantisation group):
-//   TMA         int8 tile 128 x 128 (128-byte swizzle) -> shared ring Q
-//   converters  Q row -> exact bf16 -> TMEM A stage (tcgen05.st; |q| <= 127
-//               is exact in bf16)
-//   TMA         activation tile N x 128 -> shared ring B (4 stages)
-//   MMA         P = A[TMEM] x B[smem]^T into one of three TMEM partial buffers
-//   promoters   acc[row][token] += s[row][group] * P (fp32 registers)
-// so the product q * s is never rounded ("scale promotion"); the epilogue
-// adds w * acc to the fp32 output rows with vector reductions.
+// gate|up (gateup_split_kernel) and down + combine (down_split_kernel): the
+// int8 weights times their group scales become two exact fp16 operands (the
+// scale split in two, below) held in TMEM, the activations are per-row
+// power-of-two scaled fp16 copies (x by scale_gather_kernel, h in place by
+// h_scale_kernel), and the MMAs sum each item's whole reduction in TMEM: no
+// product is rounded and no per-group partial leaves the tensor memory.
 //
 // Every wait is bounded by a %globaltimer budget; on expiry the CTA drains
 // what it has in flight, frees TMEM, sets MOE_DEV_TIMEOUT and returns.
@@ -36,31 +29,14 @@ namespace moe {
 
 namespace {
 
-constexpr int kXThreads = 512;
-constexpr int kMma1 = 2, kMma2 = 15;       // second and third MMA issuing warps
-constexpr int kIssuers = 3;
-constexpr int kConv0 = 3;                  // first converter warp
-constexpr int kConv = 4;                   // converter warps
-constexpr int kProm = 8;                   // promoter warps
+constexpr int kConv = 4;                   // converter warps (one per TMEM lane quarter)
 constexpr int kXTile = 96;                 // tokens per work item at most (N)
 constexpr int kXQS = 6, kXBS = 4;          // shared-memory ring depths
-constexpr int kXAS = 3;                    // TMEM A stages
-constexpr int kXPS = 3;                    // TMEM partial buffers
 constexpr int kXBRows = 32;                // rows per activation TMA box
 constexpr uint32_t kXQBytes = 128 * 128;   // int8 weight tile
 constexpr uint32_t kXBBytes = 2 * kXTile * 128;  // 16-bit activation tile (<= 96 rows), two K halves
 constexpr uint32_t kXXchBytes = kXTile * 64 * 4;  // gate|up exchange of the up rows
-// TMEM columns: partial buffer pb at 128 * (pb + 1) (96 wide); A stage sa in
-// two 32-column halves (K 0..63 and 64..127 of the group) in the gaps.
 constexpr uint32_t kXTmemCols = 512;
-__host__ __device__ constexpr uint32_t x_pcol(int pb) { return 128u * (pb + 1); }
-__host__ __device__ constexpr uint32_t x_acol(int sa, int half) {
-  return sa < 2 ? 64u * sa + 32u * half : (half == 0 ? 224u : 352u);
-}
-static_assert(x_pcol(kXPS - 1) + kXTile <= kXTmemCols, "tensor memory columns");
-static_assert(x_pcol(0) + kXTile <= x_acol(2, 0) && x_acol(2, 0) + 32 <= x_pcol(1) &&
-                  x_pcol(1) + kXTile <= x_acol(2, 1) && x_acol(2, 1) + 32 <= x_pcol(2),
-              "A stages and partials overlap");
 
 constexpr size_t kXOffQ = 0;
 constexpr size_t kXOffB = kXOffQ + kXQS * kXQBytes;
@@ -68,15 +44,6 @@ constexpr size_t kXOffX = kXOffB + kXBS * kXBBytes;
 constexpr size_t kXOffBar = kXOffX + kXXchBytes;
 constexpr size_t kXSmem = kXOffBar + 512 + 1024;  // + barriers + alignment slack
 static_assert(kXSmem <= 232448, "shared memory per CTA");
-
-struct XBars {
-  uint64_t q_full[kXQS], q_empty[kXQS], a_full[kXAS], a_empty[kXAS], b_full[kXBS],
-      b_empty[kXBS];
-  uint64_t p_full[kXPS], p_empty[kXPS], done[kIssuers], xch_full, xch_empty;
-  uint32_t tmem_holder;
-  int abort;
-};
-static_assert(sizeof(XBars) <= 512, "barrier block");
 
 // Tensor maps: weights (gate|up: 3-D, the 64 gate rows and the matching 64
 // up rows of a group in one copy; down: 128 rows), and activations as 3-D
@@ -101,321 +68,12 @@ struct XParams {
   const float *weights, *sgate;
   int H;
   const int *perm;                    // list position -> entry t * K + j
+  // h rows: routed list positions [0, T*K), shared tokens at T*K + t
+  const float *hscale;                // down: 2^s of each row's fp16 copy of h
+  int T8;                             // T * K
   uint32_t *status;
   unsigned long long budget_ns;
 };
-
-// 16 int8 (one 16-byte chunk) -> 8 32-bit TMEM columns of two bf16 values:
-// exact fp32 values, of which bf16 keeps the upper halves (<= 8 significant
-// bits).
-__device__ __forceinline__ void cvt_chunk_bf16(const uint4 q, uint32_t *o) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const f4 a = i8x4_to_f32(w[i]);
-    o[2 * i] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
-    o[2 * i + 1] = __byte_perm(__float_as_uint(a.z), __float_as_uint(a.w), 0x7632);
-  }
-}
-
-// Warp roles (512 threads): warp 0 issues the TMA copies (one of the weight
-// tile and one of the activation tile per K group), warps 1, 2 and 15 issue
-// the MMAs of the K groups g with g mod 3 = 0, 1, 2 (one issuing thread
-// sustains only about one tcgen05 instruction per hundred cycles), warp 1
-// also owns TMEM, warps 3..6 convert (one per TMEM lane quarter), warps 7..14
-// promote and run the epilogue (two per lane quarter, splitting the token
-// columns).
-__global__ void __launch_bounds__(kXThreads, 1)
-down_tc_kernel(const __grid_constant__ XMaps maps, const XParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  XBars *bars = reinterpret_cast<XBars *>(smem + kXOffBar);
-  volatile int *abort = &bars->abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = *p.n_items;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kXQS; ++i) {
-      ptx::mbar_init(&bars->q_full[i], 1);
-      ptx::mbar_init(&bars->q_empty[i], kConv);
-    }
-    for (int i = 0; i < kXAS; ++i) {
-      ptx::mbar_init(&bars->a_full[i], kConv);
-      ptx::mbar_init(&bars->a_empty[i], 1);
-    }
-    for (int i = 0; i < kXBS; ++i) {
-      ptx::mbar_init(&bars->b_full[i], 1);
-      ptx::mbar_init(&bars->b_empty[i], 1);
-    }
-    for (int i = 0; i < kXPS; ++i) {
-      ptx::mbar_init(&bars->p_full[i], 1);
-      ptx::mbar_init(&bars->p_empty[i], kProm);
-    }
-    for (int i = 0; i < kIssuers; ++i) ptx::mbar_init(&bars->done[i], 1);
-    ptx::mbar_init(&bars->xch_full, kProm / 2);   // the warps holding up rows
-    ptx::mbar_init(&bars->xch_empty, kProm / 2);  // the warps holding gate rows
-    bars->abort = 0;
-    ptx::fence_mbar_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(&bars->tmem_holder, kXTmemCols);
-    ptx::tmem_relinquish();
-    ptx::tc_fence_before();
-  }
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = bars->tmem_holder;
-  const uint64_t budget = p.budget_ns;
-  auto groups_of = [&](const int4 &itm) {
-    return (itm.x == kE ? p.K_shared : p.K_routed) / kG;
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      ptx::tma_prefetch_desc(&maps.a[0]); ptx::tma_prefetch_desc(&maps.a[1]);
-      for (int i = 0; i < 3; ++i) {
-        ptx::tma_prefetch_desc(&maps.b[0][i]); ptx::tma_prefetch_desc(&maps.b[1][i]);
-      }
-      const uint64_t pol_w = ptx::policy_evict_first();
-      const uint64_t pol_x = ptx::policy_evict_last();
-      uint32_t nq = 0, nb = 0;  // stages issued on the Q and B rings
-      bool stop = false;
-      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
-        const int4 itm = p.items[it];
-        const bool sh = itm.x == kE;
-        const int ng = groups_of(itm);
-        const int rA = (sh ? 0 : itm.x * p.rows_routed) + itm.y * 128;
-        const int nbx = (itm.w + kXBRows - 1) / kXBRows;  // activation box: 32 * nbx rows
-        for (int g = 0; g < ng; ++g) {
-          const uint32_t sq = nq % kXQS;
-          if (!ptx::mbar_wait(&bars->q_empty[sq], ((nq / kXQS) & 1) ^ 1, abort, budget)) { stop = true; break; }
-          uint8_t *dq = smem + kXOffQ + sq * kXQBytes;
-          ptx::mbar_expect_tx(&bars->q_full[sq], kXQBytes);
-          ptx::tma_load_2d(dq, &maps.a[sh ? 1 : 0], g * 128, rA, &bars->q_full[sq], pol_w);
-          ++nq;
-          const uint32_t sb = nb % kXBS;
-          if (!ptx::mbar_wait(&bars->b_empty[sb], ((nb / kXBS) & 1) ^ 1, abort, budget)) { stop = true; break; }
-          uint8_t *db = smem + kXOffB + sb * kXBBytes;
-          ptx::mbar_expect_tx(&bars->b_full[sb], 2u * nbx * kXBRows * 128);
-          ptx::tma_load_3d(db, &maps.b[sh ? 1 : 0][nbx - 1], 0, itm.z, 2 * g, &bars->b_full[sb],
-                           pol_x);
-          ++nb;
-        }
-      }
-      // After an abort, the copies still in flight must land before the CTA
-      // exits: wait (bounded) for the last stages issued on each ring.
-      if (*abort) {
-        int never = 0;
-        for (uint32_t k = 0; k < kXQS && k < nq; ++k) {
-          const uint32_t j = nq - 1 - k;
-          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, budget);
-        }
-        for (uint32_t k = 0; k < kXBS && k < nb; ++k) {
-          const uint32_t j = nb - 1 - k;
-          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, budget);
-        }
-      }
-    }
-  } else if (warp == 1 || warp == kMma1 || warp == kMma2) {
-    // ------------------------------------ MMA issuers (groups mod kIssuers)
-    if (lane == 0) {
-      const uint32_t par = warp == 1 ? 0 : warp == kMma1 ? 1 : 2;
-      uint32_t gs = 0;
-      bool issued = false;
-      for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
-        const int4 itm = p.items[it];
-        const int ng = groups_of(itm);
-        const int n16 = (itm.w + 15) & ~15;
-        const uint32_t bhalf = static_cast<uint32_t>((itm.w + kXBRows - 1) / kXBRows) * kXBRows * 128;
-        const uint32_t idesc = ptx::idesc_bf16_f32(128, n16);
-        for (int g = 0; g < ng; ++g, ++gs) {
-          if (gs % kIssuers != par) continue;
-          const int sa = gs % kXAS, sb = gs % kXBS, pb = gs % kXPS;
-          if (!ptx::mbar_wait(&bars->a_full[sa], (gs / kXAS) & 1, abort, budget)) break;
-          if (!ptx::mbar_wait(&bars->b_full[sb], (gs / kXBS) & 1, abort, budget)) break;
-          if (!ptx::mbar_wait(&bars->p_empty[pb], ((gs / kXPS) & 1) ^ 1, abort, budget)) break;
-          ptx::tc_fence_after();
-          const uint32_t b0 = ptx::smem_u32(smem + kXOffB + sb * kXBBytes);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {  // K = 16 per instruction: 8 TMEM columns of A
-            const uint32_t boff = (k >> 2) * bhalf + (k & 3) * 32;
-            ptx::mma_tmem_a(tmem + x_pcol(pb), tmem + x_acol(sa, k >> 2) + (k & 3) * 8,
-                            ptx::sw128_desc(b0 + boff), idesc, k > 0);
-          }
-          ptx::mma_commit(&bars->a_empty[sa]);
-          ptx::mma_commit(&bars->b_empty[sb]);
-          ptx::mma_commit(&bars->p_full[pb]);
-          issued = true;
-        }
-      }
-      if (issued) {  // all MMAs complete before TMEM is released
-        ptx::mma_commit(&bars->done[par]);
-        int never = 0;
-        ptx::mbar_wait(&bars->done[par], 0, &never, budget);
-      }
-    }
-  } else if (warp < kConv0 + kConv) {
-    // ------------------------------------------------------- converters
-    const int quarter = warp & 3;  // TMEM lanes 32 * quarter .. + 31
-    const int r = quarter * 32 + lane;
-    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t gs = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int ng = groups_of(p.items[it]);
-      for (int g = 0; g < ng; ++g, ++gs) {
-        const int sq = gs % kXQS, sa = gs % kXAS;
-        if (!ptx::mbar_wait(&bars->q_full[sq], (gs / kXQS) & 1, abort, budget)) { ok = false; break; }
-        if (!ptx::mbar_wait(&bars->a_empty[sa], ((gs / kXAS) & 1) ^ 1, abort, budget)) { ok = false; break; }
-        ptx::tc_fence_after();
-        // row r of the swizzled tile: 16-byte chunk c sits at chunk c ^ (r & 7)
-        const uint8_t *src = smem + kXOffQ + sq * kXQBytes + r * 128;
-        uint4 q[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
-        const uint32_t ta0 = tmem + tl + x_acol(sa, 0), ta1 = tmem + tl + x_acol(sa, 1);
-        uint32_t v0[32], v1[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) cvt_chunk_bf16(q[c], v0 + 8 * c);
-        ptx::tmem_st32(ta0, v0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) cvt_chunk_bf16(q[4 + c], v1 + 8 * c);
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars->q_empty[sq]);
-        ptx::tmem_st32(ta1, v1);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars->a_full[sa]);
-      }
-    }
-  } else {
-    // --------------------------------------------- promoters + epilogue
-    const int quarter = warp & 3;
-    const int ch = (warp - kConv0 - kConv) >> 2;  // column blocks ch, ch + 2, ch + 4
-    const int r = quarter * 32 + lane;       // tile row of this thread
-    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
-    float acc[48];
-    uint32_t gs = 0, n_done = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++n_done) {
-      const int4 itm = p.items[it];
-      const bool sh = itm.x == kE;
-      const int ng = groups_of(itm);
-      const int n = itm.w, nblk = (n + 15) >> 4;
-      // this row's group scales
-      const moe_bf16 *srow =
-          (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * p.rows_routed * ng) +
-          static_cast<size_t>(itm.y * 128 + r) * ng;
-      // The row's group scales, 16 at a time, packed two per word and
-      // consumed from the low half; the per-column data of the epilogue.
-      // Both are loaded here so that their latency hides behind the groups.
-      uint32_t sw[8];
-      auto load_scales = [&](int g0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sw[i] = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (g0 + i < ng) sw[i >> 1] |= static_cast<uint32_t>(srow[g0 + i]) << (16 * (i & 1));
-      };
-      load_scales(0);
-      float cs[3];  // the column's combine weight
-      int ct[3];    // down: the column's token
-#pragma unroll
-      for (int jb = 0; jb < 3; ++jb) {
-        cs[jb] = 0.0f;
-        ct[jb] = 0;
-        const int cl = (ch + 2 * jb) * 16 + (lane & 15);
-        if (cl < n) {
-          if (sh) {
-            ct[jb] = itm.z + cl;
-            cs[jb] = p.sgate ? p.sgate[itm.z + cl] : 0.0f;
-          } else {
-            const int ent = p.perm[itm.z + cl];
-            ct[jb] = ent / kK;
-            cs[jb] = p.weights[ent];
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 48; ++j) acc[j] = 0.0f;
-      for (int g = 0; g < ng; ++g, ++gs) {
-        const int pb = gs % kXPS;
-        if (!ptx::mbar_wait(&bars->p_full[pb], (gs / kXPS) & 1, abort, budget)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const float sc = bf16_lo(sw[0]);
-        const uint32_t tb = tmem + tl + x_pcol(pb);
-#pragma unroll
-        for (int jb = 0; jb < 3; ++jb) {
-          const int b = ch + 2 * jb;
-          if (b < nblk) {
-            float v[16];
-            ptx::tmem_ld16(tb + b * 16, v);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) acc[jb * 16 + j] = fmaf(sc, v[j], acc[jb * 16 + j]);
-          }
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&bars->p_empty[pb]);
-        if ((g & 15) == 15) {
-          load_scales(g + 1);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 7; ++i) sw[i] = __funnelshift_r(sw[i], sw[i + 1], 16);
-          sw[7] >>= 16;
-        }
-      }
-      if (!ok) break;
-      // ------------------------------------------------------ epilogue
-      // acc[jb * 16 + j] is column (ch + 2 * jb) * 16 + j of this row
-      {
-        // Weighted combine, out_acc[t][row] += w * acc: a 4 x 4 transpose
-        // among each four lanes leaves every lane four consecutive rows of
-        // one column, added with one 16-byte reduction.
-        const int q4 = lane & 3;
-        const bool lo2 = (q4 & 2) == 0, odd = (q4 & 1) != 0;
-        const int nrow4 = itm.y * 128 + quarter * 32 + (lane & ~3);
-#pragma unroll
-        for (int jb = 0; jb < 3; ++jb) {
-          const int b = ch + 2 * jb;
-          if (b < nblk) {
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              const float *v = &acc[jb * 16 + c4 * 4];  // this row, columns c4*4 .. +3
-              // lanes q and q ^ 2 swap 2 x 2 blocks
-              const float r0 = __shfl_xor_sync(0xFFFFFFFFu, lo2 ? v[2] : v[0], 2);
-              const float r1 = __shfl_xor_sync(0xFFFFFFFFu, lo2 ? v[3] : v[1], 2);
-              const float x0 = lo2 ? v[0] : r0, x1 = lo2 ? v[1] : r1;
-              const float x2 = lo2 ? r0 : v[2], x3 = lo2 ? r1 : v[3];
-              // lanes q and q ^ 1 swap single elements
-              const float p0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? x0 : x1, 1);
-              const float p1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? x2 : x3, 1);
-              const float y0 = odd ? p0 : x0, y1 = odd ? x1 : p0;
-              const float y2 = odd ? p1 : x2, y3 = odd ? x3 : p1;
-              // now: column c4 * 4 + q4, rows nrow4 .. nrow4 + 3
-              const int j = c4 * 4 + q4;
-              const int tj = __shfl_sync(0xFFFFFFFFu, ct[jb], j);  // lane j holds column j's
-              const float wj = __shfl_sync(0xFFFFFFFFu, cs[jb], j);
-              if (b * 16 + j < n && wj != 0.0f)
-                ptx::red_add_v4_f32(p.out_acc + static_cast<size_t>(tj) * p.H + nrow4, wj * y0,
-                                    wj * y1, wj * y2, wj * y3);
-            }
-          }
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 1) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kXTmemCols);
-  }
-  if (threadIdx.x == 0 && bars->abort) set_status(p.status, MOE_DEV_TIMEOUT);
-}
 
 // ------------------------------ gate|up with the scales split (no promotion)
 //
@@ -778,6 +436,329 @@ gateup_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
   if (threadIdx.x == 0 && bars->abort) set_status(p.status, MOE_DEV_TIMEOUT);
 }
 
+// ----------------------------- down + combine with the scales split (no promotion)
+//
+// The same scheme as gateup_split_kernel for the down projection: the weight
+// tile is 128 consecutive output rows, the activations are the h rows
+// converted in place to fp16 with a power of two per row (h_scale_kernel),
+// and the epilogue adds w * 2^s_h * 2^e * (A1 x h + A2 x h) to the fp32 output
+// rows with vector reductions.
+__global__ void __launch_bounds__(kGThreads, 1)
+down_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  GBars *bars = reinterpret_cast<GBars *>(smem + kXOffBar);
+  volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *p.n_items;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kXQS; ++i) {
+      ptx::mbar_init(&bars->q_full[i], 1);
+      ptx::mbar_init(&bars->q_empty[i], kConv);
+    }
+    for (int i = 0; i < kGAS; ++i) {
+      ptx::mbar_init(&bars->a_full[i], kConv);
+      ptx::mbar_init(&bars->a_empty[i], 2);  // both issuers
+    }
+    for (int i = 0; i < kXBS; ++i) {
+      ptx::mbar_init(&bars->b_full[i], 1);
+      ptx::mbar_init(&bars->b_empty[i], 2);  // both issuers
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->d_full[i], 1);
+      ptx::mbar_init(&bars->d_empty[i], kGEpi);
+      ptx::mbar_init(&bars->done[i], 1);
+    }
+    ptx::mbar_init(&bars->xch_full, kGEpi / 2);   // the warps holding up rows
+    ptx::mbar_init(&bars->xch_empty, kGEpi / 2);  // the warps holding gate rows
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_holder, kXTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_holder;
+  const uint64_t budget = p.budget_ns;
+  auto groups_of = [&](const int4 &itm) {
+    return (itm.x == kE ? p.K_shared : p.K_routed) / kG;
+  };
+  // the scales of output row r of item itm's 128-row tile
+  auto scale_row = [&](const int4 &itm, int r, int ng) {
+    const bool sh = itm.x == kE;
+    return (sh ? p.s_shared : p.s_routed + static_cast<size_t>(itm.x) * p.rows_routed * ng) +
+           static_cast<size_t>(itm.y * 128 + r) * ng;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&maps.a[0]); ptx::tma_prefetch_desc(&maps.a[1]);
+      for (int i = 0; i < 3; ++i) {
+        ptx::tma_prefetch_desc(&maps.b[0][i]); ptx::tma_prefetch_desc(&maps.b[1][i]);
+      }
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      uint32_t nq = 0, nb = 0;
+      bool stop = false;
+      int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+        const int4 itm = nxt;  // descriptors are read one item ahead
+        if (it + static_cast<int>(gridDim.x) < n_items) nxt = p.items[it + gridDim.x];
+        const bool sh = itm.x == kE;
+        const int ng = groups_of(itm);
+        const int rA = (sh ? 0 : itm.x * p.rows_routed) + itm.y * 128;
+        const int nbx = (itm.w + kXBRows - 1) / kXBRows;
+        for (int g = 0; g < ng; ++g) {
+          const uint32_t sq = nq % kXQS;
+          if (!ptx::mbar_wait(&bars->q_empty[sq], ((nq / kXQS) & 1) ^ 1, abort, budget)) { stop = true; break; }
+          ptx::mbar_expect_tx(&bars->q_full[sq], kXQBytes);
+          ptx::tma_load_2d(smem + kXOffQ + sq * kXQBytes, &maps.a[sh ? 1 : 0], g * 128, rA,
+                           &bars->q_full[sq], pol_w);
+          ++nq;
+          const uint32_t sb = nb % kXBS;
+          if (!ptx::mbar_wait(&bars->b_empty[sb], ((nb / kXBS) & 1) ^ 1, abort, budget)) { stop = true; break; }
+          ptx::mbar_expect_tx(&bars->b_full[sb], 2u * nbx * kXBRows * 128);
+          ptx::tma_load_3d(smem + kXOffB + sb * kXBBytes, &maps.b[sh ? 1 : 0][nbx - 1], 0, itm.z,
+                           2 * g, &bars->b_full[sb], pol_x);
+          ++nb;
+        }
+      }
+      if (*abort) {  // let the copies in flight land before exiting
+        int never = 0;
+        for (uint32_t k = 0; k < kXQS && k < nq; ++k) {
+          const uint32_t j = nq - 1 - k;
+          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, budget);
+        }
+        for (uint32_t k = 0; k < kXBS && k < nb; ++k) {
+          const uint32_t j = nb - 1 - k;
+          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, budget);
+        }
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // --------------------------------- MMA issuers (A1 part, A2 part)
+    if (lane == 0) {
+      const int me = warp - 1;
+      uint32_t gs = 0, nit = 0;
+      bool issued = false;
+      int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+      for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x, ++nit) {
+        const int4 itm = nxt;  // descriptors are read one item ahead
+        if (it + static_cast<int>(gridDim.x) < n_items) nxt = p.items[it + gridDim.x];
+        const int ng = groups_of(itm);
+        const int n16 = (itm.w + 15) & ~15;
+        const uint32_t bhalf = static_cast<uint32_t>((itm.w + kXBRows - 1) / kXBRows) * kXBRows * 128;
+        const uint32_t idesc = ptx::idesc_f16_f32(128, n16);
+        // the accumulator must have been read by the previous item's epilogue
+        if (!ptx::mbar_wait(&bars->d_empty[me], (nit & 1) ^ 1, abort, budget)) break;
+        ptx::tc_fence_after();
+        bool first = true;
+        for (int g = 0; g < ng; ++g, ++gs) {
+          const int sa = gs % kGAS, sb = gs % kXBS;
+          if (!ptx::mbar_wait(&bars->a_full[sa], (gs / kGAS) & 1, abort, budget)) break;
+          if (!ptx::mbar_wait(&bars->b_full[sb], (gs / kXBS) & 1, abort, budget)) break;
+          ptx::tc_fence_after();
+          const uint32_t b0 = ptx::smem_u32(smem + kXOffB + sb * kXBBytes);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // K = 16 per instruction: 8 TMEM columns of A
+            const uint64_t bd = ptx::sw128_desc(b0 + (k >> 2) * bhalf + (k & 3) * 32);
+            ptx::mma_tmem_a(tmem + g_dcol(me), tmem + g_acol(sa, me) + k * 8, bd, idesc,
+                            !(first && k == 0));
+          }
+          first = false;
+          ptx::mma_commit(&bars->a_empty[sa]);
+          ptx::mma_commit(&bars->b_empty[sb]);
+          issued = true;
+        }
+        if (*abort) break;
+        ptx::mma_commit(&bars->d_full[me]);  // this item's sums are complete
+      }
+      if (issued) {  // all MMAs complete before TMEM is released
+        ptx::mma_commit(&bars->done[me]);
+        int never = 0;
+        ptx::mbar_wait(&bars->done[me], 0, &never, budget);
+      }
+    }
+  } else if (warp < kGConv0 + kConv) {
+    // ------------------------------------------------------- converters
+    const int quarter = warp & 3;  // TMEM lanes 32 * quarter .. + 31
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t gs = 0;
+    bool ok = true;
+    int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int4 itm = nxt;  // descriptors are read one item ahead
+      const int ng = groups_of(itm);
+      const moe_bf16 *srow = scale_row(itm, r, ng);
+      if (it + static_cast<int>(gridDim.x) < n_items) {  // the next item's scales into L1
+        nxt = p.items[it + gridDim.x];
+        const moe_bf16 *ns = scale_row(nxt, r, groups_of(nxt));
+        asm volatile("prefetch.L1 [%0];" ::"l"(ns));
+      }
+      const int ef = row_scale_exp(srow, ng);
+      const float down = __uint_as_float(static_cast<uint32_t>(258 - ef) << 23);  // 2^-e
+      for (int g = 0; g < ng; ++g, ++gs) {
+        const int sq = gs % kXQS, sa = gs % kGAS;
+        // s = s_a + s_b: s_a keeps the top four significand bits of s
+        const uint16_t sbits = srow[g];
+        const float s_a = bf16_to_f32(static_cast<uint16_t>(sbits & 0xFFF0u));
+        const float s_b = bf16_to_f32(sbits) - s_a;
+        // multipliers s' and the constants -1152 s' (all exact in fp16)
+        const __half2 ha = __float2half2_rn(s_a * down), hb = __float2half2_rn(s_b * down);
+        const __half2 ca = __float2half2_rn(-1152.0f * s_a * down);
+        const __half2 cb = __float2half2_rn(-1152.0f * s_b * down);
+        const uint32_t ha2 = *reinterpret_cast<const uint32_t *>(&ha);
+        const uint32_t hb2 = *reinterpret_cast<const uint32_t *>(&hb);
+        const uint32_t ca2 = *reinterpret_cast<const uint32_t *>(&ca);
+        const uint32_t cb2 = *reinterpret_cast<const uint32_t *>(&cb);
+        if (!ptx::mbar_wait(&bars->q_full[sq], (gs / kXQS) & 1, abort, budget)) { ok = false; break; }
+        if (!ptx::mbar_wait(&bars->a_empty[sa], ((gs / kGAS) & 1) ^ 1, abort, budget)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint8_t *src = smem + kXOffQ + sq * kXQBytes + r * 128;
+        uint4 q[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(src + ((c ^ (r & 7)) << 4));
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v1[32], v2[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 qc = q[4 * hf + c];
+            const uint32_t w[4] = {qc.x, qc.y, qc.z, qc.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t u = w[i] ^ 0x80808080u;  // q + 128 per byte
+              const uint32_t m[2] = {__byte_perm(u, 0x64646464u, 0x4140),   // 1024 + u
+                                     __byte_perm(u, 0x64646464u, 0x4342)};
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(v1[8 * c + 2 * i + h])
+                    : "r"(m[h]), "r"(ha2), "r"(ca2));
+                asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(v2[8 * c + 2 * i + h])
+                    : "r"(m[h]), "r"(hb2), "r"(cb2));
+              }
+            }
+          }
+          if (hf == 1) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars->q_empty[sq]);
+          }
+          ptx::tmem_st32(tmem + tl + g_acol(sa, 0) + 32 * hf, v1);
+          ptx::tmem_st32(tmem + tl + g_acol(sa, 1) + 32 * hf, v2);
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->a_full[sa]);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int ch = (warp - kGConv0 - kConv) >> 2;  // column blocks ch, ch + 2, ch + 4
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = static_cast<uint32_t>(quarter * 32) << 16;
+    float acc[48];
+    uint32_t nit = 0;
+    int4 nxt = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++nit) {
+      const int4 itm = nxt;  // descriptors are read one item ahead
+      if (it + static_cast<int>(gridDim.x) < n_items) nxt = p.items[it + gridDim.x];
+      const bool sh = itm.x == kE;
+      const int ng = groups_of(itm);
+      const int n = itm.w, nblk = (n + 15) >> 4;
+      const float up = __uint_as_float(
+          static_cast<uint32_t>(row_scale_exp(scale_row(itm, r, ng), ng) - 4) << 23);  // 2^e
+      // the columns' token and combine weight (the h row's 2^s included;
+      // lane j: column j of each block)
+      float cs[3];
+      int ct[3];
+#pragma unroll
+      for (int jb = 0; jb < 3; ++jb) {
+        cs[jb] = 0.0f;
+        ct[jb] = 0;
+        const int cl = (ch + 2 * jb) * 16 + (lane & 15);
+        if (cl < n) {
+          if (sh) {
+            ct[jb] = itm.z + cl;
+            cs[jb] = (p.sgate ? p.sgate[itm.z + cl] : 0.0f) * p.hscale[p.T8 + itm.z + cl];
+          } else {
+            const int ent = p.perm[itm.z + cl];
+            ct[jb] = ent / kK;
+            cs[jb] = p.weights[ent] * p.hscale[itm.z + cl];
+          }
+        }
+      }
+      if (!ptx::mbar_wait(&bars->d_full[0], nit & 1, abort, budget)) break;
+      if (!ptx::mbar_wait(&bars->d_full[1], nit & 1, abort, budget)) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int jb = 0; jb < 3; ++jb) {
+        const int b = ch + 2 * jb;
+        if (b < nblk) {
+          float v[16], w[16];
+          ptx::tmem_ld16(tmem + tl + g_dcol(0) + b * 16, v);
+          ptx::tmem_ld16(tmem + tl + g_dcol(1) + b * 16, w);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[jb * 16 + j] = (v[j] + w[j]) * up;
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&bars->d_empty[0]);
+        ptx::mbar_arrive(&bars->d_empty[1]);
+      }
+      // Weighted combine, out_acc[t][row] += w * acc: a 4 x 4 transpose
+      // among each four lanes leaves every lane four consecutive rows of one
+      // column, added with one 16-byte reduction.
+      {
+        const int q4 = lane & 3;
+        const bool lo2 = (q4 & 2) == 0, odd = (q4 & 1) != 0;
+        const int nrow4 = itm.y * 128 + quarter * 32 + (lane & ~3);
+#pragma unroll
+        for (int jb = 0; jb < 3; ++jb) {
+          const int b = ch + 2 * jb;
+          if (b < nblk) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float *v = &acc[jb * 16 + c4 * 4];  // this row, columns c4*4 .. +3
+              const float r0 = __shfl_xor_sync(0xFFFFFFFFu, lo2 ? v[2] : v[0], 2);
+              const float r1 = __shfl_xor_sync(0xFFFFFFFFu, lo2 ? v[3] : v[1], 2);
+              const float x0 = lo2 ? v[0] : r0, x1 = lo2 ? v[1] : r1;
+              const float x2 = lo2 ? r0 : v[2], x3 = lo2 ? r1 : v[3];
+              const float p0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? x0 : x1, 1);
+              const float p1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? x2 : x3, 1);
+              const float y0 = odd ? p0 : x0, y1 = odd ? x1 : p0;
+              const float y2 = odd ? p1 : x2, y3 = odd ? x3 : p1;
+              const int j = c4 * 4 + q4;  // this lane's column now, rows nrow4 .. +3
+              const int tj = __shfl_sync(0xFFFFFFFFu, ct[jb], j);
+              const float wj = __shfl_sync(0xFFFFFFFFu, cs[jb], j);
+              if (b * 16 + j < n && wj != 0.0f)
+                ptx::red_add_v4_f32(p.out_acc + static_cast<size_t>(tj) * p.H + nrow4, wj * y0,
+                                    wj * y1, wj * y2, wj * y3);
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kXTmemCols);
+  }
+  if (threadIdx.x == 0 && bars->abort) set_status(p.status, MOE_DEV_TIMEOUT);
+}
+
 // ------------------------------------ token -> expert lists, work items
 
 // One CTA per expert e (grid kE, kLiThreads threads).  Every CTA histograms
@@ -925,8 +906,11 @@ __global__ void scale_gather_kernel(const moe_bf16 *__restrict__ x, int T, int H
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const moe_bf16 *xr = x + static_cast<size_t>(t) * H;
-  const int nc = H / 256;  // chunks per lane
+  // 16-byte chunk c of this lane holds elements c * 256 + lane * 8 .. + 7; H
+  // is a multiple of 128, so the last chunk may cover only half the lanes
+  const int nc = (H + 255) / 256;
   const bool in_regs = nc <= kGatherMaxChunks;
+  auto valid = [&](int c) { return c * 256 + lane * 8 < H; };
   uint4 v[kGatherMaxChunks];
   float m = 0.0f;
   auto absmax = [&](const uint4 &q) {
@@ -937,12 +921,13 @@ __global__ void scale_gather_kernel(const moe_bf16 *__restrict__ x, int T, int H
   if (in_regs) {
 #pragma unroll
     for (int c = 0; c < kGatherMaxChunks; ++c)
-      if (c < nc) v[c] = ld_nc(xr + c * 256 + lane * 8);
+      if (valid(c)) v[c] = ld_nc(xr + c * 256 + lane * 8);
 #pragma unroll
     for (int c = 0; c < kGatherMaxChunks; ++c)
-      if (c < nc) absmax(v[c]);
+      if (valid(c)) absmax(v[c]);
   } else {
-    for (int c = 0; c < nc; ++c) absmax(ld_nc(xr + c * 256 + lane * 8));
+    for (int c = 0; c < nc; ++c)
+      if (valid(c)) absmax(ld_nc(xr + c * 256 + lane * 8));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -973,13 +958,70 @@ __global__ void scale_gather_kernel(const moe_bf16 *__restrict__ x, int T, int H
   if (in_regs) {
 #pragma unroll
     for (int c = 0; c < kGatherMaxChunks; ++c)
-      if (c < nc) emit(c, v[c]);
+      if (valid(c)) emit(c, v[c]);
   } else {
-    for (int c = 0; c < nc; ++c) emit(c, ld_nc(xr + c * 256 + lane * 8));
+    for (int c = 0; c < nc; ++c)
+      if (valid(c)) emit(c, ld_nc(xr + c * 256 + lane * 8));
   }
   float4 *orow = reinterpret_cast<float4 *>(out_acc + static_cast<size_t>(t) * H);
   for (int k = lane; k < H / 4; k += 32) orow[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (lane == 0) xscale[t] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
+}
+
+// h in place from bf16 to fp16 for the down projection: row p (a routed list
+// position p < S, or the shared expert's token t at S + t) is multiplied by
+// 2^-s with 2^s chosen from the row's largest |h| as for the tokens, so every
+// element within 2^29 of that largest is exact; 2^s is kept in hscale
+// (routed at p, shared at T*K + t).  One warp per row, held in registers.
+constexpr int kHMaxChunks = 8;  // 16-byte chunks per lane (rows of up to 2048)
+
+__global__ void h_scale_kernel(moe_bf16 *__restrict__ h_routed, int I, moe_bf16 *__restrict__ h_shared,
+                               int Is, const int32_t *__restrict__ offsets, int T,
+                               float *__restrict__ hscale) {
+  const int S = offsets[kE];
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= S + (Is > 0 ? T : 0)) return;
+  const bool sh = row >= S;
+  const size_t idx = sh ? static_cast<size_t>(T) * kK + (row - S) : static_cast<size_t>(row);
+  const int len = sh ? Is : I;
+  moe_bf16 *hr = sh ? h_shared + static_cast<size_t>(row - S) * Is : h_routed + static_cast<size_t>(row) * I;
+  // 16-byte chunk c of this lane holds elements c * 256 + lane * 8 .. + 7;
+  // len is a multiple of 128, so the last chunk may cover only half the lanes
+  auto valid = [&](int c) { return c * 256 + lane * 8 < len; };
+  uint4 v[kHMaxChunks];
+  float m = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kHMaxChunks; ++c)
+    if (valid(c)) v[c] = *reinterpret_cast<const uint4 *>(hr + c * 256 + lane * 8);
+#pragma unroll
+  for (int c = 0; c < kHMaxChunks; ++c)
+    if (valid(c)) {
+      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  int sexp = 0;
+  if (m > 0.0f && isfinite(m)) {
+    sexp = static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14;
+    sexp = max(-110, min(110, sexp));
+  }
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - sexp) << 23);
+#pragma unroll
+  for (int c = 0; c < kHMaxChunks; ++c)
+    if (valid(c)) {
+      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 hh = __floats2half2_rn(bf16_lo(w[i]) * down, bf16_hi(w[i]) * down);
+        o[i] = *reinterpret_cast<const uint32_t *>(&hh);
+      }
+      *reinterpret_cast<uint4 *>(hr + c * 256 + lane * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  if (lane == 0) hscale[idx] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
 }
 
 __global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
@@ -1002,21 +1044,6 @@ __global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
   }
 }
 
-cudaError_t launch_down(const XMaps &maps, const XParams &p, cudaStream_t s) {
-  static bool attr[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(down_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kXSmem));
-    if (e != cudaSuccess) return e;
-    attr[dev] = true;
-  }
-  down_tc_kernel<<<tc_sm_count(), kXThreads, kXSmem, s>>>(maps, p);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_gateup_split(const XMaps &maps, const XParams &p, cudaStream_t s) {
   static bool attr[64] = {false};
   int dev = 0;
@@ -1029,6 +1056,21 @@ cudaError_t launch_gateup_split(const XMaps &maps, const XParams &p, cudaStream_
     attr[dev] = true;
   }
   gateup_split_kernel<<<tc_sm_count(), kGThreads, kXSmem, s>>>(maps, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_split(const XMaps &maps, const XParams &p, cudaStream_t s) {
+  static bool attr[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(down_split_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kXSmem));
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  down_split_kernel<<<tc_sm_count(), kGThreads, kXSmem, s>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -1046,6 +1088,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                               const moe_weights &w, const int32_t *ids, const Lists &L,
                               const float *weights,
                               const float *sgate, uint16_t *xs16, uint16_t *x16, float *xscale,
+                              float *hscale,
                               moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
                               moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
                               cudaStream_t s, StageRecorder &rec) {
@@ -1091,7 +1134,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   ok = ok && act_maps(gm.b[0], xs16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rows_r, H) &&
        tc_make_map(&dm.a[0], w.w2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
                    static_cast<uint64_t>(kE) * H, I, 128, 128) &&
-       act_maps(dm.b[0], h_routed, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows_r, I);
+       act_maps(dm.b[0], h_routed, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rows_r, I);
   if (shared) {
     const uint64_t dims[3] = {static_cast<uint64_t>(H), 2 * static_cast<uint64_t>(Is), 2};
     const uint64_t strides[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(Is) * H};
@@ -1100,7 +1143,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                             box) &&
          act_maps(gm.b[1], x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, T, H) &&
          tc_make_map(&dm.a[1], w.ws2_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, Is, 128, 128) &&
-         act_maps(dm.b[1], h_shared, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, T, Is);
+         act_maps(dm.b[1], h_shared, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, T, Is);
   } else {
     gm.a[1] = gm.a[0]; dm.a[1] = dm.a[0];
     for (int i = 0; i < 3; ++i) { gm.b[1][i] = gm.b[0][i]; dm.b[1][i] = dm.b[0][i]; }
@@ -1113,16 +1156,24 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   p.s_routed = w.w13_s; p.s_shared = w.ws13_s;
   p.xscale = xscale; p.perm = L.perm;
   p.h_routed = h_routed; p.h_shared = h_shared;
+  p.T8 = T * kK;
   p.status = status; p.budget_ns = tc_wait_budget_ns();
   TC_STEP(launch_gateup_split(gm, p, s));
+  {
+    const int rows = T * kK + (Is > 0 ? T : 0);  // at most; the kernel reads the count
+    h_scale_kernel<<<(rows + 7) / 8, 256, 0, s>>>(h_routed, I, h_shared, Is, L.offsets, T,
+                                                  hscale);
+    TC_STEP(cudaGetLastError());
+  }
   XParams q{};
   q.items = dn; q.n_items = counters + 1;
   q.K_routed = I; q.K_shared = Is;
   q.rows_routed = H; q.rows_shared = H;
   q.s_routed = w.w2_s; q.s_shared = w.ws2_s;
   q.out_acc = out_acc; q.perm = L.perm; q.weights = weights; q.sgate = sgate; q.H = H;
+  q.hscale = hscale; q.T8 = T * kK;
   q.status = status; q.budget_ns = tc_wait_budget_ns();
-  TC_STEP(launch_down(dm, q, s));
+  TC_STEP(launch_down_split(dm, q, s));
   const size_t n4 = static_cast<size_t>(T) * H / 4;
   acc_to_bf16_kernel<<<tc_sm_count() * 4, 256, 0, s>>>(out_acc, n4, out);
   TC_STEP(cudaGetLastError());

@@ -156,3 +156,28 @@ def test_block_nonfinite_input_sets_status_and_keeps_shared(env):
     assert (ids[1].cpu().numpy() == -1).all() and (ids[0].cpu().numpy() >= 0).all()
     blk.clear_status()
     assert blk.status() == 0
+
+
+@pytest.mark.parametrize("T", [200])
+def test_block_prefill_route_rows_odd_multiple_of_128(env, T):
+    """Prefill route with H, I, Is odd multiples of 128 (row chunks that cover
+    half a warp), every token checked against the oracle."""
+    import torch
+    moe, dev = env
+    dims = W.Dims(H=640, I=384, Is=384)
+    w = W.make_weights(dims, 11)
+    x, _ = W.make_x(dims, T, 12)
+    wd = {k: to_dev(v, dev) for k, v in w.items()}
+    blk = moe.MoEBlock(dims.H, dims.I, dims.Is, wd, T_max=T, device=dev)
+    out = torch.empty((T, dims.H), dtype=torch.int16, device=dev)
+    logits = torch.empty((T, 256), dtype=torch.float32, device=dev)
+    gate = torch.empty((T,), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
+    blk.forward(to_dev(x, dev), out=out, ids=ids, logits=logits, gate_logit=gate)
+    torch.cuda.synchronize()
+    assert blk.status() == 0
+    ref = oracle.block_forward(dims.as_dict(), w, x, route_logits=logits.cpu().numpy(),
+                               route_gate=gate.cpu().numpy(), nthreads=ncpu(),
+                               want=("out", "out_f64"))
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert_out_close(bits(out), ref["out"], "H640 prefill route")
