@@ -160,10 +160,10 @@ const char *const kStageNames[] = {"router_gemv", "select_top8", "expert_lists",
                                    "gateup_swiglu", "down", "combine"};
 constexpr int kStages = 6;
 const char *const kFusedStageNames[] = {"decode_fused"};
-const char *const kTcStageNames[] = {"router_tc", "router_gate_gemv", "select_top8",
-                                     "lists_items", "scale_gather", "gateup_swiglu_tc",
-                                     "h_scale", "down_combine_tc", "acc_to_bf16"};
-constexpr int kTcStages = 9;
+const char *const kTcStageNames[] = {"router_tc", "select_top8", "lists_items",
+                                     "scale_gather", "gateup_swiglu_tc", "h_scale",
+                                     "down_combine_tc", "acc_to_bf16"};
+constexpr int kTcStages = 8;
 
 // Records `ev[i]` after kernel i-1 when profiling (ev[0] before the first).
 struct Rec : StageRecorder {
@@ -224,14 +224,10 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   }
   int4 *items = at<int4>(ws, L.items);
   int *counters = at<int>(ws, L.counters);
-  MOE_TRY(launch_router_tc(x, T, H, w->w_router, logits, status, s));
+  MOE_TRY(launch_router_tc(x, T, H, w->w_router, logits, status, s, lists.counts));
   MOE_TRY(rec());
-  if (wg) {
-    MOE_TRY(launch_router_gemv(x, T, H, w->w_router, wg, logits, glog, s, true));
-    MOE_TRY(rec());
-  }
-  MOE_TRY(launch_select(logits, T, kE, wg ? glog : nullptr, ids, wts, wg ? sg : nullptr,
-                        status, s));
+  MOE_TRY(launch_select(logits, T, kE, nullptr, ids, wts, wg ? sg : nullptr, status, s, x, wg,
+                        H, glog, lists.counts));
   MOE_TRY(rec());
   MOE_TRY(launch_experts_tc(x, T, H, I, Is, *w, ids, lists, wts, wg ? sg : nullptr,
                             at<uint16_t>(ws, L.xs), at<uint16_t>(ws, L.x16),
@@ -440,7 +436,7 @@ int moe_block_kernel_count(const moe_dims *dims, int T) {
   const Route r = route_of(dims, T);
   if (r == kRouteFused) return 1;
   if (r == kRouteGemv) return kStages;
-  return dims->shared_inter > 0 ? kTcStages : kTcStages - 1;
+  return kTcStages;
 }
 
 const char *moe_block_kernel_name(const moe_dims *dims, int T, int i) {
@@ -449,7 +445,6 @@ const char *moe_block_kernel_name(const moe_dims *dims, int T, int i) {
   const Route r = route_of(dims, T);
   if (r == kRouteFused) return kFusedStageNames[i];
   if (r == kRouteGemv) return kStageNames[i];
-  if (dims->shared_inter == 0 && i >= 1) ++i;  // no gate-logit GEMV
   return kTcStageNames[i];
 }
 

@@ -28,10 +28,15 @@ cudaError_t launch_router_gemv(const moe_bf16 *x, int T, int H, const moe_bf16 *
                                const moe_bf16 *w_gate, float *logits, float *gate_logit,
                                cudaStream_t s, bool gate_only = false);
 
-// A2: one warp per token.
+// A2: one warp per token.  With x and w_gate given, the shared gate's logit
+// is computed here (written to gate_out when that is given) instead of read
+// from gate_logit; counts (optional, zero on entry) receives per-expert token
+// counts.
 cudaError_t launch_select(const float *logits, int T, int ld, const float *gate_logit,
                           int32_t *ids, float *weights, float *sgate, uint32_t *status,
-                          cudaStream_t s);
+                          cudaStream_t s, const moe_bf16 *x = nullptr,
+                          const moe_bf16 *w_gate = nullptr, int H = 0,
+                          float *gate_out = nullptr, int32_t *counts = nullptr);
 
 // A3: deterministic counting sort of the T*K entries (single CTA).
 cudaError_t launch_lists(const int32_t *ids, int T, Lists L, uint32_t *status, cudaStream_t s);
@@ -93,12 +98,15 @@ unsigned long long tc_wait_budget_ns();
 size_t tc_items_bytes(int T, int I, int Is, int H);
 
 // A1 router logits [T][E] as a tcgen05 GEMM (the gate row is left to the
-// GEMV launcher with gate_only = true).  `status` may be NULL.
+// selection kernel or to the GEMV launcher with gate_only = true).  `status`
+// may be NULL; zero_counts (optional, kE ints) is zeroed by the kernel.
 cudaError_t launch_router_tc(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
-                             float *logits, uint32_t *status, cudaStream_t s);
+                             float *logits, uint32_t *status, cudaStream_t s,
+                             int32_t *zero_counts = nullptr);
 
 // A3..A7 for prefill-size T: builds the token -> expert lists of ids [T][K]
-// into L (counts, offsets, perm, slot_of; not active) with the work items,
+// into L (offsets, perm, slot_of from the per-expert counts that the
+// selection left in L.counts; not active) with the work items,
 // the tokens' scaled fp16 copies (xs16 [T*K][H] in list order, x16 [T][H],
 // xscale [T]), runs gate|up + SwiGLU (h in bf16), converts h in place to
 // per-row scaled fp16 (2^s of each row in hscale [T*K + T]), runs down + weighted combine into out_acc [T][H] (fp32, zeroed

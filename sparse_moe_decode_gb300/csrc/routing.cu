@@ -98,13 +98,34 @@ cudaError_t launch_router_gemv(const moe_bf16 *x, int T, int H, const moe_bf16 *
 
 constexpr int kSelWarps = 4;
 
+// One warp per token.  The shared gate's logit comes from gate_logit, or,
+// when x and w_gate are given, from the token's own dot product with the gate
+// row (the same lane order and fp32 summation as the router kernels; written
+// to gate_out if that is given).  counts (optional, zeroed before the launch)
+// receives the number of tokens that select each expert.
 __global__ void __launch_bounds__(kSelWarps * 32)
 select_kernel(const float *__restrict__ logits, int T, int ld,
-              const float *__restrict__ gate_logit, int32_t *__restrict__ ids,
-              float *__restrict__ weights, float *__restrict__ sgate, uint32_t *status) {
+              const float *__restrict__ gate_logit, const moe_bf16 *__restrict__ x,
+              const moe_bf16 *__restrict__ w_gate, int H, float *__restrict__ gate_out,
+              int32_t *__restrict__ ids, float *__restrict__ weights, float *__restrict__ sgate,
+              int32_t *__restrict__ counts, uint32_t *status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (t >= T) return;
+  float g = 0.0f;
+  if (w_gate) {
+    const moe_bf16 *xr = x + static_cast<size_t>(t) * H;
+    for (int k = lane * 8; k < H; k += 256) {
+      const uint4 wv = ld_nc(w_gate + k), xv = ld_nc(xr + k);
+      g = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), g); g = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), g);
+      g = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), g); g = fmaf(bf16_hi(wv.y), bf16_hi(xv.y), g);
+      g = fmaf(bf16_lo(wv.z), bf16_lo(xv.z), g); g = fmaf(bf16_hi(wv.z), bf16_hi(xv.z), g);
+      g = fmaf(bf16_lo(wv.w), bf16_lo(xv.w), g); g = fmaf(bf16_hi(wv.w), bf16_hi(xv.w), g);
+    }
+    g = warp_sum(g);
+  } else if (gate_logit) {
+    g = gate_logit[t];
+  }
   int id[8];
   float w[8];
   const bool ok = select_top8_warp(logits + static_cast<size_t>(t) * ld, lane, id, w);
@@ -117,15 +138,20 @@ select_kernel(const float *__restrict__ logits, int T, int ld,
       if (lane == i) { myid = id[i]; myw = w[i]; }
     ids[static_cast<size_t>(t) * kK + lane] = myid;
     weights[static_cast<size_t>(t) * kK + lane] = myw;
+    if (counts && myid >= 0) atomicAdd(counts + myid, 1);
   }
-  if (lane == 0 && sgate && gate_logit) sgate[t] = sigmoidf_(gate_logit[t]);
+  if (lane == 0) {
+    if (sgate && (gate_logit || w_gate)) sgate[t] = sigmoidf_(g);
+    if (gate_out && w_gate) gate_out[t] = g;
+  }
 }
 
 cudaError_t launch_select(const float *logits, int T, int ld, const float *gate_logit,
                           int32_t *ids, float *weights, float *sgate, uint32_t *status,
-                          cudaStream_t s) {
+                          cudaStream_t s, const moe_bf16 *x, const moe_bf16 *w_gate, int H,
+                          float *gate_out, int32_t *counts) {
   select_kernel<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, s>>>(
-      logits, T, ld, gate_logit, ids, weights, sgate, status);
+      logits, T, ld, gate_logit, x, w_gate, H, gate_out, ids, weights, sgate, counts, status);
   return cudaGetLastError();
 }
 

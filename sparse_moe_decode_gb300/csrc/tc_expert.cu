@@ -761,11 +761,11 @@ down_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
 
 // ------------------------------------ token -> expert lists, work items
 
-// One CTA per expert e (grid kE, kLiThreads threads).  Every CTA histograms
-// all T*K entries (so it knows the offsets of the experts before it), then
-// compacts the entries with ids == e in entry order, which yields the list
-// sorted by (e, t, j) as the one-CTA counting sort does, and lays out e's
-// work items: gate|up -> (e, 64-row pair tile m, first list row, n), down ->
+// One CTA per expert e (grid kE, kLiThreads threads).  Every CTA reads the
+// per-expert counts of the selection (so it knows the offsets of the experts
+// before it), then compacts the entries with ids == e in entry order, which
+// yields the list sorted by (e, t, j) as the one-CTA counting sort does, and
+// lays out e's work items: gate|up -> (e, 64-row pair tile m, first list row, n), down ->
 // (e, 128-row tile m, first, n).  CTA 0 also writes the shared expert's items
 // (e == kE, B rows indexed by token), the item totals and slot_of = -1 for
 // entries that name no expert.
@@ -775,31 +775,15 @@ constexpr int kLiPer = 16;  // entries per thread and pass
 __global__ void __launch_bounds__(kLiThreads)
 lists_items_kernel(const int32_t *__restrict__ ids, int T, Lists L, int I, int Is, int H,
                    int4 *__restrict__ gu, int *__restrict__ n_gu, int4 *__restrict__ dn,
-                   int *__restrict__ n_dn, uint32_t *status) {
+                   int *__restrict__ n_dn) {
   __shared__ int hist[kE];
   __shared__ int pre[kE], tpre[kE];
   __shared__ int scan_tmp[32];
   __shared__ int run;
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = T * kK;
-  if (tid < kE) hist[tid] = 0;
+  if (tid < kE) hist[tid] = L.counts[tid];  // from the selection kernel
   if (tid == 0) run = 0;
-  __syncthreads();
-  bool bad = false;
-  for (int i0 = 0; i0 < n; i0 += kLiThreads * kLiPer) {
-    int v[kLiPer];
-#pragma unroll
-    for (int u = 0; u < kLiPer; ++u) {
-      const int i = i0 + u * kLiThreads + tid;
-      v[u] = i < n ? ids[i] : -1;
-    }
-#pragma unroll
-    for (int u = 0; u < kLiPer; ++u) {
-      if (v[u] >= kE) bad = true;
-      if (v[u] >= 0 && v[u] < kE) atomicAdd(&hist[v[u]], 1);
-    }
-  }
-  if (bad && e == 0) set_status(status, MOE_DEV_BAD_EXPERT);
   __syncthreads();
   const int c = tid < kE ? hist[tid] : 0;
   const int off = block_exclusive_scan_256(c, scan_tmp);
@@ -808,7 +792,6 @@ lists_items_kernel(const int32_t *__restrict__ ids, int T, Lists L, int I, int I
   __syncthreads();
   const int cnt = hist[e], base = pre[e];
   if (tid == 0) {
-    L.counts[e] = cnt;
     L.offsets[e] = base;
     if (e == kE - 1) L.offsets[kE] = base + cnt;
   }
@@ -1103,7 +1086,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   const size_t ts = (static_cast<size_t>(T) + kXTile - 1) / kXTile;
   int4 *dn = items + tiles * (I / 64) + ts * (Is / 64);
   lists_items_kernel<<<kE, kLiThreads, 0, s>>>(ids, T, L, I, Is, H, gu, counters, dn,
-                                              counters + 1, status);
+                                              counters + 1);
   TC_STEP(cudaGetLastError());
   scale_gather_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, L.slot_of, xs16, x16, xscale,
                                                    out_acc);

@@ -45,7 +45,7 @@ static_assert(sizeof(RBars) <= 256, "barrier block");
 __global__ void __launch_bounds__(kRThreads, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  int T, int H, float *__restrict__ logits, uint32_t *status,
-                 unsigned long long budget) {
+                 unsigned long long budget, int32_t *__restrict__ zero_counts) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -54,6 +54,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = 2 * ((T + kRTok - 1) / kRTok);
   const int nk = H / 64;
+  if (zero_counts && blockIdx.x == 0)  // per-expert counts of the selection that follows
+    for (int i = threadIdx.x; i < kE; i += blockDim.x) zero_counts[i] = 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRStages; ++i) {
@@ -231,7 +233,8 @@ unsigned long long tc_wait_budget_ns() {
 }
 
 cudaError_t launch_router_tc(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
-                             float *logits, uint32_t *status, cudaStream_t s) {
+                             float *logits, uint32_t *status, cudaStream_t s,
+                             int32_t *zero_counts) {
   CUtensorMap a, b;
   if (!tc_make_map(&a, w_router, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kE, H, 128, 64) ||
       !tc_make_map(&b, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, kRTok, 64))
@@ -249,7 +252,7 @@ cudaError_t launch_router_tc(const moe_bf16 *x, int T, int H, const moe_bf16 *w_
   const int n_items = 2 * ((T + kRTok - 1) / kRTok);
   const int grid = n_items < tc_sm_count() ? n_items : tc_sm_count();
   router_tc_kernel<<<grid, kRThreads, kRSmem, s>>>(a, b, T, H, logits, status,
-                                                   tc_wait_budget_ns());
+                                                   tc_wait_budget_ns(), zero_counts);
   return cudaGetLastError();
 }
 
