@@ -48,6 +48,26 @@ WORKLOAD_T = {"decode": 1, "verify": 32, "prefill": 2048}
 LABEL = {"decode": "decode_T1", "verify": "verify_T32", "prefill": "prefill_T2048"}
 
 
+def read_peak_gbs(torch, dev, gib: float = 2.0, reps: int = 5):
+    """Self-measured read-only HBM bandwidth: a reduction over a buffer far
+    larger than L2, best of reps, CUDA events (a measurement aid, not the
+    hot path)."""
+    n = int(gib * (1 << 30)) // 4
+    buf = torch.ones(n, dtype=torch.float32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = None
+    for _ in range(reps + 1):
+        e0.record()
+        buf.sum()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    del buf
+    torch.cuda.empty_cache()
+    return n * 4 / (best * 1e-3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -225,10 +245,14 @@ class Bench:
         # routing of each input (bank 0 computes the same ids up to relabelling)
         ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
         self.n_active = []
+        self.per_expert = []  # (min, max) tokens per expert over the 256 experts
         for r in range(banks):
             moe.moe_block_forward(self.dims, self.banks[0], self.x[r], T, self.out, ids, None,
                                   None, None, self.ws, self.ws_bytes)
-            self.n_active.append(len(np.unique(ids.cpu().numpy())))
+            h = ids.cpu().numpy().ravel()
+            self.n_active.append(len(np.unique(h[h >= 0])))
+            cnt = np.bincount(h[h >= 0], minlength=256)
+            self.per_expert.append((int(cnt.min()), int(cnt.max())))
         torch.cuda.synchronize()
         assert moe.moe_read_status(self.ws) == 0
 
@@ -425,6 +449,7 @@ def main():
         return float(t.item())
 
     pk = peaks()
+    read_gbs = read_peak_gbs(torch, dev) if world == 1 or rank == 0 else None
     order = [args.workload] + ([] if args.only else
                                [n for n in ("decode", "verify", "prefill") if n != args.workload])
     results = {}
@@ -450,6 +475,11 @@ def main():
             "achieved_gbs": gbs, "frac_hbm_measured": gbs / pk["hbm_gbs"],
             "frac_hbm_8000": gbs / 8000.0, "tflops": tfs,
             "frac_bf16_peak": tfs / pk["bf16_tflops"],
+            "frac_bf16_peak_sustained": (tfs / pk["bf16_tflops_sustained"]
+                                         if pk.get("bf16_tflops_sustained") else None),
+            "frac_hbm_read_self": gbs / read_gbs if read_gbs else None,
+            "tokens_per_expert_min_max": [min(a for a, _ in b.per_expert),
+                                          max(c for _, c in b.per_expert)],
             "frac_roofline_time": max(t_hbm, t_tc) / (ms * 1e-3),
             "kernels_ms": {n: float(v) for n, v in zip(b.kernel_names, per_kernel)},
             "dominant_kernel": b.kernel_names[k_dom], "wall_s": wall, "clocks": clk,
@@ -478,6 +508,7 @@ def main():
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
             "traffic": measured_traffic(kname, LABEL[args.workload]),
             "peak_src": pk["src"] + " (copy, burst)", "kernel_ms": kms,
+            "read_peak_self_gbs": read_gbs,
             "algorithmic_bytes_per_launch": kbytes}
     cb = cpu_baseline(args.workload, budget_s=args.cpu_budget) if world == 1 or rank == 0 else None
     line = {
