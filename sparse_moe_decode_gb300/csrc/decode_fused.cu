@@ -248,16 +248,17 @@ __device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams 
 }
 
 // Producer: issue gate|up unit j (expert e, row pairs i0..i0+7) into ring
-// stage j % kFStages.
-__device__ __forceinline__ void produce_gu(FusedSmem &S, const FusedParams &p, int j, int e,
+// stage j % kFStages; false if the stage was not issued (abort).
+__device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p, int j, int e,
                                            int i0, uint64_t pol, uint64_t budget, int lane) {
   const int s = j % kFStages;
+  int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
   if (lane == 0) {
     fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
-    if (!aborted(S)) ptx::mbar_expect_tx(&S.full[s], 16u * p.H + 2u * 8 * 2 * (p.H / kG));
+    go = aborted(S) ? 0 : 1;
+    if (go) ptx::mbar_expect_tx(&S.full[s], 16u * p.H + 2u * 8 * 2 * (p.H / kG));
   }
-  __syncwarp();
-  if (aborted(S)) return;
+  if (!__shfl_sync(0xFFFFFFFFu, go, 0)) return false;
   if (lane < 4) {
     // lanes 0/1: 8 consecutive gate / up rows, one contiguous copy of 8 * H
     // bytes each (bulk copies of >= 8 KB stream at full rate); lanes 2/3:
@@ -276,15 +277,18 @@ __device__ __forceinline__ void produce_gu(FusedSmem &S, const FusedParams &p, i
     }
   }
   __syncwarp();
+  return true;
 }
 
-// Producer: issue down stage k (units k*U .. ) into ring stage (n_local + k).
-__device__ __forceinline__ void produce_down(FusedSmem &S, const FusedParams &p, const Work &wk,
+// Producer: issue down stage k (units k*U .. ) into ring stage (n_local + k);
+// false if the stage was not issued (abort).
+__device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p, const Work &wk,
                                              int k, uint64_t pol, uint64_t budget, int lane) {
   const int j = wk.n_local + k;
   const int s = j % kFStages;
   const int u0 = k * wk.units_per_stage;
   const int nu = min(wk.units_per_stage, wk.n_down_units - u0);
+  int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
   if (lane == 0) {
     fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
     uint32_t tx = 0;
@@ -292,10 +296,10 @@ __device__ __forceinline__ void produce_down(FusedSmem &S, const FusedParams &p,
       const int Ii = down_unit(S, p, u0 + u) == kE ? p.Is : p.I;
       tx += 16u * Ii + 2u * 16 * (Ii / kG);
     }
-    if (!aborted(S)) ptx::mbar_expect_tx(&S.full[s], tx);
+    go = aborted(S) ? 0 : 1;
+    if (go) ptx::mbar_expect_tx(&S.full[s], tx);
   }
-  __syncwarp();
-  if (aborted(S)) return;
+  if (!__shfl_sync(0xFFFFFFFFu, go, 0)) return false;
   if (lane < 2 * nu) {
     // lane u < nu: one contiguous copy of unit u's 16 rows (16 * Ii bytes);
     // lane nu + u: their group scales (16 * Ii/128 bf16) into the scale area
@@ -314,6 +318,7 @@ __device__ __forceinline__ void produce_down(FusedSmem &S, const FusedParams &p,
     }
   }
   __syncwarp();
+  return true;
 }
 
 // Phase R: router partials.  Task (r, ks): one warp dots row r (256 expert
@@ -817,24 +822,24 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     const uint64_t pol = ptx::policy_evict_first();
     // the shared expert's unit needs no routing: fetch it at once
     const bool early = p.Is > 0 && static_cast<int>(blockIdx.x) < p.Is / 8;
-    if (early) produce_gu(S, p, 0, kE, 8 * blockIdx.x, pol, budget, lane);
+    int issued = 0;  // stages whose copies were issued
+    if (early && produce_gu(S, p, 0, kE, 8 * blockIdx.x, pol, budget, lane)) ++issued;
     if (lane == 0) fwait(&S.routed, 0, S, budget);
     __syncwarp();
     const Work wk = make_work(S, p);
-    int issued = early ? 1 : 0;
-    for (int j = issued; j < wk.n_local && !aborted(S); ++j, ++issued) {
+    for (int j = early ? 1 : 0; j < wk.n_local && !aborted(S); ++j) {
       int e, i0;
       gu_unit(S, wk, j, e, i0);
-      produce_gu(S, p, j, e, i0, pol, budget, lane);
+      if (produce_gu(S, p, j, e, i0, pol, budget, lane)) ++issued;
     }
-    for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k, ++issued)
-      produce_down(S, p, wk, k, pol, budget, lane);
+    for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k)
+      if (produce_down(S, p, wk, k, pol, budget, lane)) ++issued;
     // after an abort, let the copies already in flight land before exiting
     if (aborted(S) && lane == 0) {
       int never = 0;
       for (int k = 0; k < kFStages && k < issued; ++k) {
         const int j = issued - 1 - k;
-        ptx::mbar_wait(&S.full[j % kFStages], (j / kFStages) & 1, &never, budget);
+        ptx::mbar_wait(&S.full[j % kFStages], (j / kFStages) & 1, &never, ptx::kDrainBudgetNs);
       }
     }
   } else {

@@ -52,6 +52,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Budget of the waits that let work already in flight finish after an abort
+// (TMA copies landing, MMAs completing before TMEM is freed): independent of
+// the configurable budget of the pipeline waits, so that a small pipeline
+// budget still never frees shared or tensor memory under an operation.
+constexpr unsigned long long kDrainBudgetNs = 2000000000ull;
+
 // Bounded wait: spins until the phase with `parity` completes, `*abort`
 // becomes non-zero, or `budget_ns` of %globaltimer elapse.  Returns false if
 // it gave up (and then sets *abort).

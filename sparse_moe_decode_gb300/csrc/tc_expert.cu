@@ -215,11 +215,11 @@ gateup_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
         int never = 0;
         for (uint32_t k = 0; k < kXQS && k < nq; ++k) {
           const uint32_t j = nq - 1 - k;
-          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, budget);
+          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, ptx::kDrainBudgetNs);
         }
         for (uint32_t k = 0; k < kXBS && k < nb; ++k) {
           const uint32_t j = nb - 1 - k;
-          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, budget);
+          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, ptx::kDrainBudgetNs);
         }
       }
     }
@@ -264,7 +264,7 @@ gateup_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
       if (issued) {  // all MMAs complete before TMEM is released
         ptx::mma_commit(&bars->done[me]);
         int never = 0;
-        ptx::mbar_wait(&bars->done[me], 0, &never, budget);
+        ptx::mbar_wait(&bars->done[me], 0, &never, ptx::kDrainBudgetNs);
       }
     }
   } else if (warp < kGConv0 + kConv) {
@@ -533,11 +533,11 @@ down_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
         int never = 0;
         for (uint32_t k = 0; k < kXQS && k < nq; ++k) {
           const uint32_t j = nq - 1 - k;
-          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, budget);
+          ptx::mbar_wait(&bars->q_full[j % kXQS], (j / kXQS) & 1, &never, ptx::kDrainBudgetNs);
         }
         for (uint32_t k = 0; k < kXBS && k < nb; ++k) {
           const uint32_t j = nb - 1 - k;
-          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, budget);
+          ptx::mbar_wait(&bars->b_full[j % kXBS], (j / kXBS) & 1, &never, ptx::kDrainBudgetNs);
         }
       }
     }
@@ -582,7 +582,7 @@ down_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
       if (issued) {  // all MMAs complete before TMEM is released
         ptx::mma_commit(&bars->done[me]);
         int never = 0;
-        ptx::mbar_wait(&bars->done[me], 0, &never, budget);
+        ptx::mbar_wait(&bars->done[me], 0, &never, ptx::kDrainBudgetNs);
       }
     }
   } else if (warp < kGConv0 + kConv) {

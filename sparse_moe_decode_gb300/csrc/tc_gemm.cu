@@ -101,7 +101,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         int never = 0;
         for (uint32_t k = 0; k < kRStages && k < n; ++k) {
           const uint32_t j = n - 1 - k;
-          ptx::mbar_wait(&bars->full[j % kRStages], (j / kRStages) & 1, &never, budget);
+          ptx::mbar_wait(&bars->full[j % kRStages], (j / kRStages) & 1, &never, ptx::kDrainBudgetNs);
         }
       }
     }
@@ -132,7 +132,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       if (issued) {  // all MMAs complete before TMEM is released
         ptx::mma_commit(&bars->done);
         int never = 0;
-        ptx::mbar_wait(&bars->done, 0, &never, budget);
+        ptx::mbar_wait(&bars->done, 0, &never, ptx::kDrainBudgetNs);
       }
     }
   } else {
