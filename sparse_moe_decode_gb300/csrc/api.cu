@@ -201,7 +201,7 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
                                 at<float>(ws, L.xscale), at<float>(ws, L.rpart),
                                 at<int32_t>(ws, L.ids), at<float>(ws, L.weights),
                                 at<float>(ws, L.sgate), hr, hs, out, ids_out, weights_out,
-                                logits_out, gate_logit_out, status, grid_bar, s));
+                                logits_out, gate_logit_out, status, grid_bar, grid_bar + 1, s));
     MOE_TRY(rec());
     return MOE_OK;
   }

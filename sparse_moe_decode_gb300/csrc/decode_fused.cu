@@ -12,8 +12,10 @@
 //      barrier publishes the selections;
 //   L  every CTA builds the token -> expert lists in shared memory;
 //   W  gate|up + SwiGLU: work unit = 8 gate rows + their 8 up rows of one
-//      expert (16 rows x H int8); each CTA takes a contiguous, equal share
-//      of the routed units; a producer warp streams each unit's rows (and their
+//      expert (16 rows x H int8); the first Is / 8 CTAs take one shared
+//      unit each before routing is known, and the routed units are claimed
+//      from a grid-wide counter, so that faster CTAs take more of them; a
+//      producer warp streams each unit's rows (and their
 //      group scales) with bulk async copies into a 5-stage shared-memory ring
 //      (the shared expert's first units are fetched before routing is
 //      known); three warp quads consume units in turn, each warp a quarter
@@ -82,6 +84,7 @@ struct FusedParams {
   float *weights_out, *logits_out, *gate_logit_out;
   uint32_t *status;
   unsigned *grid_bar;
+  unsigned *unit_claims;  // routed gate|up units claimed so far (zeroed in phase R)
   unsigned long long budget_ns;
 };
 
@@ -104,6 +107,8 @@ struct FusedSmem {
   unsigned long long mask[kE];
   int scan_tmp[8];
   uint64_t full[kFStages], empty[kFStages], routed;
+  int2 stage_unit[kFStages];  // gate|up stage: (expert, first row pair); x < 0: no more units
+  int down_base;              // ring index of the first down stage
   uint64_t red_full[kFQuads][2], red_empty[kFQuads][2];
   int abort;
 };
@@ -193,9 +198,7 @@ __device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t 
 // Routing-derived work of this CTA (identical in every thread of the CTA).
 struct Work {
   int nSb, nIb;        // gate|up units of the shared expert, per routed expert
-  int has_shared;      // this CTA takes shared-expert unit blockIdx.x first
-  int r_begin;         // first routed unit of this CTA (contiguous range)
-  int n_local;         // gate|up units of this CTA
+  int has_shared;      // this CTA takes shared-expert unit blockIdx.x first (before routing)
   int n0;              // first output row of this CTA in the down phase (-1: none)
   int n_down_units;    // shared expert + active experts (0 if n0 < 0)
   int unit_stride;     // bytes of one down unit (16 rows) in a ring stage
@@ -203,22 +206,6 @@ struct Work {
   int units_per_stage;
   int n_down_stages;
 };
-
-// gate|up unit j of this CTA: the expert (kE = shared) and its first row
-// pair i0.  CTA c takes shared unit c (if any) first, then a contiguous run
-// of routed units, so consecutive units mostly share an expert (and its
-// tokens' activations).
-__device__ __forceinline__ void gu_unit(const FusedSmem &S, const Work &wk, int j, int &e,
-                                        int &i0) {
-  if (wk.has_shared && j == 0) {
-    e = kE;
-    i0 = 8 * static_cast<int>(blockIdx.x);
-  } else {
-    const int b = wk.r_begin + j - wk.has_shared;
-    e = S.active[1 + b / wk.nIb];
-    i0 = 8 * (b % wk.nIb);
-  }
-}
 
 // down unit u of this CTA: the expert (kE = shared)
 __device__ __forceinline__ int down_unit(const FusedSmem &S, const FusedParams &p, int u) {
@@ -231,12 +218,8 @@ __device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams 
   wk.nSb = p.Is / 8;
   wk.nIb = p.I / 8;
   const int n_active = S.active[0];
-  const int R = n_active * wk.nIb;  // routed units in the grid
-  const int c = blockIdx.x, G = gridDim.x;
+  const int c = blockIdx.x;
   wk.has_shared = c < wk.nSb ? 1 : 0;
-  wk.r_begin = static_cast<int>((static_cast<long long>(R) * c) / G);
-  const int r_end = static_cast<int>((static_cast<long long>(R) * (c + 1)) / G);
-  wk.n_local = wk.has_shared + (r_end - wk.r_begin);
   wk.n0 = 16 * static_cast<int>(blockIdx.x) < p.H ? 16 * static_cast<int>(blockIdx.x) : -1;
   wk.n_down_units = wk.n0 >= 0 ? (p.Is > 0 ? 1 : 0) + n_active : 0;
   const int imax = p.I > p.Is ? p.I : p.Is;
@@ -256,7 +239,10 @@ __device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p, i
   if (lane == 0) {
     fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
     go = aborted(S) ? 0 : 1;
-    if (go) ptx::mbar_expect_tx(&S.full[s], 16u * p.H + 2u * 8 * 2 * (p.H / kG));
+    if (go) {
+      S.stage_unit[s] = make_int2(e, i0);  // published by the arrival below
+      ptx::mbar_expect_tx(&S.full[s], 16u * p.H + 2u * 8 * 2 * (p.H / kG));
+    }
   }
   if (!__shfl_sync(0xFFFFFFFFu, go, 0)) return false;
   if (lane < 4) {
@@ -280,11 +266,11 @@ __device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p, i
   return true;
 }
 
-// Producer: issue down stage k (units k*U .. ) into ring stage (n_local + k);
-// false if the stage was not issued (abort).
+// Producer: issue down stage k (units k*U .. ) into ring stage
+// (S.down_base + k); false if the stage was not issued (abort).
 __device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p, const Work &wk,
                                              int k, uint64_t pol, uint64_t budget, int lane) {
-  const int j = wk.n_local + k;
+  const int j = S.down_base + k;
   const int s = j % kFStages;
   const int u0 = k * wk.units_per_stage;
   const int nu = min(wk.units_per_stage, wk.n_down_units - u0);
@@ -324,6 +310,7 @@ __device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p,
 // Phase R: router partials.  Task (r, ks): one warp dots row r (256 expert
 // rows, row 256 = shared gate) over K-slice ks (512 wide) with every token.
 __device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, int lane) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.unit_claims = 0u;  // claimed after barrier 1
   // Token scaling for the fp16 tensor-core path: warp gw < T writes token gw
   // as x * 2^-s in fp16 with s = exponent(max |x_t|) - 14, so the largest
   // magnitude lands in [2^14, 2^15).  A bf16 value (8 significant bits) is
@@ -616,13 +603,20 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 
 // Phase W consumer: gate|up unit j of this CTA, by quad q (warp wq of 4
 // takes K quarter wq).
-__device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, const Work &wk,
-                                           int j, int q, int wq, int lane, uint64_t budget,
-                                           uint32_t &npass) {
+// Returns false at the stage that marks the end of the gate|up units (after
+// releasing it).
+__device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, int j, int q,
+                                           int wq, int lane, uint64_t budget, uint32_t &npass) {
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
-  int e, i0;
-  gu_unit(S, wk, j, e, i0);
+  if (aborted(S)) return false;
+  const int2 un = S.stage_unit[s];
+  if (un.x < 0) {
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+    return false;
+  }
+  const int e = un.x, i0 = un.y;
   const bool sh = e == kE;
   const int n_tok = sh ? p.T : S.counts[e];
   const int p0 = sh ? 0 : S.offsets[e];
@@ -724,13 +718,14 @@ __device__ __forceinline__ void consume_gu(FusedSmem &S, const FusedParams &p, c
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
   }
+  return true;
 }
 
 // Phase D consumer: down stage k (units k*U ..), by quad q; warp wq takes
 // units wq, wq + 4, ... of the stage, each over its full K (= I or Is).
 __device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p, const Work &wk,
                                              int k, int wq, int lane, uint64_t budget) {
-  const int j = wk.n_local + k;
+  const int j = S.down_base + k;
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
   const int u0 = k * wk.units_per_stage;
@@ -822,25 +817,58 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     const uint64_t pol = ptx::policy_evict_first();
     // the shared expert's unit needs no routing: fetch it at once
     const bool early = p.Is > 0 && static_cast<int>(blockIdx.x) < p.Is / 8;
-    int issued = 0;  // stages whose copies were issued
-    if (early && produce_gu(S, p, 0, kE, 8 * blockIdx.x, pol, budget, lane)) ++issued;
+    // per ring slot, the latest stage whose copies were issued: after an
+    // abort only those can still be in flight (a slot is reused only after
+    // its previous copies landed and were consumed)
+    int last_use[kFStages];
+#pragma unroll
+    for (int i = 0; i < kFStages; ++i) last_use[i] = -1;
+    auto issued_at = [&](int jj) {
+#pragma unroll
+      for (int i = 0; i < kFStages; ++i)
+        if (jj % kFStages == i) last_use[i] = jj;
+    };
+    if (early && produce_gu(S, p, 0, kE, 8 * blockIdx.x, pol, budget, lane)) issued_at(0);
     if (lane == 0) fwait(&S.routed, 0, S, budget);
     __syncwarp();
     const Work wk = make_work(S, p);
-    for (int j = early ? 1 : 0; j < wk.n_local && !aborted(S); ++j) {
-      int e, i0;
-      gu_unit(S, wk, j, e, i0);
-      if (produce_gu(S, p, j, e, i0, pol, budget, lane)) ++issued;
+    // Routed gate|up units are claimed from a grid-wide counter, one ahead,
+    // so that CTAs that run faster take more of them.
+    const unsigned n_routed = static_cast<unsigned>(S.active[0] * wk.nIb);
+    unsigned claim = 0;
+    if (lane == 0) claim = atomicAdd(p.unit_claims, 1u);
+    claim = __shfl_sync(0xFFFFFFFFu, claim, 0);
+    int j = early ? 1 : 0;  // ring index of the next stage
+    while (claim < n_routed && !aborted(S)) {
+      const unsigned b = claim;
+      unsigned nx = 0;
+      if (lane == 0) nx = atomicAdd(p.unit_claims, 1u);
+      const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
+      if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
+      ++j;
+      claim = __shfl_sync(0xFFFFFFFFu, nx, 0);
+    }
+    // one end marker per quad, then the down stages
+    for (int k = 0; k < kFQuads && !aborted(S); ++k, ++j) {
+      if (lane == 0) {
+        fwait(&S.empty[j % kFStages], ((j / kFStages) & 1) ^ 1, S, budget);
+        if (!aborted(S)) {
+          S.down_base = j - k + kFQuads;
+          S.stage_unit[j % kFStages] = make_int2(-1, 0);
+          ptx::mbar_arrive(&S.full[j % kFStages]);
+        }
+      }
+      __syncwarp();
     }
     for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k)
-      if (produce_down(S, p, wk, k, pol, budget, lane)) ++issued;
+      if (produce_down(S, p, wk, k, pol, budget, lane)) issued_at(S.down_base + k);
     // after an abort, let the copies already in flight land before exiting
     if (aborted(S) && lane == 0) {
       int never = 0;
-      for (int k = 0; k < kFStages && k < issued; ++k) {
-        const int j = issued - 1 - k;
-        ptx::mbar_wait(&S.full[j % kFStages], (j / kFStages) & 1, &never, ptx::kDrainBudgetNs);
-      }
+#pragma unroll
+      for (int i = 0; i < kFStages; ++i)
+        if (last_use[i] >= 0)
+          ptx::mbar_wait(&S.full[i], (last_use[i] / kFStages) & 1, &never, ptx::kDrainBudgetNs);
     }
   } else {
     // ----------------------------------------------------------- consumers
@@ -851,8 +879,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
     uint32_t npass = 0;
-    for (int j = q; j < wk.n_local; j += kFQuads)
-      consume_gu(S, p, wk, j, q, wq, lane, budget, npass);
+    for (int j = q; consume_gu(S, p, j, q, wq, lane, budget, npass); j += kFQuads) {
+    }
     grid_sync(p.grid_bar, S, budget);
     for (int k = q; k < wk.n_down_stages; k += kFQuads)
       consume_down(S, p, wk, k, wq, lane, budget);
@@ -915,7 +943,8 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 float *sel_sg, moe_bf16 *h_routed,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
-                                uint32_t *status, unsigned *grid_bar, cudaStream_t s) {
+                                uint32_t *status, unsigned *grid_bar, unsigned *unit_claims,
+                                cudaStream_t s) {
   FusedParams p{};
   p.x = x; p.x16 = x16; p.xscale = xscale;
   p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 512;
@@ -923,6 +952,7 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
   p.w13_q = w.w13_q; p.w13_s = w.w13_s; p.w2_q = w.w2_q; p.w2_s = w.w2_s;
   p.ws13_q = w.ws13_q; p.ws13_s = w.ws13_s; p.ws2_q = w.ws2_q; p.ws2_s = w.ws2_s;
   p.rpart = rpart; p.sel_ids = sel_ids; p.sel_w = sel_w; p.sel_sg = sel_sg;
+  p.unit_claims = unit_claims;
   p.h_routed = h_routed; p.h_shared = h_shared; p.out = out;
   p.ids_out = ids_out; p.weights_out = weights_out; p.logits_out = logits_out;
   p.gate_logit_out = gate_logit_out; p.status = status; p.grid_bar = grid_bar;
