@@ -317,9 +317,15 @@ __device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, in
   // exact in fp16 whenever the scaled value is a normal fp16, i.e. for every
   // element within 2^29 of the token's largest; smaller ones are off by less
   // than 2^-40 of that largest.  2^s is undone on the fp32 results.
+  // The router tasks go to the first warps of the grid; the token scaling
+  // goes to the warps after them when the grid has that many, so that no
+  // warp does both.
+  const int n_tasks = (kE + (p.Is > 0 ? 1 : 0)) * p.KS;
+  const int n_warps = static_cast<int>(gridDim.x) * kFConsumerWarps;
   {
-    const int gw = blockIdx.x * kFConsumerWarps + cwarp;
-    if (gw < p.T) {
+    const int gwarp = blockIdx.x * kFConsumerWarps + cwarp;
+    const int gw = n_tasks + p.T <= n_warps ? gwarp - n_tasks : gwarp;
+    if (gw >= 0 && gw < p.T) {
       const moe_bf16 *xr = p.x + static_cast<size_t>(gw) * p.H;
       float m = 0.0f;
       for (int k = lane * 8; k < p.H; k += 256) {
@@ -352,8 +358,6 @@ __device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, in
       if (lane == 0) p.xscale[gw] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
     }
   }
-  const int rows = kE + (p.Is > 0 ? 1 : 0);
-  const int n_tasks = rows * p.KS;
   for (int task = blockIdx.x * kFConsumerWarps + cwarp; task < n_tasks;
        task += gridDim.x * kFConsumerWarps) {
     const int r = task / p.KS, ks = task % p.KS;
