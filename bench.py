@@ -167,16 +167,16 @@ def down_bytes(d: W.Dims, T: int, n_active: int):
 MEASURED_TRAFFIC = {
     "decode_fused": {"bytes": 529.0e6, "workload": "verify_T32",
                      "sources": ["decode_fused.cu", "common.cuh", "select.cuh", "sm100_ptx.cuh"],
-                     "sha256_16": "20609ec655a8ff00",
+                     "sha256_16": "d270be78367bb0c1",
                      "profile": "profiles/decode_fused_verify_T32.md"},
-    "gateup_swiglu_tc": {"bytes": 645.0e6, "workload": "prefill_T2048",
+    "gateup_swiglu_tc": {"bytes": 646.5e6, "workload": "prefill_T2048",
                          "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],
-                         "sha256_16": "e9de3cd0acd53d86",
-                         "profile": "profiles/tc_expert_prefill_T2048.md"},
-    "down_combine_tc": {"bytes": 314.5e6, "workload": "prefill_T2048",
+                         "sha256_16": "15d66d1e5a1f6cff",
+                         "profile": "profiles/split_kernels_prefill_T2048.md"},
+    "down_combine_tc": {"bytes": 315.8e6, "workload": "prefill_T2048",
                         "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],
-                        "sha256_16": "e9de3cd0acd53d86",
-                        "profile": "profiles/tc_expert_prefill_T2048.md"},
+                        "sha256_16": "15d66d1e5a1f6cff",
+                        "profile": "profiles/split_kernels_prefill_T2048.md"},
 }
 
 
