@@ -58,6 +58,7 @@ constexpr int kFScaleBytes = 512;              // the group scales of a stage's 
 constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
 constexpr int kRP = 260;                     // router partial row: 257 used, 16-byte rows
 constexpr int kFLocalSelT = kFConsumerWarps;  // tokens selected by every CTA itself
+constexpr int kFClaim = 4;  // routed gate|up units per claim of the grid-wide counter
 
 struct FusedParams {
   const moe_bf16 *x;
@@ -836,20 +837,24 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     if (lane == 0) fwait(&S.routed, 0, S, budget);
     __syncwarp();
     const Work wk = make_work(S, p);
-    // Routed gate|up units are claimed from a grid-wide counter, one ahead,
-    // so that CTAs that run faster take more of them.
+    // Routed gate|up units are claimed from a grid-wide counter, kFClaim
+    // consecutive units (rows of one expert) at a time and one claim ahead,
+    // so that CTAs that run faster take more of them while the counter's
+    // round trip overlaps the issue of the units already claimed.
     const unsigned n_routed = static_cast<unsigned>(S.active[0] * wk.nIb);
     unsigned claim = 0;
-    if (lane == 0) claim = atomicAdd(p.unit_claims, 1u);
+    if (lane == 0) claim = atomicAdd(p.unit_claims, static_cast<unsigned>(kFClaim));
     claim = __shfl_sync(0xFFFFFFFFu, claim, 0);
     int j = early ? 1 : 0;  // ring index of the next stage
     while (claim < n_routed && !aborted(S)) {
-      const unsigned b = claim;
       unsigned nx = 0;
-      if (lane == 0) nx = atomicAdd(p.unit_claims, 1u);
-      const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
-      if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
-      ++j;
+      if (lane == 0) nx = atomicAdd(p.unit_claims, static_cast<unsigned>(kFClaim));
+      const unsigned end = min(claim + static_cast<unsigned>(kFClaim), n_routed);
+      for (unsigned b = claim; b < end && !aborted(S); ++b) {
+        const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
+        if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
+        ++j;
+      }
       claim = __shfl_sync(0xFFFFFFFFu, nx, 0);
     }
     // one end marker per quad, then the down stages
