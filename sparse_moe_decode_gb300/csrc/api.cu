@@ -107,7 +107,7 @@ Layout layout(const moe_dims *d, int T) {
   L.h_routed = take(2 * t * kK * I);
   L.h_shared = take(2 * t * (Is ? Is : 1));
   const Route r = route_of(d, T);
-  if (r == kRouteGemv) L.y = take(4 * t * (kK + 1) * H);
+  if (r == kRouteGemv || r == kRouteFused) L.y = take(4 * t * (kK + 1) * H);
   if (r == kRouteFused) L.rpart = take(4 * t * 260 * (H / 512));
   if (r == kRouteFused || r == kRouteTc) {
     L.x16 = take(2 * t * H);
@@ -201,7 +201,8 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
                                 at<float>(ws, L.xscale), at<float>(ws, L.rpart),
                                 at<int32_t>(ws, L.ids), at<float>(ws, L.weights),
                                 at<float>(ws, L.sgate), hr, hs, out, ids_out, weights_out,
-                                logits_out, gate_logit_out, status, grid_bar, grid_bar + 1, s));
+                                logits_out, gate_logit_out, status, grid_bar, grid_bar + 1,
+                                grid_bar + 2, at<float>(ws, L.y), s));
     MOE_TRY(rec());
     return MOE_OK;
   }

@@ -1,6 +1,6 @@
 // decode_fused.cu -- the whole block (A1..A7) for decode-size T in one
-// persistent cooperative kernel: one CTA per SM, phases separated by two
-// bounded grid barriers (three when T > 12).
+// persistent cooperative kernel: one CTA per SM, phases separated by three
+// bounded grid barriers (four when T > 12).
 //
 //   R  router: 257 rows x (H/512) K-slices of 512, one warp each, fp32
 //      partials (the pages' S1 split of the router into K-slices);
@@ -26,10 +26,20 @@
 //      group in fp32, a rotating reducer warp adds the four K quarters;
 //      h = bf16(silu(gate) * up) goes to global;
 //   -- grid barrier 2 --
-//   D  down + combine: CTA c owns output rows 16c .. 16c+15 of every expert;
-//      the producer has been streaming those rows since its gate|up units
-//      were done; y for every (token, slot) of those rows stays in shared
-//      memory and the CTA writes the combined bf16 output rows itself.
+//   D  down + combine, two modes chosen by T (the same in every CTA).
+//      Item mode (T > kFRowOwnerT): work item = R consecutive output rows
+//      (R * max(I, Is) = one 32 KB stage) of one expert, claimed from a
+//      second grid-wide counter by the producers as soon as their gate|up
+//      claims run out, so the down weights stream in while the gate|up tail
+//      is still computing; each warp of the consuming quad takes 16 of the
+//      rows over the full K, and y for every (slot, row) goes to global
+//      memory (fp32); after a third grid barrier every thread of the grid
+//      forms two output elements.  Row-owner mode (small T, where the extra
+//      barrier would cost more than the even split of the bytes gains): CTA
+//      c owns output rows 16c .. 16c+15 of every expert, its y stays in
+//      shared memory and the CTA writes its combined rows itself.  Both
+//      combine the 8 routed y in rank order, then the shared expert's, with
+//      one bf16 rounding.
 //
 // The tensor cores here are the register-fragment form (mma.sync): at
 // decode sizes each weight meets 1..~10 tokens, the kernel is bound by HBM,
@@ -58,11 +68,12 @@ constexpr int kFScaleBytes = 512;              // the group scales of a stage's 
 constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
 constexpr int kRP = 260;                     // router partial row: 257 used, 16-byte rows
 constexpr int kFLocalSelT = kFConsumerWarps;  // tokens selected by every CTA itself
-constexpr int kFClaim = 4;  // routed gate|up units per claim of the grid-wide counter
+constexpr int kFClaim = 4;  // routed gate|up units per claim when there are many
+constexpr int kFRowOwnerT = 8;  // down phase in row-owner mode up to this T
 
 struct FusedParams {
   const moe_bf16 *x;
-  uint16_t *x16;        // [T][H] fp16: x * 2^-xexp[t], exact (see phase_router)
+  uint16_t *x16;        // [T][H] fp16: x * 2^-xexp[t], exact (see scale_token)
   float *xscale;        // [T] 2^xexp[t]
   int T, H, I, Is, KS;  // KS = H / 512 router K-slices
   const moe_bf16 *w_router, *w_gate;
@@ -80,12 +91,14 @@ struct FusedParams {
   float *sel_sg;       // [T]
   moe_bf16 *h_routed;  // [T*K][I], rows in list order
   moe_bf16 *h_shared;  // [T][Is]
+  float *y;            // [T*K + T][H] down outputs: routed slots in list order, then shared
   moe_bf16 *out;       // [T][H]
   int32_t *ids_out;
   float *weights_out, *logits_out, *gate_logit_out;
   uint32_t *status;
   unsigned *grid_bar;
   unsigned *unit_claims;  // routed gate|up units claimed so far (zeroed in phase R)
+  unsigned *down_claims;  // down items claimed so far (zeroed in phase R)
   unsigned long long budget_ns;
 };
 
@@ -93,8 +106,8 @@ struct FusedSmem {
   uint8_t ring[kFStages][kFStageBytes];
   uint8_t ring_s[kFStages][kFScaleBytes];  // bf16 scales of each stage's rows
   union {
-    float red[kFQuads][2][4][2][32][4];      // gate|up: quad reduction, 2 buffers
-    float ys[16][kFusedMaxT * (kK + 1)];     // down: y of this CTA's 16 rows
+    float red[kFQuads][2][4][2][32][4];        // gate|up: quad reduction, 2 buffers
+    float ys[16][kFRowOwnerT * (kK + 1)];      // row-owner down: y of this CTA's 16 rows
   } u;
   int32_t ids[kFusedMaxT][kK];
   float wts[kFusedMaxT][kK];
@@ -108,7 +121,7 @@ struct FusedSmem {
   unsigned long long mask[kE];
   int scan_tmp[8];
   uint64_t full[kFStages], empty[kFStages], routed;
-  int2 stage_unit[kFStages];  // gate|up stage: (expert, first row pair); x < 0: no more units
+  int2 stage_unit[kFStages];  // (expert, first row pair | first output row); x < 0: end
   int down_base;              // ring index of the first down stage
   uint64_t red_full[kFQuads][2], red_empty[kFQuads][2];
   int abort;
@@ -146,9 +159,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 }
 
 // Loads of data written earlier in this launch by other CTAs: L2 only.
-__device__ __forceinline__ uint4 ld_cg16(const void *p) {
-  return __ldcg(reinterpret_cast<const uint4 *>(p));
-}
 
 __device__ __forceinline__ uint4 ld_ca16(const void *p) {
   return __ldca(reinterpret_cast<const uint4 *>(p));
@@ -196,39 +206,53 @@ __device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t 
   ptx::named_barrier(1, kFConsumers);
 }
 
-// Routing-derived work of this CTA (identical in every thread of the CTA).
+// Routing-derived work sizes (identical in every thread of the CTA; the
+// mode and the item sizes are identical in every CTA).
 struct Work {
-  int nSb, nIb;        // gate|up units of the shared expert, per routed expert
-  int has_shared;      // this CTA takes shared-expert unit blockIdx.x first (before routing)
-  int n0;              // first output row of this CTA in the down phase (-1: none)
-  int n_down_units;    // shared expert + active experts (0 if n0 < 0)
-  int unit_stride;     // bytes of one down unit (16 rows) in a ring stage
-  int scale_stride;    // bytes of one down unit's scales in the stage's scale area
+  int nSb, nIb;         // gate|up units of the shared expert, per routed expert
+  int n_exp;            // experts with down work: the shared one (if any) + the active ones
+  int row_owner;        // down mode (see the file comment)
+  // item mode
+  int down_rows;        // R: output rows of one down item (a multiple of 16)
+  int nrb;              // down items per expert: ceil(H / R)
+  // row-owner mode
+  int n0;               // first output row of this CTA (-1: none)
+  int unit_stride;      // bytes of one 16-row unit in a ring stage
+  int scale_stride;     // bytes of one unit's scales in the stage's scale area
   int units_per_stage;
-  int n_down_stages;
+  int n_down_stages;    // of this CTA
 };
-
-// down unit u of this CTA: the expert (kE = shared)
-__device__ __forceinline__ int down_unit(const FusedSmem &S, const FusedParams &p, int u) {
-  if (p.Is > 0) return u == 0 ? kE : S.active[u];
-  return S.active[1 + u];
-}
 
 __device__ __forceinline__ Work make_work(const FusedSmem &S, const FusedParams &p) {
   Work wk;
   wk.nSb = p.Is / 8;
   wk.nIb = p.I / 8;
-  const int n_active = S.active[0];
-  const int c = blockIdx.x;
-  wk.has_shared = c < wk.nSb ? 1 : 0;
-  wk.n0 = 16 * static_cast<int>(blockIdx.x) < p.H ? 16 * static_cast<int>(blockIdx.x) : -1;
-  wk.n_down_units = wk.n0 >= 0 ? (p.Is > 0 ? 1 : 0) + n_active : 0;
+  wk.n_exp = (p.Is > 0 ? 1 : 0) + S.active[0];
+  wk.row_owner = p.T <= kFRowOwnerT ? 1 : 0;
   const int imax = p.I > p.Is ? p.I : p.Is;
+  // R rows of K <= imax fill at most one stage; their scales (R * imax/128
+  // bf16) then fit the stage's 512-byte scale area
+  wk.down_rows = min(p.H, (kFStageBytes / imax) & ~15);
+  wk.nrb = (p.H + wk.down_rows - 1) / wk.down_rows;
+  wk.n0 = 16 * static_cast<int>(blockIdx.x) < p.H ? 16 * static_cast<int>(blockIdx.x) : -1;
   wk.unit_stride = 16 * imax;
   wk.scale_stride = 2 * 16 * (imax / kG);
   wk.units_per_stage = kFStageBytes / wk.unit_stride;
-  wk.n_down_stages = (wk.n_down_units + wk.units_per_stage - 1) / wk.units_per_stage;
+  const int nu = wk.n0 >= 0 ? wk.n_exp : 0;
+  wk.n_down_stages = (nu + wk.units_per_stage - 1) / wk.units_per_stage;
   return wk;
+}
+
+// down expert a (0 .. n_exp - 1): the shared expert (kE) first, then the active ones
+__device__ __forceinline__ int down_expert(const FusedSmem &S, const FusedParams &p, int a) {
+  return p.Is > 0 ? (a == 0 ? kE : S.active[a]) : S.active[1 + a];
+}
+
+// down item b (item mode): the expert and its first output row
+__device__ __forceinline__ int2 down_item(const FusedSmem &S, const FusedParams &p,
+                                          const Work &wk, unsigned b) {
+  const int a = static_cast<int>(b) / wk.nrb, rb = static_cast<int>(b) % wk.nrb;
+  return make_int2(down_expert(S, p, a), rb * wk.down_rows);
 }
 
 // Producer: issue gate|up unit j (expert e, row pairs i0..i0+7) into ring
@@ -267,129 +291,185 @@ __device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p, i
   return true;
 }
 
-// Producer: issue down stage k (units k*U .. ) into ring stage
-// (S.down_base + k); false if the stage was not issued (abort).
+// Producer: issue down stage j.  Item mode: item (e, n0) = rows n0 ..
+// n0 + nr - 1 of expert e's down matrix (nr * K contiguous bytes) and their
+// group scales.  Row-owner mode (item = (kE + 1, k)): this CTA's stage k,
+// the 16 rows n0 of down experts k * U .., one contiguous copy each, at a
+// fixed stride.  False if the stage was not issued (abort).
 __device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p, const Work &wk,
-                                             int k, uint64_t pol, uint64_t budget, int lane) {
-  const int j = S.down_base + k;
+                                             int j, int2 item, uint64_t pol, uint64_t budget,
+                                             int lane) {
   const int s = j % kFStages;
-  const int u0 = k * wk.units_per_stage;
-  const int nu = min(wk.units_per_stage, wk.n_down_units - u0);
+  const bool rows = item.x > kE;
+  const int a0 = rows ? item.y * wk.units_per_stage : 0;
+  const int nu = rows ? min(wk.units_per_stage, wk.n_exp - a0) : 1;
   int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
   if (lane == 0) {
     fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
     uint32_t tx = 0;
     for (int u = 0; u < nu; ++u) {
-      const int Ii = down_unit(S, p, u0 + u) == kE ? p.Is : p.I;
-      tx += 16u * Ii + 2u * 16 * (Ii / kG);
+      const int e = rows ? down_expert(S, p, a0 + u) : item.x;
+      const int Ii = e == kE ? p.Is : p.I;
+      const int nr = rows ? 16 : min(wk.down_rows, p.H - item.y);
+      tx += static_cast<uint32_t>(nr) * Ii + 2u * nr * (Ii / kG);
     }
     go = aborted(S) ? 0 : 1;
-    if (go) ptx::mbar_expect_tx(&S.full[s], tx);
+    if (go) {
+      S.stage_unit[s] = item;  // published by the arrival below
+      ptx::mbar_expect_tx(&S.full[s], tx);
+    }
   }
   if (!__shfl_sync(0xFFFFFFFFu, go, 0)) return false;
   if (lane < 2 * nu) {
-    // lane u < nu: one contiguous copy of unit u's 16 rows (16 * Ii bytes);
-    // lane nu + u: their group scales (16 * Ii/128 bf16) into the scale area
+    // lane u < nu: unit u's rows; lane nu + u: their group scales
     const int u = lane < nu ? lane : lane - nu;
-    const int e = down_unit(S, p, u0 + u);
+    const int e = rows ? down_expert(S, p, a0 + u) : item.x;
     const int Ii = e == kE ? p.Is : p.I;
+    const int ng = Ii / kG;
+    const int n0 = rows ? wk.n0 : item.y;
+    const int nr = rows ? 16 : min(wk.down_rows, p.H - n0);
     if (lane < nu) {
-      const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(wk.n0) * p.Is
-                                  : p.w2_q + (static_cast<size_t>(e) * p.H + wk.n0) * p.I;
-      bulk_g2s(S.ring[s] + u * wk.unit_stride, src, 16u * Ii, &S.full[s], pol);
+      const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(n0) * p.Is
+                                  : p.w2_q + (static_cast<size_t>(e) * p.H + n0) * p.I;
+      bulk_g2s(S.ring[s] + u * wk.unit_stride, src, static_cast<uint32_t>(nr) * Ii, &S.full[s],
+               pol);
     } else {
-      const int ng = Ii / kG;
-      const moe_bf16 *src = e == kE ? p.ws2_s + static_cast<size_t>(wk.n0) * ng
-                                    : p.w2_s + (static_cast<size_t>(e) * p.H + wk.n0) * ng;
-      bulk_g2s(S.ring_s[s] + u * wk.scale_stride, src, 2u * 16 * ng, &S.full[s], pol);
+      const moe_bf16 *src = e == kE ? p.ws2_s + static_cast<size_t>(n0) * ng
+                                    : p.w2_s + (static_cast<size_t>(e) * p.H + n0) * ng;
+      bulk_g2s(S.ring_s[s] + u * wk.scale_stride, src, 2u * nr * ng, &S.full[s], pol);
     }
   }
   __syncwarp();
   return true;
 }
 
-// Phase R: router partials.  Task (r, ks): one warp dots row r (256 expert
-// rows, row 256 = shared gate) over K-slice ks (512 wide) with every token.
-__device__ __forceinline__ void phase_router(const FusedParams &p, int cwarp, int lane) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.unit_claims = 0u;  // claimed after barrier 1
-  // Token scaling for the fp16 tensor-core path: warp gw < T writes token gw
-  // as x * 2^-s in fp16 with s = exponent(max |x_t|) - 14, so the largest
-  // magnitude lands in [2^14, 2^15).  A bf16 value (8 significant bits) is
-  // exact in fp16 whenever the scaled value is a normal fp16, i.e. for every
-  // element within 2^29 of the token's largest; smaller ones are off by less
-  // than 2^-40 of that largest.  2^s is undone on the fp32 results.
-  // The router tasks go to the first warps of the grid; the token scaling
-  // goes to the warps after them when the grid has that many, so that no
-  // warp does both.
-  const int n_tasks = (kE + (p.Is > 0 ? 1 : 0)) * p.KS;
-  const int n_warps = static_cast<int>(gridDim.x) * kFConsumerWarps;
-  {
-    const int gwarp = blockIdx.x * kFConsumerWarps + cwarp;
-    const int gw = n_tasks + p.T <= n_warps ? gwarp - n_tasks : gwarp;
-    if (gw >= 0 && gw < p.T) {
-      const moe_bf16 *xr = p.x + static_cast<size_t>(gw) * p.H;
-      float m = 0.0f;
-      for (int k = lane * 8; k < p.H; k += 256) {
-        const uint4 v = ld_nc(xr + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Token scaling for the fp16 tensor-core path: token t becomes x * 2^-s in
+// fp16 with s = exponent(max |x_t|) - 14, so the largest magnitude lands in
+// [2^14, 2^15).  A bf16 value (8 significant bits) is exact in fp16 whenever
+// the scaled value is a normal fp16, i.e. for every element within 2^29 of
+// the token's largest; smaller ones are off by less than 2^-40 of that
+// largest.  2^s is undone on the fp32 results.  One warp.
+__device__ __forceinline__ void scale_token(const FusedParams &p, int t, int lane) {
+  const moe_bf16 *xr = p.x + static_cast<size_t>(t) * p.H;
+  float m = 0.0f;
+  for (int k = lane * 8; k < p.H; k += 256) {
+    const uint4 v = ld_nc(xr + k);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      int sexp = 0;
-      if (m > 0.0f && isfinite(m)) {
-        sexp = static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14;
-        sexp = max(-110, min(110, sexp));
-      }
-      const float down = __uint_as_float(static_cast<uint32_t>(127 - sexp) << 23);  // 2^-s
-      for (int k = lane * 8; k < p.H; k += 256) {
-        const uint4 v = ld_nc(xr + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 h = __floats2half2_rn(bf16_lo(w[i]) * down, bf16_hi(w[i]) * down);
-          o[i] = *reinterpret_cast<const uint32_t *>(&h);
-        }
-        *reinterpret_cast<uint4 *>(p.x16 + static_cast<size_t>(gw) * p.H + k) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      if (lane == 0) p.xscale[gw] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
-    }
+    for (int i = 0; i < 4; ++i)
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
   }
-  for (int task = blockIdx.x * kFConsumerWarps + cwarp; task < n_tasks;
-       task += gridDim.x * kFConsumerWarps) {
-    const int r = task / p.KS, ks = task % p.KS;
-    const int k = ks * 512 + lane * 16;
-    const moe_bf16 *wrow = r < kE ? p.w_router + static_cast<size_t>(r) * p.H : p.w_gate;
-    const uint4 wv0 = ld_nc(wrow + k), wv1 = ld_nc(wrow + k + 8);
-    const uint32_t wq[8] = {wv0.x, wv0.y, wv0.z, wv0.w, wv1.x, wv1.y, wv1.z, wv1.w};
-    for (int t0 = 0; t0 < p.T; t0 += 8) {
-      uint4 xa[8], xb[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (t0 + u < p.T) {
-          xa[u] = ld_nc(p.x + static_cast<size_t>(t0 + u) * p.H + k);
-          xb[u] = ld_nc(p.x + static_cast<size_t>(t0 + u) * p.H + k + 8);
-        }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (t0 + u >= p.T) break;
-        const uint32_t xq[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w,
-                                xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          a = fmaf(bf16_lo(wq[i]), bf16_lo(xq[i]), a);
-          a = fmaf(bf16_hi(wq[i]), bf16_hi(xq[i]), a);
-        }
-        a = warp_sum(a);
-        if (lane == 0) p.rpart[(static_cast<size_t>(t0 + u) * p.KS + ks) * kRP + r] = a;
-      }
-    }
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  int sexp = 0;
+  if (m > 0.0f && isfinite(m)) {
+    sexp = static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127 - 14;
+    sexp = max(-110, min(110, sexp));
   }
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - sexp) << 23);  // 2^-s
+  for (int k = lane * 8; k < p.H; k += 256) {
+    const uint4 v = ld_nc(xr + k);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(bf16_lo(w[i]) * down, bf16_hi(w[i]) * down);
+      o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p.x16 + static_cast<size_t>(t) * p.H + k) =
+        make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) p.xscale[t] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
+}
+
+// Phase R: router partials (the pages' split of the router GEMV into
+// K-slices).  CTA c takes K-slice ks = c mod KS (512 wide) of a group of at
+// most 16 rows (256 expert rows, row 256 = the shared gate): it stages the
+// slices of every token and of its rows in shared memory (ring stages 1..,
+// unused until routing is known; rows padded to 1040 bytes so that the
+// fragment loads below hit distinct banks), all loads in flight at once.
+// Task (nt, kq) is one warp: bf16 m16n8k16 tensor-core MMAs (products
+// exact, fp32 accumulation) of tokens 8nt .. 8nt+7 over the slice's K
+// quarter kq; the four quarters are then added in order.  Every token's
+// partials are formed the same way whatever T is, so a token's routing
+// does not depend on the batch it rides in.  The last warp of CTA t (t < T)
+// scales token t instead.
+constexpr int kRStride = 520;  // bf16 per staged row
+
+__device__ __forceinline__ void phase_router(FusedSmem &S, const FusedParams &p, int cwarp,
+                                             int lane) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {  // claimed after barrier 1
+    *p.unit_claims = 0u;
+    *p.down_claims = 0u;
+  }
+  const int G = static_cast<int>(gridDim.x);
+  const bool scales = static_cast<int>(blockIdx.x) < p.T;
+  if (scales && cwarp == kFConsumerWarps - 1) {
+    for (int t = blockIdx.x; t < p.T; t += G) scale_token(p, t, lane);
+    return;
+  }
+  const int n_rw = kFConsumerWarps - (scales ? 1 : 0);  // router warps of this CTA
+  const int rows_total = kE + (p.Is > 0 ? 1 : 0);
+  const int n_rg = G / p.KS;  // row groups
+  const int rpg = min(16, (rows_total + n_rg - 1) / n_rg);
+  const int rg = static_cast<int>(blockIdx.x) / p.KS, ks = static_cast<int>(blockIdx.x) % p.KS;
+  const int r0 = rg * rpg;
+  const int nr = rg < n_rg ? max(0, min(rpg, rows_total - r0)) : 0;
+  if (nr == 0) return;  // (the size check makes the groups cover every row)
+  // staged slices: the T token rows from ring stage 1 (up to 65 KB), then the
+  // 16 weight rows (rows nr.. zero)
+  moe_bf16 *xs = reinterpret_cast<moe_bf16 *>(S.ring[1]);
+  moe_bf16 *ws = xs + p.T * kRStride;
+  const int n_x = p.T * 64;  // uint4 per token slice: 64
+  for (int i = cwarp * 32 + lane; i < n_x + 16 * 64; i += n_rw * 32) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    moe_bf16 *dst;
+    if (i < n_x) {
+      v = ld_nc(p.x + static_cast<size_t>(i >> 6) * p.H + ks * 512 + (i & 63) * 8);
+      dst = xs + (i >> 6) * kRStride + (i & 63) * 8;
+    } else {
+      const int ri = (i - n_x) >> 6;
+      if (ri < nr) {
+        const int r = r0 + ri;
+        const moe_bf16 *wrow = r < kE ? p.w_router + static_cast<size_t>(r) * p.H : p.w_gate;
+        v = ld_nc(wrow + ks * 512 + (i & 63) * 8);
+      }
+      dst = ws + ri * kRStride + (i & 63) * 8;
+    }
+    *reinterpret_cast<uint4 *>(dst) = v;
+  }
+  ptx::named_barrier(5, n_rw * 32);
+  const int g = lane >> 2, c = lane & 3;
+  const int n_nt = (p.T + 7) / 8;
+  float *part = reinterpret_cast<float *>(ws + 16 * kRStride);  // [n_nt * 4][4][32]
+  for (int task = cwarp; task < 4 * n_nt; task += n_rw) {
+    const int nt = task >> 2, kq = task & 3;
+    const int t = nt * 8 + g;  // this lane's B column (token)
+    const uint32_t *xr = reinterpret_cast<const uint32_t *>(xs + min(t, p.T - 1) * kRStride);
+    const uint32_t *wlo = reinterpret_cast<const uint32_t *>(ws + g * kRStride);
+    const uint32_t *whi = reinterpret_cast<const uint32_t *>(ws + (g + 8) * kRStride);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k2 = 64 * kq; k2 < 64 * kq + 64; k2 += 8) {  // k2: bf16 pairs, 8 per k16 step
+      const uint32_t b0 = t < p.T ? xr[k2 + c] : 0u, b1 = t < p.T ? xr[k2 + 4 + c] : 0u;
+      mma16816(d, wlo[k2 + c], whi[k2 + c], wlo[k2 + 4 + c], whi[k2 + 4 + c], b0, b1);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) part[(task * 4 + i) * 32 + lane] = d[i];
+  }
+  ptx::named_barrier(5, n_rw * 32);
+  // d0, d1 of lane l: row g, tokens 8nt + 2c, +1; d2, d3: row g + 8
+  for (int idx = cwarp * 32 + lane; idx < n_nt * 128; idx += n_rw * 32) {
+    const int nt = idx >> 7, i = (idx >> 5) & 3, ln = idx & 31;
+    const float *q = part + (nt * 16 + i) * 32 + ln;  // quarter kq at q[kq * 128]
+    const float v = ((q[0] + q[128]) + q[256]) + q[384];
+    const int row = (ln >> 2) + (i >> 1) * 8, tok = nt * 8 + 2 * (ln & 3) + (i & 1);
+    if (row < nr && tok < p.T)
+      p.rpart[(static_cast<size_t>(tok) * p.KS + ks) * kRP + r0 + row] = v;
+  }
+  // the staged slices were written and read by the generic proxy; the ring
+  // is next written by bulk copies (async proxy)
+  ptx::fence_proxy_async_smem();
 }
 
 // Token t's selection: fold the K-slice partials (fixed order), select the
@@ -570,9 +650,12 @@ __device__ __forceinline__ void mma_slice_f16(const uint8_t *rows, int stride, i
 // token tile, bf16 operands.  The B fragments of up to four slices (256 of
 // K) are fetched together before their MMAs, so each batch pays one memory
 // latency; each slice's partial sums are promoted with its group's scales
-// (lo: rows 0..7, hi: rows 8..15).  brow = this lane's token row or NULL.
+// (lo: rows 0..7, hi: rows 8..15).  brow = this lane's token row or NULL:
+// rows of h, written before the grid barrier that precedes the down phase
+// and read by no SM earlier in the launch, so L1 holds no stale copy and
+// caching them there serves the other warps and items of the same expert.
 __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int kb, int kn,
-                                          const moe_bf16 *brow, int g, int c, bool cg,
+                                          const moe_bf16 *brow, int g, int c,
                                           const moe_bf16 *s_lo, const moe_bf16 *s_hi,
                                           float (&acc)[4]) {
   for (int kk = kb; kk < kb + kn; kk += 256) {
@@ -582,8 +665,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
     for (int sl = 0; sl < 4; ++sl) {
       if (brow && sl < ns) {
         const moe_bf16 *src = brow + kk + 64 * sl + 16 * c;
-        const uint4 x0 = cg ? ld_cg16(src) : ld_nc(src);
-        const uint4 x1 = cg ? ld_cg16(src + 8) : ld_nc(src + 8);
+        const uint4 x0 = ld_ca16(src), x1 = ld_ca16(src + 8);
         xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
         xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
       } else {
@@ -726,61 +808,88 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
   return true;
 }
 
-// Phase D consumer: down stage k (units k*U ..), by quad q; warp wq takes
-// units wq, wq + 4, ... of the stage, each over its full K (= I or Is).
-__device__ __forceinline__ void consume_down(FusedSmem &S, const FusedParams &p, const Work &wk,
-                                             int k, int wq, int lane, uint64_t budget) {
-  const int j = S.down_base + k;
-  const int s = j % kFStages;
-  fwait(&S.full[s], (j / kFStages) & 1, S, budget);
-  const int u0 = k * wk.units_per_stage;
-  const int nu = min(wk.units_per_stage, wk.n_down_units - u0);
+// One 16-row down unit of expert e over its full K (rows: the unit's int8
+// rows at stride K, sbase: their scales, row by row) against every token of
+// the expert; y goes to shared memory (ys != NULL: row-owner mode, rows
+// 0..15 of this CTA) or to global row n0 of each slot.
+__device__ __forceinline__ void down_unit_gemm(const FusedSmem &S, const FusedParams &p, int e,
+                                               const uint8_t *rows, const moe_bf16 *sbase,
+                                               float (*ys)[kFRowOwnerT * (kK + 1)], int n0,
+                                               int lane) {
+  const bool sh = e == kE;
+  const int Ii = sh ? p.Is : p.I;
+  const int ng = Ii / kG;
+  const int n_tok = sh ? p.T : S.counts[e];
+  const int p0 = sh ? p.T * kK : S.offsets[e];  // first y slot of the expert
   const int g = lane >> 2, c = lane & 3;
-  for (int u = wq; u < nu; u += 4) {
-    const int e = down_unit(S, p, u0 + u);
-    const bool sh = e == kE;
-    const int Ii = sh ? p.Is : p.I;
-    const int ng = Ii / kG;
-    const int n_tok = sh ? p.T : S.counts[e];
-    const int p0 = sh ? 0 : S.offsets[e];
-    const moe_bf16 *sbase = reinterpret_cast<const moe_bf16 *>(S.ring_s[s] + u * wk.scale_stride);
-    const moe_bf16 *s_lo = sbase + g * ng;
-    const moe_bf16 *s_hi = sbase + (g + 8) * ng;
-    const uint8_t *rows = S.ring[s] + u * wk.unit_stride;
-    for (int tb = 0; tb < n_tok; tb += kFPass) {
-      const int ntiles = min(2, (n_tok - tb + 7) / 8);
-      const moe_bf16 *brow[2];
+  const moe_bf16 *s_lo = sbase + g * ng;
+  const moe_bf16 *s_hi = sbase + (g + 8) * ng;
+  for (int tb = 0; tb < n_tok; tb += kFPass) {
+    const int ntiles = min(2, (n_tok - tb + 7) / 8);
+    const moe_bf16 *brow[2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int idx = tb + 8 * nt + g;
-        brow[nt] = nullptr;
-        if (idx < n_tok)
-          brow[nt] = sh ? p.h_shared + static_cast<size_t>(idx) * p.Is
-                        : p.h_routed + static_cast<size_t>(p0 + idx) * p.I;
-      }
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      for (int nt = 0; nt < ntiles; ++nt)
-        unit_gemm(rows, Ii, 0, Ii, brow[nt], g, c, true, s_lo, s_hi, acc[nt]);
+    for (int nt = 0; nt < 2; ++nt) {
+      const int idx = tb + 8 * nt + g;
+      brow[nt] = nullptr;
+      if (idx < n_tok)
+        brow[nt] = sh ? p.h_shared + static_cast<size_t>(idx) * p.Is
+                      : p.h_routed + static_cast<size_t>(p0 + idx) * p.I;
+    }
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int nt = 0; nt < ntiles; ++nt)
+      unit_gemm(rows, Ii, 0, Ii, brow[nt], g, c, s_lo, s_hi, acc[nt]);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int col = 0; col < 2; ++col) {
-          const int idx = tb + 8 * nt + 2 * c + col;
-          if (nt < ntiles && idx < n_tok) {
-            const int slot = sh ? p.T * kK + idx : p0 + idx;
-            S.u.ys[g][slot] = acc[nt][col];
-            S.u.ys[g + 8][slot] = acc[nt][2 + col];
+      for (int col = 0; col < 2; ++col) {
+        const int idx = tb + 8 * nt + 2 * c + col;
+        if (nt < ntiles && idx < n_tok) {
+          if (ys) {
+            ys[g][p0 + idx] = acc[nt][col];
+            ys[g + 8][p0 + idx] = acc[nt][2 + col];
+          } else {
+            float *yr = p.y + static_cast<size_t>(p0 + idx) * p.H + n0;
+            yr[g] = acc[nt][col];
+            yr[g + 8] = acc[nt][2 + col];
           }
         }
-    }
+      }
+  }
+}
+
+// Phase D consumer: the down stage in ring stage j, by one quad: warp wq
+// takes the stage's 16-row units wq, wq + 4, ....  Returns false at the
+// stage that marks the end of the down stages (after releasing it).
+__device__ __forceinline__ bool consume_down(FusedSmem &S, const FusedParams &p, const Work &wk,
+                                             int j, int wq, int lane, uint64_t budget) {
+  const int s = j % kFStages;
+  fwait(&S.full[s], (j / kFStages) & 1, S, budget);
+  if (aborted(S)) return false;
+  const int2 it = S.stage_unit[s];
+  if (it.x > kE) {  // row-owner stage k = it.y
+    const int a0 = it.y * wk.units_per_stage;
+    const int nu = min(wk.units_per_stage, wk.n_exp - a0);
+    for (int u = wq; u < nu; u += 4)
+      down_unit_gemm(S, p, down_expert(S, p, a0 + u), S.ring[s] + u * wk.unit_stride,
+                     reinterpret_cast<const moe_bf16 *>(S.ring_s[s] + u * wk.scale_stride),
+                     S.u.ys, 0, lane);
+  } else if (it.x >= 0) {  // item (e, n0)
+    const int e = it.x, n0 = it.y;
+    const int Ii = e == kE ? p.Is : p.I;
+    const int nu = min(wk.down_rows, p.H - n0) / 16;
+    for (int u = wq; u < nu; u += 4)
+      down_unit_gemm(S, p, e, S.ring[s] + static_cast<size_t>(16 * u) * Ii,
+                     reinterpret_cast<const moe_bf16 *>(S.ring_s[s]) + 16 * u * (Ii / kG),
+                     nullptr, n0 + 16 * u, lane);
   }
   __syncwarp();
   if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+  return it.x >= 0;
 }
 
-// A7 for this CTA's 16 output rows: slots in rank order, then the shared
-// expert, fp32, one bf16 rounding.
-__device__ __forceinline__ void phase_combine(FusedSmem &S, const FusedParams &p, const Work &wk) {
+// Row-owner mode: this CTA's 16 output rows from the y in shared memory:
+// slots in rank order, then the shared expert, fp32, one bf16 rounding.
+__device__ __forceinline__ void combine_rows(FusedSmem &S, const FusedParams &p, const Work &wk) {
   if (wk.n0 < 0) return;
   for (int i = threadIdx.x; i < 16 * p.T; i += kFConsumers) {
     const int r = i & 15, t = i >> 4;
@@ -793,6 +902,38 @@ __device__ __forceinline__ void phase_combine(FusedSmem &S, const FusedParams &p
     }
     if (p.Is > 0 && S.sg[t] != 0.0f) acc = fmaf(S.sg[t], S.u.ys[r][p.T * kK + t], acc);
     p.out[static_cast<size_t>(t) * p.H + wk.n0 + r] = f32_to_bf16(acc);
+  }
+}
+
+// Item mode: out[t][n] = sum over token t's slots in rank order of w * y, then
+// the shared expert's sg * y, in fp32 with one bf16 rounding; two adjacent
+// n per thread, spread over the consumer threads of the whole grid.
+__device__ __forceinline__ void phase_combine(FusedSmem &S, const FusedParams &p) {
+  const int half = p.H / 2;
+  const int n_all = p.T * half;
+  for (int i = blockIdx.x * kFConsumers + threadIdx.x; i < n_all;
+       i += gridDim.x * kFConsumers) {
+    const int t = i / half, n = 2 * (i - t * half);
+    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kK; ++j) {
+      const int slot = S.slot_of[t][j];
+      const float w = S.wts[t][j];
+      if (slot >= 0 && w != 0.0f) {
+        const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.y + static_cast<size_t>(slot) * p.H + n));
+        a0 = fmaf(w, v.x, a0);
+        a1 = fmaf(w, v.y, a1);
+      }
+    }
+    if (p.Is > 0 && S.sg[t] != 0.0f) {
+      const float2 v = __ldcg(reinterpret_cast<const float2 *>(
+          p.y + static_cast<size_t>(p.T * kK + t) * p.H + n));
+      a0 = fmaf(S.sg[t], v.x, a0);
+      a1 = fmaf(S.sg[t], v.y, a1);
+    }
+    const uint32_t o = static_cast<uint32_t>(f32_to_bf16(a0)) |
+                       (static_cast<uint32_t>(f32_to_bf16(a1)) << 16);
+    *reinterpret_cast<uint32_t *>(p.out + static_cast<size_t>(t) * p.H + n) = o;
   }
 }
 
@@ -837,19 +978,21 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     if (lane == 0) fwait(&S.routed, 0, S, budget);
     __syncwarp();
     const Work wk = make_work(S, p);
-    // Routed gate|up units are claimed from a grid-wide counter, kFClaim
-    // consecutive units (rows of one expert) at a time and one claim ahead,
-    // so that CTAs that run faster take more of them while the counter's
-    // round trip overlaps the issue of the units already claimed.
+    // Routed gate|up units are claimed from a grid-wide counter, one claim
+    // ahead, so that CTAs that run faster take more of them.  When there are
+    // many, a claim takes kFClaim consecutive units (rows of one expert), so
+    // that the counter's round trip overlaps the issue of the units already
+    // claimed; when there are few, single units keep the split even.
     const unsigned n_routed = static_cast<unsigned>(S.active[0] * wk.nIb);
+    const unsigned gu_claim = n_routed >= 24u * gridDim.x ? static_cast<unsigned>(kFClaim) : 1u;
     unsigned claim = 0;
-    if (lane == 0) claim = atomicAdd(p.unit_claims, static_cast<unsigned>(kFClaim));
+    if (lane == 0) claim = atomicAdd(p.unit_claims, gu_claim);
     claim = __shfl_sync(0xFFFFFFFFu, claim, 0);
     int j = early ? 1 : 0;  // ring index of the next stage
     while (claim < n_routed && !aborted(S)) {
       unsigned nx = 0;
-      if (lane == 0) nx = atomicAdd(p.unit_claims, static_cast<unsigned>(kFClaim));
-      const unsigned end = min(claim + static_cast<unsigned>(kFClaim), n_routed);
+      if (lane == 0) nx = atomicAdd(p.unit_claims, gu_claim);
+      const unsigned end = min(claim + gu_claim, n_routed);
       for (unsigned b = claim; b < end && !aborted(S); ++b) {
         const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
         if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
@@ -857,20 +1000,52 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       }
       claim = __shfl_sync(0xFFFFFFFFu, nx, 0);
     }
-    // one end marker per quad, then the down stages
-    for (int k = 0; k < kFQuads && !aborted(S); ++k, ++j) {
-      if (lane == 0) {
-        fwait(&S.empty[j % kFStages], ((j / kFStages) & 1) ^ 1, S, budget);
-        if (!aborted(S)) {
-          S.down_base = j - k + kFQuads;
-          S.stage_unit[j % kFStages] = make_int2(-1, 0);
-          ptx::mbar_arrive(&S.full[j % kFStages]);
+    // one end marker per quad (each quad takes every kFQuads-th stage, so
+    // kFQuads consecutive markers reach every quad once)
+    auto end_markers = [&](bool gateup) {
+      for (int k = 0; k < kFQuads && !aborted(S); ++k, ++j) {
+        if (lane == 0) {
+          fwait(&S.empty[j % kFStages], ((j / kFStages) & 1) ^ 1, S, budget);
+          if (!aborted(S)) {
+            if (gateup) S.down_base = j - k + kFQuads;
+            S.stage_unit[j % kFStages] = make_int2(-1, 0);
+            ptx::mbar_arrive(&S.full[j % kFStages]);
+          }
         }
+        __syncwarp();
       }
-      __syncwarp();
+    };
+    end_markers(true);
+    if (wk.row_owner) {
+      for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k, ++j)
+        if (produce_down(S, p, wk, j, make_int2(kE + 1, k), pol, budget, lane)) issued_at(j);
     }
-    for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k)
-      if (produce_down(S, p, wk, k, pol, budget, lane)) issued_at(S.down_base + k);
+    // Down items, claimed from their own counter the same way (their costs
+    // differ with the expert's token count, so a static split would not
+    // balance them); their weights need no h, so they stream while the
+    // gate|up units are still computing.  A CTA claims at most cap items:
+    // before the grid barrier no down stage is consumed, and without a cap
+    // the CTAs that reach this point first would take several items per quad
+    // when there are few (decode).
+    const unsigned n_down = wk.row_owner ? 0u : static_cast<unsigned>(wk.n_exp * wk.nrb);
+    const unsigned G = gridDim.x;
+    const unsigned per_claim = n_down >= 8u * G ? 2u : 1u;
+    const unsigned cap = max(static_cast<unsigned>(kFQuads), (4u * n_down / 3u + G - 1u) / G);
+    unsigned taken = 0;
+    claim = n_down;
+    if (lane == 0 && n_down > 0) claim = atomicAdd(p.down_claims, per_claim);
+    taken += per_claim;
+    claim = __shfl_sync(0xFFFFFFFFu, claim, 0);
+    while (claim < n_down && !aborted(S)) {
+      unsigned nx = n_down;
+      if (lane == 0 && taken < cap) nx = atomicAdd(p.down_claims, per_claim);
+      taken += per_claim;
+      const unsigned end = min(claim + per_claim, n_down);
+      for (unsigned b = claim; b < end && !aborted(S); ++b, ++j)
+        if (produce_down(S, p, wk, j, down_item(S, p, wk, b), pol, budget, lane)) issued_at(j);
+      claim = __shfl_sync(0xFFFFFFFFu, nx, 0);
+    }
+    end_markers(false);
     // after an abort, let the copies already in flight land before exiting
     if (aborted(S) && lane == 0) {
       int never = 0;
@@ -882,7 +1057,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
   } else {
     // ----------------------------------------------------------- consumers
     const int q = warp >> 2, wq = warp & 3;
-    phase_router(p, warp, lane);
+    phase_router(S, p, warp, lane);
     grid_sync(p.grid_bar, S, budget);
     phase_select_lists(S, p, warp, lane, budget);
     if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
@@ -891,10 +1066,15 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     for (int j = q; consume_gu(S, p, j, q, wq, lane, budget, npass); j += kFQuads) {
     }
     grid_sync(p.grid_bar, S, budget);
-    for (int k = q; k < wk.n_down_stages; k += kFQuads)
-      consume_down(S, p, wk, k, wq, lane, budget);
-    ptx::named_barrier(1, kFConsumers);
-    phase_combine(S, p, wk);
+    for (int j = S.down_base + q; consume_down(S, p, wk, j, wq, lane, budget); j += kFQuads) {
+    }
+    if (wk.row_owner) {
+      ptx::named_barrier(1, kFConsumers);
+      combine_rows(S, p, wk);
+    } else {
+      grid_sync(p.grid_bar, S, budget);
+      phase_combine(S, p);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0 && aborted(S)) set_status(p.status, MOE_DEV_TIMEOUT);
@@ -941,9 +1121,9 @@ bool fused_decode_supported(int T, int H, int I, int Is) {
       sms[dev] = device_sms();
     }
   }
-  // the SMs must cover the H / 16 output-row blocks and the Is / 8 shared
-  // gate|up units (one per CTA)
-  return sms[dev] > 0 && sms[dev] * 16 >= H && sms[dev] * 8 >= Is;
+  // the SMs must cover the Is / 8 shared gate|up units (one per CTA) and the
+  // router's 257 rows in groups of at most 16 per K-slice
+  return sms[dev] > 0 && sms[dev] * 8 >= Is && (sms[dev] / (H / 512)) * 16 >= kE + 1;
 }
 
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
@@ -953,7 +1133,7 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, unsigned *unit_claims,
-                                cudaStream_t s) {
+                                unsigned *down_claims, float *y, cudaStream_t s) {
   FusedParams p{};
   p.x = x; p.x16 = x16; p.xscale = xscale;
   p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 512;
@@ -962,6 +1142,8 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
   p.ws13_q = w.ws13_q; p.ws13_s = w.ws13_s; p.ws2_q = w.ws2_q; p.ws2_s = w.ws2_s;
   p.rpart = rpart; p.sel_ids = sel_ids; p.sel_w = sel_w; p.sel_sg = sel_sg;
   p.unit_claims = unit_claims;
+  p.down_claims = down_claims;
+  p.y = y;
   p.h_routed = h_routed; p.h_shared = h_shared; p.out = out;
   p.ids_out = ids_out; p.weights_out = weights_out; p.logits_out = logits_out;
   p.gate_logit_out = gate_logit_out; p.status = status; p.grid_bar = grid_bar;

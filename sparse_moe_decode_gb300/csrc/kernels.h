@@ -63,16 +63,17 @@ constexpr int kFusedMaxH = 2048;  // hidden (multiple of 512)
 constexpr int kFusedMaxI = 2048;  // expert / shared intermediate
 
 // Whether the fused kernel runs these sizes on the current device (one CTA
-// per SM must fit, and the SMs must cover H / 16 output-row blocks).
+// per SM must fit, and the SMs must cover the Is / 8 shared gate|up units
+// and the router rows in groups of 16 per 512-wide K-slice).
 bool fused_decode_supported(int T, int H, int I, int Is);
 size_t fused_smem_bytes();
 
 // A1..A7 in one cooperative launch.  x16 [T][H] fp16 and xscale [T] (the
 // tokens' scaled fp16 copies), rpart [T][H/512][260] fp32, sel_ids [T][K],
 // sel_w [T][K], sel_sg [T], h_routed [T*K][I], h_shared [T][Is],
-// unit_claims (one counter) scratch; grid_bar is a 32-bit counter whose
-// low 31 bits must be zero before the first launch (each grid barrier leaves
-// them unchanged).
+// y [T*K + T][H] fp32, unit_claims and down_claims (one counter each)
+// scratch; grid_bar is a 32-bit counter whose low 31 bits must be zero before the first launch
+// (each grid barrier leaves them unchanged).
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 const moe_weights &w, uint16_t *x16, float *xscale,
                                 float *rpart, int32_t *sel_ids, float *sel_w,
@@ -80,7 +81,7 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, unsigned *unit_claims,
-                                cudaStream_t s);
+                                unsigned *down_claims, float *y, cudaStream_t s);
 
 // ---- prefill-size T: tcgen05 GEMMs (tc_gemm.cu: router; tc_expert.cu: experts)
 

@@ -82,7 +82,7 @@ def test_block_pr1(env):
 def test_block_pr1_ragged_T(env):
     moe, dev = env
     dims, w = workload("pr1")
-    for T in (1, 3, 9, 33, 65):
+    for T in (1, 3, 9, 12, 13, 33, 64, 65):
         x, _ = W.make_x(dims, T, 7 + T)
         check_block(moe, dev, "pr1", x)
 
@@ -101,7 +101,7 @@ def test_block_verify_T32_skewed(env):
     assert len(np.unique(g["ids"])) > 100  # many distinct experts are active
 
 
-@pytest.mark.parametrize("T", [2, 19, 20, 46, 47, 768, 4097])
+@pytest.mark.parametrize("T", [2, 12, 13, 19, 20, 46, 47, 64, 768, 4097])
 def test_block_decode_dims_T_sweep(env, T):
     moe, dev = env
     dims, _ = workload("decode")
