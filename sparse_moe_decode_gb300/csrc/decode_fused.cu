@@ -62,7 +62,8 @@ constexpr int kFQuads = 3;  // 13 warps: at most 4 per SM sub-partition, 128 reg
 constexpr int kFConsumerWarps = 4 * kFQuads;
 constexpr int kFConsumers = kFConsumerWarps * 32;
 constexpr int kFThreads = kFConsumers + 32;  // + one producer warp
-constexpr int kFStages = 5;
+constexpr int kFStages = 6;
+constexpr int kFRedBufs = 1;  // buffers of each quad's reduction exchange
 constexpr int kFStageBytes = 16 * kFusedMaxH;  // one gate|up unit, or packed down units
 constexpr int kFScaleBytes = 512;              // the group scales of a stage's rows
 constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
@@ -106,7 +107,7 @@ struct FusedSmem {
   uint8_t ring[kFStages][kFStageBytes];
   uint8_t ring_s[kFStages][kFScaleBytes];  // bf16 scales of each stage's rows
   union {
-    float red[kFQuads][2][4][2][32][4];        // gate|up: quad reduction, 2 buffers
+    float red[kFQuads][kFRedBufs][4][2][32][4];  // gate|up: quad reduction exchange
     float ys[16][kFRowOwnerT * (kK + 1)];      // row-owner down: y of this CTA's 16 rows
   } u;
   int32_t ids[kFusedMaxT][kK];
@@ -123,7 +124,7 @@ struct FusedSmem {
   uint64_t full[kFStages], empty[kFStages], routed;
   int2 stage_unit[kFStages];  // (expert, first row pair | first output row); x < 0: end
   int down_base;              // ring index of the first down stage
-  uint64_t red_full[kFQuads][2], red_empty[kFQuads][2];
+  uint64_t red_full[kFQuads][kFRedBufs], red_empty[kFQuads][kFRedBufs];
   int abort;
 };
 
@@ -768,10 +769,12 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
       if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
     }
     // Hand the four K quarters to this pass's reducing warp (it rotates over
-    // the quad) through a double-buffered exchange; only the reducer waits.
+    // the quad) through an exchange of kFRedBufs buffers; only the reducer
+    // waits.
     const uint32_t u = npass++;
-    const int b = u & 1;
-    fwait(&S.red_empty[q][b], ((u >> 1) & 1) ^ 1, S, budget);
+    const int b = u % kFRedBufs;
+    const uint32_t rpar = (u / kFRedBufs) & 1;
+    fwait(&S.red_empty[q][b], rpar ^ 1, S, budget);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -779,7 +782,7 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&S.red_full[q][b]);
     if (wq == static_cast<int>(u & 3)) {
-      fwait(&S.red_full[q][b], (u >> 1) & 1, S, budget);
+      fwait(&S.red_full[q][b], rpar, S, budget);
       for (int nt = 0; nt < ntiles; ++nt) {
         float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -949,7 +952,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     }
     ptx::mbar_init(&S.routed, 1);
     for (int q = 0; q < kFQuads; ++q)
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < kFRedBufs; ++b) {
         ptx::mbar_init(&S.red_full[q][b], 4);   // the quad's four warps
         ptx::mbar_init(&S.red_empty[q][b], 1);  // the pass's reducing warp
       }
