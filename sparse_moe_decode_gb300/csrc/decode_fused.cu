@@ -1,6 +1,7 @@
 // decode_fused.cu -- the whole block (A1..A7) for decode-size T in one
-// persistent cooperative kernel: one CTA per SM, phases separated by three
-// bounded grid barriers (four when T > 12).
+// persistent cooperative kernel: one CTA per SM, phases separated by bounded
+// grid barriers (two, one more when T > 12 for the shared selection, one
+// more when T > 8 for the item-mode combine).
 //
 //   R  router: 257 rows x (H/512) K-slices of 512, one warp each, fp32
 //      partials (the pages' S1 split of the router into K-slices);
@@ -58,10 +59,19 @@
 namespace moe {
 namespace {
 
-constexpr int kFQuads = 3;  // 13 warps: at most 4 per SM sub-partition, 128 registers
+constexpr int kFQuads = 3;
 constexpr int kFConsumerWarps = 4 * kFQuads;
 constexpr int kFConsumers = kFConsumerWarps * 32;
-constexpr int kFThreads = kFConsumers + 32;  // + one producer warp
+// 16 warps, 128 registers: warp 0 is the producer, alone on its SM
+// sub-partition (warps 4, 8 and 12 idle), so that the consumers' issue does
+// not delay its copies; warps w with w mod 4 != 0 are consumer warps.
+constexpr int kFThreads = 512;
+
+// consumer warp index (0 .. 11) of warp w (w mod 4 != 0)
+__device__ __forceinline__ int consumer_warp(int w) { return w - (w >> 2) - 1; }
+__device__ __forceinline__ int consumer_tid() {
+  return consumer_warp(threadIdx.x >> 5) * 32 + (threadIdx.x & 31);
+}
 constexpr int kFStages = 6;
 constexpr int kFRedBufs = 1;  // buffers of each quad's reduction exchange
 constexpr int kFStageBytes = 16 * kFusedMaxH;  // one gate|up unit, or packed down units
@@ -190,7 +200,7 @@ __device__ __forceinline__ void fwait(uint64_t *bar, uint32_t parity, FusedSmem 
 // counter and leaves its low bits unchanged.  Bounded by the wait budget.
 __device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t budget) {
   ptx::named_barrier(1, kFConsumers);
-  if (threadIdx.x == 0) {
+  if (consumer_tid() == 0) {
     __threadfence();
     const unsigned inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1) : 1u;
     const unsigned old = atomicAdd(bar, inc);
@@ -399,7 +409,7 @@ constexpr int kRStride = 520;  // bf16 per staged row
 
 __device__ __forceinline__ void phase_router(FusedSmem &S, const FusedParams &p, int cwarp,
                                              int lane) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) {  // claimed after barrier 1
+  if (blockIdx.x == 0 && consumer_tid() == 0) {  // claimed after barrier 1
     *p.unit_claims = 0u;
     *p.down_claims = 0u;
   }
@@ -543,7 +553,7 @@ __device__ __forceinline__ void select_token(FusedSmem &S, const FusedParams &p,
 // token -> expert lists in shared memory.
 __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedParams &p, int cwarp,
                                                    int lane, uint64_t budget) {
-  const int tid = threadIdx.x;  // consumer threads
+  const int tid = consumer_tid();
   if (p.T <= kFLocalSelT) {
     if (cwarp < p.T) select_token(S, p, cwarp, lane, true);
   } else {
@@ -894,7 +904,7 @@ __device__ __forceinline__ bool consume_down(FusedSmem &S, const FusedParams &p,
 // slots in rank order, then the shared expert, fp32, one bf16 rounding.
 __device__ __forceinline__ void combine_rows(FusedSmem &S, const FusedParams &p, const Work &wk) {
   if (wk.n0 < 0) return;
-  for (int i = threadIdx.x; i < 16 * p.T; i += kFConsumers) {
+  for (int i = consumer_tid(); i < 16 * p.T; i += kFConsumers) {
     const int r = i & 15, t = i >> 4;
     float acc = 0.0f;
 #pragma unroll
@@ -914,7 +924,7 @@ __device__ __forceinline__ void combine_rows(FusedSmem &S, const FusedParams &p,
 __device__ __forceinline__ void phase_combine(FusedSmem &S, const FusedParams &p) {
   const int half = p.H / 2;
   const int n_all = p.T * half;
-  for (int i = blockIdx.x * kFConsumers + threadIdx.x; i < n_all;
+  for (int i = blockIdx.x * kFConsumers + consumer_tid(); i < n_all;
        i += gridDim.x * kFConsumers) {
     const int t = i / half, n = 2 * (i - t * half);
     float a0 = 0.0f, a1 = 0.0f;
@@ -961,7 +971,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
   }
   __syncthreads();
 
-  if (warp == kFConsumerWarps) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = ptx::policy_evict_first();
     // the shared expert's unit needs no routing: fetch it at once
@@ -1057,13 +1067,14 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
         if (last_use[i] >= 0)
           ptx::mbar_wait(&S.full[i], (last_use[i] / kFStages) & 1, &never, ptx::kDrainBudgetNs);
     }
-  } else {
+  } else if ((warp & 3) != 0) {
     // ----------------------------------------------------------- consumers
-    const int q = warp >> 2, wq = warp & 3;
-    phase_router(S, p, warp, lane);
+    const int cw = consumer_warp(warp);
+    const int q = cw >> 2, wq = cw & 3;
+    phase_router(S, p, cw, lane);
     grid_sync(p.grid_bar, S, budget);
-    phase_select_lists(S, p, warp, lane, budget);
-    if (threadIdx.x == 0) ptx::mbar_arrive(&S.routed);
+    phase_select_lists(S, p, cw, lane, budget);
+    if (consumer_tid() == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
     uint32_t npass = 0;
     for (int j = q; consume_gu(S, p, j, q, wq, lane, budget, npass); j += kFQuads) {
