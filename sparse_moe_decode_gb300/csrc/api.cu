@@ -56,7 +56,7 @@ size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 struct Layout {
   size_t status, logits, gate_logit, ids, weights, sgate;
   size_t counts, offsets, active, perm, slot_of;
-  size_t h_routed, h_shared, y, rpart, x16, xscale, hscale, xstage, ostage;
+  size_t h_routed, h_shared, h16, y, rpart, x16, xscale, hscale, xstage, ostage;
   size_t xs, acc, items, counters, total;
 };
 
@@ -108,7 +108,10 @@ Layout layout(const moe_dims *d, int T) {
   L.h_shared = take(2 * t * (Is ? Is : 1));
   const Route r = route_of(d, T);
   if (r == kRouteGemv || r == kRouteFused) L.y = take(4 * t * (kK + 1) * H);
-  if (r == kRouteFused) L.rpart = take(4 * t * 260 * (H / 512));
+  if (r == kRouteFused) {
+    L.rpart = take(4 * t * 260 * (H / 512));
+    L.h16 = take(2 * t * (kK * I + Is));
+  }
   if (r == kRouteFused || r == kRouteTc) {
     L.x16 = take(2 * t * H);
     L.xscale = take(4 * t);
@@ -202,7 +205,8 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
                                 at<int32_t>(ws, L.ids), at<float>(ws, L.weights),
                                 at<float>(ws, L.sgate), hr, hs, out, ids_out, weights_out,
                                 logits_out, gate_logit_out, status, grid_bar, grid_bar + 1,
-                                grid_bar + 2, at<float>(ws, L.y), s));
+                                grid_bar + 2, at<float>(ws, L.y), at<uint16_t>(ws, L.h16),
+                                grid_bar + 3, s));
     MOE_TRY(rec());
     return MOE_OK;
   }

@@ -102,6 +102,9 @@ struct FusedParams {
   float *sel_sg;       // [T]
   moe_bf16 *h_routed;  // [T*K][I], rows in list order
   moe_bf16 *h_shared;  // [T][Is]
+  uint16_t *h16_routed;  // [T*K][I] fp16 copies of h (exact while every |h| < 2^15)
+  uint16_t *h16_shared;  // [T][Is]
+  unsigned *h_wide;      // nonzero: some |h| >= 2^15 (or not finite); zeroed in phase R
   float *y;            // [T*K + T][H] down outputs: routed slots in list order, then shared
   moe_bf16 *out;       // [T][H]
   int32_t *ids_out;
@@ -409,9 +412,10 @@ constexpr int kRStride = 520;  // bf16 per staged row
 
 __device__ __forceinline__ void phase_router(FusedSmem &S, const FusedParams &p, int cwarp,
                                              int lane) {
-  if (blockIdx.x == 0 && consumer_tid() == 0) {  // claimed after barrier 1
+  if (blockIdx.x == 0 && consumer_tid() == 0) {  // claimed / set after barrier 1
     *p.unit_claims = 0u;
     *p.down_claims = 0u;
+    *p.h_wide = 0u;
   }
   const int G = static_cast<int>(gridDim.x);
   const bool scales = static_cast<int>(blockIdx.x) < p.T;
@@ -665,8 +669,9 @@ __device__ __forceinline__ void mma_slice_f16(const uint8_t *rows, int stride, i
 // rows of h, written before the grid barrier that precedes the down phase
 // and read by no SM earlier in the launch, so L1 holds no stale copy and
 // caching them there serves the other warps and items of the same expert.
+template <bool F16>
 __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int kb, int kn,
-                                          const moe_bf16 *brow, int g, int c,
+                                          const uint16_t *brow, int g, int c,
                                           const moe_bf16 *s_lo, const moe_bf16 *s_hi,
                                           float (&acc)[4]) {
   for (int kk = kb; kk < kb + kn; kk += 256) {
@@ -675,7 +680,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 #pragma unroll
     for (int sl = 0; sl < 4; ++sl) {
       if (brow && sl < ns) {
-        const moe_bf16 *src = brow + kk + 64 * sl + 16 * c;
+        const uint16_t *src = brow + kk + 64 * sl + 16 * c;
         const uint4 x0 = ld_ca16(src), x1 = ld_ca16(src + 8);
         xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
         xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
@@ -690,7 +695,8 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
       const int k0 = kk + 64 * sl;
       const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
       float part[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_slice(rows, stride, k0, g, c, xw[sl], part);
+      if (F16) mma_slice_f16(rows, stride, k0, g, c, xw[sl], part);
+      else mma_slice(rows, stride, k0, g, c, xw[sl], part);
       acc[0] = fmaf(slo, part[0], acc[0]);
       acc[1] = fmaf(slo, part[1], acc[1]);
       acc[2] = fmaf(shi, part[2], acc[2]);
@@ -792,6 +798,7 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&S.red_full[q][b]);
     if (wq == static_cast<int>(u & 3)) {
+      bool wide = false;
       fwait(&S.red_full[q][b], rpar, S, budget);
       for (int nt = 0; nt < ntiles; ++nt) {
         float r4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -805,11 +812,20 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
           if (idx < n_tok) {
             const float xsv = S.xs[sh ? idx : S.perm[p0 + idx] / kK];  // undo 2^-s
             const uint16_t hv = f32_to_bf16(silu_mul(r4[col] * xsv, r4[2 + col] * xsv));
-            if (sh) p.h_shared[static_cast<size_t>(idx) * p.Is + i0 + g] = hv;
-            else p.h_routed[static_cast<size_t>(p0 + idx) * p.I + i0 + g] = hv;
+            // h in fp16 as well: a bf16 value (8 significant bits) below
+            // 2^15 in magnitude is exact in fp16 down to 2^-17; smaller
+            // ones land on fp16's subnormal grid (error < 2^-25).
+            const float hf = __uint_as_float(static_cast<uint32_t>(hv) << 16);
+            const uint16_t h16 = __half_as_ushort(__float2half_rn(hf));
+            wide |= !(fabsf(hf) < 32768.0f);
+            const size_t o = sh ? static_cast<size_t>(idx) * p.Is + i0 + g
+                                : static_cast<size_t>(p0 + idx) * p.I + i0 + g;
+            (sh ? p.h_shared : p.h_routed)[o] = hv;
+            (sh ? p.h16_shared : p.h16_routed)[o] = h16;
           }
         }
       }
+      if (__any_sync(0xFFFFFFFFu, wide) && lane == 0) atomicOr(p.h_wide, 1u);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&S.red_empty[q][b]);
     }
@@ -828,7 +844,7 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
 __device__ __forceinline__ void down_unit_gemm(const FusedSmem &S, const FusedParams &p, int e,
                                                const uint8_t *rows, const moe_bf16 *sbase,
                                                float (*ys)[kFRowOwnerT * (kK + 1)], int n0,
-                                               int lane) {
+                                               bool f16, int lane) {
   const bool sh = e == kE;
   const int Ii = sh ? p.Is : p.I;
   const int ng = Ii / kG;
@@ -839,18 +855,22 @@ __device__ __forceinline__ void down_unit_gemm(const FusedSmem &S, const FusedPa
   const moe_bf16 *s_hi = sbase + (g + 8) * ng;
   for (int tb = 0; tb < n_tok; tb += kFPass) {
     const int ntiles = min(2, (n_tok - tb + 7) / 8);
-    const moe_bf16 *brow[2];
+    const uint16_t *brow[2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int idx = tb + 8 * nt + g;
       brow[nt] = nullptr;
-      if (idx < n_tok)
-        brow[nt] = sh ? p.h_shared + static_cast<size_t>(idx) * p.Is
-                      : p.h_routed + static_cast<size_t>(p0 + idx) * p.I;
+      if (idx < n_tok) {
+        const size_t o = sh ? static_cast<size_t>(idx) * p.Is : static_cast<size_t>(p0 + idx) * p.I;
+        brow[nt] = f16 ? (sh ? p.h16_shared : p.h16_routed) + o
+                       : reinterpret_cast<const uint16_t *>(sh ? p.h_shared : p.h_routed) + o;
+      }
     }
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    for (int nt = 0; nt < ntiles; ++nt)
-      unit_gemm(rows, Ii, 0, Ii, brow[nt], g, c, s_lo, s_hi, acc[nt]);
+    for (int nt = 0; nt < ntiles; ++nt) {
+      if (f16) unit_gemm<true>(rows, Ii, 0, Ii, brow[nt], g, c, s_lo, s_hi, acc[nt]);
+      else unit_gemm<false>(rows, Ii, 0, Ii, brow[nt], g, c, s_lo, s_hi, acc[nt]);
+    }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -874,7 +894,7 @@ __device__ __forceinline__ void down_unit_gemm(const FusedSmem &S, const FusedPa
 // takes the stage's 16-row units wq, wq + 4, ....  Returns false at the
 // stage that marks the end of the down stages (after releasing it).
 __device__ __forceinline__ bool consume_down(FusedSmem &S, const FusedParams &p, const Work &wk,
-                                             int j, int wq, int lane, uint64_t budget) {
+                                             int j, int wq, bool f16, int lane, uint64_t budget) {
   const int s = j % kFStages;
   fwait(&S.full[s], (j / kFStages) & 1, S, budget);
   if (aborted(S)) return false;
@@ -885,7 +905,7 @@ __device__ __forceinline__ bool consume_down(FusedSmem &S, const FusedParams &p,
     for (int u = wq; u < nu; u += 4)
       down_unit_gemm(S, p, down_expert(S, p, a0 + u), S.ring[s] + u * wk.unit_stride,
                      reinterpret_cast<const moe_bf16 *>(S.ring_s[s] + u * wk.scale_stride),
-                     S.u.ys, 0, lane);
+                     S.u.ys, 0, f16, lane);
   } else if (it.x >= 0) {  // item (e, n0)
     const int e = it.x, n0 = it.y;
     const int Ii = e == kE ? p.Is : p.I;
@@ -893,7 +913,7 @@ __device__ __forceinline__ bool consume_down(FusedSmem &S, const FusedParams &p,
     for (int u = wq; u < nu; u += 4)
       down_unit_gemm(S, p, e, S.ring[s] + static_cast<size_t>(16 * u) * Ii,
                      reinterpret_cast<const moe_bf16 *>(S.ring_s[s]) + 16 * u * (Ii / kG),
-                     nullptr, n0 + 16 * u, lane);
+                     nullptr, n0 + 16 * u, f16, lane);
   }
   __syncwarp();
   if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
@@ -1080,7 +1100,11 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     for (int j = q; consume_gu(S, p, j, q, wq, lane, budget, npass); j += kFQuads) {
     }
     grid_sync(p.grid_bar, S, budget);
-    for (int j = S.down_base + q; consume_down(S, p, wk, j, wq, lane, budget); j += kFQuads) {
+    // every h is written: the down MMAs take the fp16 copies unless some h
+    // is outside fp16's range
+    const bool f16 = __ldcg(p.h_wide) == 0u;
+    for (int j = S.down_base + q; consume_down(S, p, wk, j, wq, f16, lane, budget);
+         j += kFQuads) {
     }
     if (wk.row_owner) {
       ptx::named_barrier(1, kFConsumers);
@@ -1147,7 +1171,8 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, unsigned *unit_claims,
-                                unsigned *down_claims, float *y, cudaStream_t s) {
+                                unsigned *down_claims, float *y, uint16_t *h16,
+                                unsigned *h_wide, cudaStream_t s) {
   FusedParams p{};
   p.x = x; p.x16 = x16; p.xscale = xscale;
   p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 512;
@@ -1159,6 +1184,9 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
   p.down_claims = down_claims;
   p.y = y;
   p.h_routed = h_routed; p.h_shared = h_shared; p.out = out;
+  p.h16_routed = h16;
+  p.h16_shared = h16 + static_cast<size_t>(T) * kK * I;
+  p.h_wide = h_wide;
   p.ids_out = ids_out; p.weights_out = weights_out; p.logits_out = logits_out;
   p.gate_logit_out = gate_logit_out; p.status = status; p.grid_bar = grid_bar;
   p.budget_ns = fused_wait_budget_ns();

@@ -71,8 +71,8 @@ size_t fused_smem_bytes();
 // A1..A7 in one cooperative launch.  x16 [T][H] fp16 and xscale [T] (the
 // tokens' scaled fp16 copies), rpart [T][H/512][260] fp32, sel_ids [T][K],
 // sel_w [T][K], sel_sg [T], h_routed [T*K][I], h_shared [T][Is],
-// y [T*K + T][H] fp32, unit_claims and down_claims (one counter each)
-// scratch; grid_bar is a 32-bit counter whose low 31 bits must be zero before the first launch
+// y [T*K + T][H] fp32, h16 [T*K*I + T*Is] fp16, unit_claims, down_claims
+// and h_wide (one word each) scratch; grid_bar is a 32-bit counter whose low 31 bits must be zero before the first launch
 // (each grid barrier leaves them unchanged).
 cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 const moe_weights &w, uint16_t *x16, float *xscale,
@@ -81,7 +81,8 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 moe_bf16 *h_shared, moe_bf16 *out, int32_t *ids_out,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, unsigned *unit_claims,
-                                unsigned *down_claims, float *y, cudaStream_t s);
+                                unsigned *down_claims, float *y, uint16_t *h16,
+                                unsigned *h_wide, cudaStream_t s);
 
 // ---- prefill-size T: tcgen05 GEMMs (tc_gemm.cu: router; tc_expert.cu: experts)
 

@@ -181,3 +181,21 @@ def test_block_prefill_route_rows_odd_multiple_of_128(env, T):
                                want=("out", "out_f64"))
     assert np.array_equal(ids.cpu().numpy(), ref["ids"])
     assert_out_close(bits(out), ref["out"], "H640 prefill route")
+
+
+@pytest.mark.parametrize("T", [4, 32])
+def test_block_fused_wide_h_takes_bf16_down(env, T):
+    """Activations scaled by 2^8 scale h by 2^16, so some |h| >= 2^15 (the
+    oracle's max |h| for these inputs is about 1.1e4): the fused kernel's
+    down projection must then run on the bf16 h (its fp16 copies would
+    overflow) and still match the oracle; unscaled, it takes the fp16
+    copies.  The flag is the fifth word of the workspace."""
+    import torch
+    moe, dev = env
+    dims, _ = workload("decode")
+    x, _ = W.make_x(dims, T, 300 + T)
+    for scale, wide in ((1.0, 0), (256.0, 1)):
+        xs = W.f32_to_bf16_bits(W.bf16_bits_to_f32(x) * np.float32(scale))
+        _, _, _, blk = forward(moe, dev, "decode", xs)
+        assert int(blk.workspace[16:20].view(torch.int32).item()) == wide
+        check_block(moe, dev, "decode", xs)
