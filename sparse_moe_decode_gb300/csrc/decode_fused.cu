@@ -136,7 +136,6 @@ struct FusedSmem {
   int scan_tmp[8];
   uint64_t full[kFStages], empty[kFStages], routed;
   int2 stage_unit[kFStages];  // (expert, first row pair | first output row); x < 0: end
-  int down_base;              // ring index of the first down stage
   uint64_t red_full[kFQuads][kFRedBufs], red_empty[kFQuads][kFRedBufs];
   int abort;
 };
@@ -192,16 +191,29 @@ __device__ __forceinline__ bool aborted(FusedSmem &S) {
 
 // Bounded wait used by consumers and the producer: after an abort it no
 // longer waits, so control flow (and every named barrier) still completes.
+// The first wait of the grid to give up records where: status words 5, 6
+// and 7 = site (1: mbarrier, 2: grid barrier), detail (the mbarrier's
+// shared-memory offset, the barrier's arrival count) and the CTA.
+__device__ __forceinline__ void record_give_up(uint32_t *status, unsigned site, unsigned detail) {
+  if (atomicCAS(status + 5, 0u, site) == 0u) {
+    status[6] = detail;
+    status[7] = blockIdx.x;
+  }
+}
+
 __device__ __forceinline__ void fwait(uint64_t *bar, uint32_t parity, FusedSmem &S,
-                                      uint64_t budget) {
+                                      uint64_t budget, uint32_t *status) {
   if (aborted(S)) return;
-  ptx::mbar_wait(bar, parity, &S.abort, budget);
+  if (!ptx::mbar_wait(bar, parity, &S.abort, budget))
+    record_give_up(status, 1u, static_cast<unsigned>(reinterpret_cast<const uint8_t *>(bar) -
+                                                     reinterpret_cast<const uint8_t *>(&S)));
 }
 
 // Grid-wide barrier of the consumer threads of every CTA.  Self-resetting:
 // CTA 0 adds 2^31 - (G - 1), the others 1, so each barrier flips bit 31 of the
 // counter and leaves its low bits unchanged.  Bounded by the wait budget.
-__device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t budget) {
+__device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t budget,
+                                          uint32_t *status) {
   ptx::named_barrier(1, kFConsumers);
   if (consumer_tid() == 0) {
     __threadfence();
@@ -210,6 +222,7 @@ __device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t 
     const uint64_t t0 = ptx::globaltimer();
     while (((ld_acquire_u32(bar) ^ old) & 0x80000000u) == 0u) {
       if (aborted(S) || ptx::globaltimer() - t0 > budget) {
+        if (!aborted(S)) record_give_up(status, 2u, old & 0x7FFFFFFFu);
         *reinterpret_cast<volatile int *>(&S.abort) = 1;
         break;
       }
@@ -276,7 +289,7 @@ __device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p, i
   const int s = j % kFStages;
   int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
   if (lane == 0) {
-    fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
+    fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget, p.status);
     go = aborted(S) ? 0 : 1;
     if (go) {
       S.stage_unit[s] = make_int2(e, i0);  // published by the arrival below
@@ -319,7 +332,7 @@ __device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p,
   const int nu = rows ? min(wk.units_per_stage, wk.n_exp - a0) : 1;
   int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
   if (lane == 0) {
-    fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget);
+    fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget, p.status);
     uint32_t tx = 0;
     for (int u = 0; u < nu; ++u) {
       const int e = rows ? down_expert(S, p, a0 + u) : item.x;
@@ -563,7 +576,7 @@ __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedPara
   } else {
     const int t = blockIdx.x * kFConsumerWarps + cwarp;
     if (t < p.T) select_token(S, p, t, lane, false);
-    grid_sync(p.grid_bar, S, budget);
+    grid_sync(p.grid_bar, S, budget, p.status);
     for (int i = tid; i < p.T * kK; i += kFConsumers) {
       S.ids[i / kK][i % kK] = __ldcg(p.sel_ids + i);
       S.wts[i / kK][i % kK] = __ldcg(p.sel_w + i);
@@ -712,7 +725,7 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
 __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, int j, int q,
                                            int wq, int lane, uint64_t budget, uint32_t &npass) {
   const int s = j % kFStages;
-  fwait(&S.full[s], (j / kFStages) & 1, S, budget);
+  fwait(&S.full[s], (j / kFStages) & 1, S, budget, p.status);
   if (aborted(S)) return false;
   const int2 un = S.stage_unit[s];
   if (un.x < 0) {
@@ -790,7 +803,7 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
     const uint32_t u = npass++;
     const int b = u % kFRedBufs;
     const uint32_t rpar = (u / kFRedBufs) & 1;
-    fwait(&S.red_empty[q][b], rpar ^ 1, S, budget);
+    fwait(&S.red_empty[q][b], rpar ^ 1, S, budget, p.status);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -799,7 +812,7 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
     if (lane == 0) ptx::mbar_arrive(&S.red_full[q][b]);
     if (wq == static_cast<int>(u & 3)) {
       bool wide = false;
-      fwait(&S.red_full[q][b], rpar, S, budget);
+      fwait(&S.red_full[q][b], rpar, S, budget, p.status);
       for (int nt = 0; nt < ntiles; ++nt) {
         float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -896,7 +909,7 @@ __device__ __forceinline__ void down_unit_gemm(const FusedSmem &S, const FusedPa
 __device__ __forceinline__ bool consume_down(FusedSmem &S, const FusedParams &p, const Work &wk,
                                              int j, int wq, bool f16, int lane, uint64_t budget) {
   const int s = j % kFStages;
-  fwait(&S.full[s], (j / kFStages) & 1, S, budget);
+  fwait(&S.full[s], (j / kFStages) & 1, S, budget, p.status);
   if (aborted(S)) return false;
   const int2 it = S.stage_unit[s];
   if (it.x > kE) {  // row-owner stage k = it.y
@@ -1008,7 +1021,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
         if (jj % kFStages == i) last_use[i] = jj;
     };
     if (early && produce_gu(S, p, 0, kE, 8 * blockIdx.x, pol, budget, lane)) issued_at(0);
-    if (lane == 0) fwait(&S.routed, 0, S, budget);
+    if (lane == 0) fwait(&S.routed, 0, S, budget, p.status);
     __syncwarp();
     const Work wk = make_work(S, p);
     // Routed gate|up units are claimed from a grid-wide counter, one claim
@@ -1035,12 +1048,11 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     }
     // one end marker per quad (each quad takes every kFQuads-th stage, so
     // kFQuads consecutive markers reach every quad once)
-    auto end_markers = [&](bool gateup) {
+    auto end_markers = [&]() {
       for (int k = 0; k < kFQuads && !aborted(S); ++k, ++j) {
         if (lane == 0) {
-          fwait(&S.empty[j % kFStages], ((j / kFStages) & 1) ^ 1, S, budget);
+          fwait(&S.empty[j % kFStages], ((j / kFStages) & 1) ^ 1, S, budget, p.status);
           if (!aborted(S)) {
-            if (gateup) S.down_base = j - k + kFQuads;
             S.stage_unit[j % kFStages] = make_int2(-1, 0);
             ptx::mbar_arrive(&S.full[j % kFStages]);
           }
@@ -1048,7 +1060,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
         __syncwarp();
       }
     };
-    end_markers(true);
+    end_markers();
     if (wk.row_owner) {
       for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k, ++j)
         if (produce_down(S, p, wk, j, make_int2(kE + 1, k), pol, budget, lane)) issued_at(j);
@@ -1078,7 +1090,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
         if (produce_down(S, p, wk, j, down_item(S, p, wk, b), pol, budget, lane)) issued_at(j);
       claim = __shfl_sync(0xFFFFFFFFu, nx, 0);
     }
-    end_markers(false);
+    end_markers();
     // after an abort, let the copies already in flight land before exiting
     if (aborted(S) && lane == 0) {
       int never = 0;
@@ -1092,25 +1104,28 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     const int cw = consumer_warp(warp);
     const int q = cw >> 2, wq = cw & 3;
     phase_router(S, p, cw, lane);
-    grid_sync(p.grid_bar, S, budget);
+    grid_sync(p.grid_bar, S, budget, p.status);
     phase_select_lists(S, p, cw, lane, budget);
     if (consumer_tid() == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
     uint32_t npass = 0;
-    for (int j = q; consume_gu(S, p, j, q, wq, lane, budget, npass); j += kFQuads) {
-    }
-    grid_sync(p.grid_bar, S, budget);
+    // quad q takes ring stages q, q + kFQuads, ...: its gate|up units up to
+    // its end marker, then its down stages, so that each stage it waits for
+    // reuses the slot of a stage it consumed itself (a wait is never two
+    // phases ahead of a slot's barrier)
+    int j = q;
+    while (consume_gu(S, p, j, q, wq, lane, budget, npass)) j += kFQuads;
+    grid_sync(p.grid_bar, S, budget, p.status);
     // every h is written: the down MMAs take the fp16 copies unless some h
     // is outside fp16's range
     const bool f16 = __ldcg(p.h_wide) == 0u;
-    for (int j = S.down_base + q; consume_down(S, p, wk, j, wq, f16, lane, budget);
-         j += kFQuads) {
+    for (j += kFQuads; consume_down(S, p, wk, j, wq, f16, lane, budget); j += kFQuads) {
     }
     if (wk.row_owner) {
       ptx::named_barrier(1, kFConsumers);
       combine_rows(S, p, wk);
     } else {
-      grid_sync(p.grid_bar, S, budget);
+      grid_sync(p.grid_bar, S, budget, p.status);
       phase_combine(S, p);
     }
   }

@@ -36,7 +36,9 @@ def forward(moe, dev, name, x, T_max=None):
     blk.forward(to_dev(x, dev), out=o["out"], ids=o["ids"], weights=o["weights"],
                 logits=o["logits"], gate_logit=o["gate"])
     torch.cuda.synchronize()
-    assert blk.status() == 0
+    # status words 5..7: where a timed-out wait gave up (site, detail, CTA)
+    assert blk.status() == 0, "wait gave up: site %d detail %d cta %d" % tuple(
+        blk.workspace[20:32].view(torch.int32).tolist())
     res = {k: (bits(v) if k == "out" else v.cpu().numpy()) for k, v in o.items()}
     return dims, w, res, blk
 
