@@ -571,6 +571,14 @@ __device__ __forceinline__ void select_token(FusedSmem &S, const FusedParams &p,
 __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedParams &p, int cwarp,
                                                    int lane, uint64_t budget) {
   const int tid = consumer_tid();
+  // independent of the selection, so done first, by the last warps (idle
+  // during a local selection of T < 12 tokens)
+  for (int t2 = kFConsumers - 1 - tid; t2 < p.T; t2 += kFConsumers)
+    S.xs[t2] = __ldcg(p.xscale + t2);
+  if (tid < kE) {
+    S.counts[tid] = 0;
+    S.mask[tid] = 0ull;
+  }
   if (p.T <= kFLocalSelT) {
     if (cwarp < p.T) select_token(S, p, cwarp, lane, true);
   } else {
@@ -582,11 +590,6 @@ __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedPara
       S.wts[i / kK][i % kK] = __ldcg(p.sel_w + i);
     }
     for (int t2 = tid; t2 < p.T; t2 += kFConsumers) S.sg[t2] = __ldcg(p.sel_sg + t2);
-  }
-  for (int t2 = tid; t2 < p.T; t2 += kFConsumers) S.xs[t2] = __ldcg(p.xscale + t2);
-  if (tid < kE) {
-    S.counts[tid] = 0;
-    S.mask[tid] = 0ull;
   }
   ptx::named_barrier(1, kFConsumers);
   for (int i = tid; i < p.T * kK; i += kFConsumers) {
