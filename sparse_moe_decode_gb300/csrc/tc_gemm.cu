@@ -7,11 +7,17 @@
 // prefill chunk spreads over the SMs.  TMA brings
 // both bf16 operands into shared memory in the canonical K-major
 // SWIZZLE_128B layout; one thread issues tcgen05.mma (bf16 x bf16 -> fp32)
-// over the whole reduction into one of two TMEM accumulators; the epilogue
-// warps read it back (tcgen05.ld) and store the logits.
+// over the reduction; the epilogue warps read it back (tcgen05.ld) and store
+// the logits.  At N = 32 a tile costs more MMA issue than data, so two
+// issuing threads share it: one takes the ring stages (64-wide K steps) of
+// even index, the other those of odd index (so each ring slot always serves
+// the same issuer), each into its own TMEM accumulator, and the epilogue
+// adds the two (in that fixed order); the accumulator pairs are
+// double-buffered across a CTA's tiles.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues MMAs, warps 2..5 (one per TMEM lane quarter) write the logits.  Every wait is
+// Warp roles (224 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the even-step MMAs, warp 6 the odd-step ones, warps 2..5 (one per
+// TMEM lane quarter) write the logits.  Every wait is
 // bounded by a %globaltimer budget; on expiry the CTA drains what it has in
 // flight, frees TMEM, sets MOE_DEV_TIMEOUT and returns.
 #include <cuda.h>
@@ -24,18 +30,18 @@ namespace moe {
 
 namespace {
 
-constexpr int kRThreads = 192;
+constexpr int kRThreads = 224;
 constexpr int kRStages = 8;                 // shared-memory ring depth
 constexpr int kRTok = 32;                   // tokens per item (N)
 constexpr uint32_t kRABytes = 128 * 128;    // 128 rows x 64 bf16 of K
 constexpr uint32_t kRBBytes = kRTok * 128;  // 32 rows x 64 bf16 of K
 constexpr uint32_t kRStageBytes = kRABytes + kRBBytes;
-constexpr uint32_t kRTmemCols = 64;         // two accumulators of 32 columns
+constexpr uint32_t kRTmemCols = 128;        // two buffers x two issuers x 32 columns
 constexpr size_t kROffBar = kRStages * kRStageBytes;
 constexpr size_t kRSmem = kROffBar + 256 + 1024;  // + barriers + alignment slack
 
 struct RBars {
-  uint64_t full[kRStages], empty[kRStages], acc_full[2], acc_empty[2], done;
+  uint64_t full[kRStages], empty[kRStages], acc_full[2], acc_empty[2], done[2];
   uint32_t tmem_holder;
   int abort;
 };
@@ -63,10 +69,10 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       ptx::mbar_init(&bars->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&bars->acc_full[i], 1);
+      ptx::mbar_init(&bars->acc_full[i], 2);  // both issuers
       ptx::mbar_init(&bars->acc_empty[i], 4);
+      ptx::mbar_init(&bars->done[i], 1);
     }
-    ptx::mbar_init(&bars->done, 1);
     bars->abort = 0;
     ptx::fence_mbar_init();
   }
@@ -105,34 +111,38 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         }
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 6) {
+    if (lane == 0) {  // ------------------------------------ MMA issuers
+      const int half = warp == 1 ? 0 : 1;  // ring stages n with n mod 2 = half
       const uint32_t idesc = ptx::idesc_bf16_f32(128, kRTok);
-      uint32_t n = 0, ni = 0;
+      uint32_t ni = 0;
       bool issued = false;
       for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x, ++ni) {
         const uint32_t ab = ni & 1;
         if (!ptx::mbar_wait(&bars->acc_empty[ab], ((ni >> 1) & 1) ^ 1, abort, budget)) break;
         ptx::tc_fence_after();
-        for (int k = 0; k < nk; ++k, ++n) {
+        const uint32_t d = tmem + ab * 2 * kRTok + half * kRTok;
+        const int k0 = (half - static_cast<int>(ni * nk)) & 1;  // first K step of this issuer
+        for (int k = k0; k < nk; k += 2) {
+          const uint32_t n = ni * nk + k;  // ring stage of this K step
           const uint32_t s = n % kRStages;
           if (!ptx::mbar_wait(&bars->full[s], (n / kRStages) & 1, abort, budget)) break;
           ptx::tc_fence_after();
           const uint32_t a0 = ptx::smem_u32(smem + s * kRStageBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_bf16(tmem + ab * kRTok, ptx::sw128_desc(a0 + kk * 32),
-                          ptx::sw128_desc(a0 + kRABytes + kk * 32), idesc, k > 0 || kk > 0);
+            ptx::mma_bf16(d, ptx::sw128_desc(a0 + kk * 32),
+                          ptx::sw128_desc(a0 + kRABytes + kk * 32), idesc, k > k0 || kk > 0);
           ptx::mma_commit(&bars->empty[s]);
           issued = true;
         }
         if (*abort) break;
-        ptx::mma_commit(&bars->acc_full[ab]);
+        ptx::mma_commit(&bars->acc_full[ab]);  // with no MMAs (nk = 1): at once
       }
       if (issued) {  // all MMAs complete before TMEM is released
-        ptx::mma_commit(&bars->done);
+        ptx::mma_commit(&bars->done[half]);
         int never = 0;
-        ptx::mbar_wait(&bars->done, 0, &never, ptx::kDrainBudgetNs);
+        ptx::mbar_wait(&bars->done[half], 0, &never, ptx::kDrainBudgetNs);
       }
     }
   } else {
@@ -144,9 +154,16 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       const uint32_t ab = ni & 1;
       if (!ptx::mbar_wait(&bars->acc_full[ab], (ni >> 1) & 1, abort, budget)) break;
       ptx::tc_fence_after();
-      float v[32];
-      ptx::tmem_ld32(tmem + tl + ab * kRTok, v);
+      float v[32], v2[32];
+      // nk = 1: the tile's one K step went to the issuer of its stage's parity
+      const uint32_t only = (ni * nk) & 1;
+      ptx::tmem_ld32(tmem + tl + ab * 2 * kRTok + (nk > 1 ? 0 : only * kRTok), v);
+      if (nk > 1) ptx::tmem_ld32(tmem + tl + ab * 2 * kRTok + kRTok, v2);
       ptx::tmem_wait_ld();
+      if (nk > 1) {
+#pragma unroll
+        for (int j = 0; j < kRTok; ++j) v[j] += v2[j];  // issuer 0's sum, then issuer 1's
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars->acc_empty[ab]);
