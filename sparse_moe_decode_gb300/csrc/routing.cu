@@ -112,15 +112,32 @@ select_kernel(const float *__restrict__ logits, int T, int ld,
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (t >= T) return;
+  // the token's logits first, so that their load overlaps the gate's
+  const float4 *lrow = reinterpret_cast<const float4 *>(logits + static_cast<size_t>(t) * ld);
+  const float4 la = lrow[2 * lane], lb = lrow[2 * lane + 1];
   float g = 0.0f;
   if (w_gate) {
+    // batches of 8 chunks (2048 elements), every load of a batch in flight
+    // at once; the same lane order and fp32 summation as the router kernels
     const moe_bf16 *xr = x + static_cast<size_t>(t) * H;
-    for (int k = lane * 8; k < H; k += 256) {
-      const uint4 wv = ld_nc(w_gate + k), xv = ld_nc(xr + k);
-      g = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), g); g = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), g);
-      g = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), g); g = fmaf(bf16_hi(wv.y), bf16_hi(xv.y), g);
-      g = fmaf(bf16_lo(wv.z), bf16_lo(xv.z), g); g = fmaf(bf16_hi(wv.z), bf16_hi(xv.z), g);
-      g = fmaf(bf16_lo(wv.w), bf16_lo(xv.w), g); g = fmaf(bf16_hi(wv.w), bf16_hi(xv.w), g);
+    for (int k0 = 0; k0 < H; k0 += 2048) {
+      uint4 wv[8], xv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k = k0 + c * 256 + lane * 8;
+        if (k < H) {
+          wv[c] = ld_nc(w_gate + k);
+          xv[c] = ld_nc(xr + k);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        if (k0 + c * 256 + lane * 8 >= H) break;
+        g = fmaf(bf16_lo(wv[c].x), bf16_lo(xv[c].x), g); g = fmaf(bf16_hi(wv[c].x), bf16_hi(xv[c].x), g);
+        g = fmaf(bf16_lo(wv[c].y), bf16_lo(xv[c].y), g); g = fmaf(bf16_hi(wv[c].y), bf16_hi(xv[c].y), g);
+        g = fmaf(bf16_lo(wv[c].z), bf16_lo(xv[c].z), g); g = fmaf(bf16_hi(wv[c].z), bf16_hi(xv[c].z), g);
+        g = fmaf(bf16_lo(wv[c].w), bf16_lo(xv[c].w), g); g = fmaf(bf16_hi(wv[c].w), bf16_hi(xv[c].w), g);
+      }
     }
     g = warp_sum(g);
   } else if (gate_logit) {
@@ -128,7 +145,8 @@ select_kernel(const float *__restrict__ logits, int T, int ld,
   }
   int id[8];
   float w[8];
-  const bool ok = select_top8_warp(logits + static_cast<size_t>(t) * ld, lane, id, w);
+  const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+  const bool ok = select_top8_regs(lv, lane, id, w);
   if (!ok && lane == 0) set_status(status, MOE_DEV_NONFINITE);
   if (lane < 8) {
     int myid = id[0];
