@@ -167,7 +167,7 @@ def down_bytes(d: W.Dims, T: int, n_active: int):
 MEASURED_TRAFFIC = {
     "decode_fused": {"bytes": 530.0e6, "workload": "verify_T32",
                      "sources": ["decode_fused.cu", "common.cuh", "select.cuh", "sm100_ptx.cuh"],
-                     "sha256_16": "fb96e2695524f2da",
+                     "sha256_16": "3fb1e8a65e49be7a",
                      "profile": "profiles/decode_fused_verify_T32.md"},
     "gateup_swiglu_tc": {"bytes": 646.5e6, "workload": "prefill_T2048",
                          "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],

@@ -1,10 +1,15 @@
 // decode_fused.cu -- the whole block (A1..A7) for decode-size T in one
-// persistent cooperative kernel: one CTA per SM, phases separated by bounded
-// grid barriers (two, one more when T > 12 for the shared selection, one
-// more when T > 8 for the item-mode combine).
+// persistent cooperative kernel: one CTA per SM, 16 warps (the producer
+// warp alone on one SM sub-partition with three idle warps, twelve
+// consumer warps in three quads on the other three), phases separated by
+// bounded grid barriers (two, one more when T > 12 for the shared
+// selection, one more when T > 8 for the item-mode combine).
 //
-//   R  router: 257 rows x (H/512) K-slices of 512, one warp each, fp32
-//      partials (the pages' S1 split of the router into K-slices);
+//   R  router: each CTA stages one 512-wide K-slice of every token and of
+//      up to 16 of the 257 rows (256 experts + the shared gate) in shared
+//      memory and forms fp32 partials with bf16 tensor-core MMAs (the
+//      pages' split of the router into K-slices); the last warp of CTA t
+//      scales token t into fp16 for phase W;
 //   -- grid barrier 1 --
 //   S  one warp per token folds the partials in a fixed order and selects
 //      the top-8 with the warp merge network (softmax, shared sigmoid); for
@@ -15,32 +20,33 @@
 //   W  gate|up + SwiGLU: work unit = 8 gate rows + their 8 up rows of one
 //      expert (16 rows x H int8); the first Is / 8 CTAs take one shared
 //      unit each before routing is known, and the routed units are claimed
-//      from a grid-wide counter, so that faster CTAs take more of them; a
-//      producer warp streams each unit's rows (and their
-//      group scales) with bulk async copies into a 5-stage shared-memory ring
-//      (the shared expert's first units are fetched before routing is
-//      known); three warp quads consume units in turn, each warp a quarter
-//      of K, as m16n8k16 fp16 tensor-core MMAs: the int8 weights become fp16
-//      exactly in registers, the activations are each token's copy scaled
-//      by a power of two into fp16 (exact for every element within 2^29 of
-//      the token's largest), the group scales are promoted per 128-wide K
-//      group in fp32, a rotating reducer warp adds the four K quarters;
-//      h = bf16(silu(gate) * up) goes to global;
+//      from a grid-wide counter, so that faster CTAs take more of them; the
+//      producer streams each unit's rows and group scales with bulk async
+//      copies into a 6-stage shared-memory ring; quad q consumes ring
+//      stages q, q + 3, ..., each warp a quarter of K, as m16n8k16 fp16
+//      tensor-core MMAs: the int8 weights become fp16 exactly in registers,
+//      the activations are each token's copy scaled by a power of two into
+//      fp16 (exact for every element within 2^29 of the token's largest),
+//      the group scales are promoted per 128-wide K group in fp32, a
+//      rotating reducer warp adds the four K quarters; h = bf16(silu(gate)
+//      * up) goes to global, with an fp16 copy of each value;
 //   -- grid barrier 2 --
-//   D  down + combine, two modes chosen by T (the same in every CTA).
-//      Item mode (T > kFRowOwnerT): work item = R consecutive output rows
-//      (R * max(I, Is) = one 32 KB stage) of one expert, claimed from a
-//      second grid-wide counter by the producers as soon as their gate|up
-//      claims run out, so the down weights stream in while the gate|up tail
-//      is still computing; each warp of the consuming quad takes 16 of the
-//      rows over the full K, and y for every (slot, row) goes to global
-//      memory (fp32); after a third grid barrier every thread of the grid
-//      forms two output elements.  Row-owner mode (small T, where the extra
-//      barrier would cost more than the even split of the bytes gains): CTA
-//      c owns output rows 16c .. 16c+15 of every expert, its y stays in
-//      shared memory and the CTA writes its combined rows itself.  Both
-//      combine the 8 routed y in rank order, then the shared expert's, with
-//      one bf16 rounding.
+//   D  down + combine, two modes chosen by T (the same in every CTA); each
+//      quad's down stages continue its own ring sequence past its gate|up
+//      end marker.  Item mode (T > kFRowOwnerT): work item = R consecutive
+//      output rows (R * max(I, Is) = one 32 KB stage) of one expert,
+//      claimed from a second grid-wide counter by the producer as soon as
+//      its gate|up claims run out, so the down weights stream in while the
+//      gate|up tail is still computing; each warp of the consuming quad
+//      takes 16 of the rows over the full K (fp16 MMAs on the fp16 h, bf16
+//      ones on the bf16 h when some |h| >= 2^15), and y for every (slot,
+//      row) goes to global memory (fp32); after a third grid barrier every
+//      thread of the grid forms two output elements.  Row-owner mode (small
+//      T, where the extra barrier would cost more than the even split of
+//      the bytes gains): CTA c owns output rows 16c .. 16c+15 of every
+//      expert, its y stays in shared memory and the CTA writes its combined
+//      rows itself.  Both combine the 8 routed y in rank order, then the
+//      shared expert's, with one bf16 rounding.
 //
 // The tensor cores here are the register-fragment form (mma.sync): at
 // decode sizes each weight meets 1..~10 tokens, the kernel is bound by HBM,
