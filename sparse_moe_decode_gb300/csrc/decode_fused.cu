@@ -1040,13 +1040,14 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     // claimed; when there are few, single units keep the split even.
     const unsigned n_routed = static_cast<unsigned>(S.active[0] * wk.nIb);
     const unsigned gu_claim = n_routed >= 24u * gridDim.x ? static_cast<unsigned>(kFClaim) : 1u;
-    unsigned claim = 0;
-    if (lane == 0) claim = atomicAdd(p.unit_claims, gu_claim);
-    claim = __shfl_sync(0xFFFFFFFFu, claim, 0);
+    // the first claim of CTA c is c itself (no round trip to the counter);
+    // the counter numbers the claims after the first G
+    const unsigned gu_base = gridDim.x * gu_claim;
+    unsigned claim = blockIdx.x * gu_claim;
     int j = early ? 1 : 0;  // ring index of the next stage
     while (claim < n_routed && !aborted(S)) {
       unsigned nx = 0;
-      if (lane == 0) nx = atomicAdd(p.unit_claims, gu_claim);
+      if (lane == 0) nx = gu_base + atomicAdd(p.unit_claims, gu_claim);
       const unsigned end = min(claim + gu_claim, n_routed);
       for (unsigned b = claim; b < end && !aborted(S); ++b) {
         const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
@@ -1085,14 +1086,12 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     const unsigned G = gridDim.x;
     const unsigned per_claim = n_down >= 8u * G ? 2u : 1u;
     const unsigned cap = max(static_cast<unsigned>(kFQuads), (4u * n_down / 3u + G - 1u) / G);
-    unsigned taken = 0;
-    claim = n_down;
-    if (lane == 0 && n_down > 0) claim = atomicAdd(p.down_claims, per_claim);
-    taken += per_claim;
-    claim = __shfl_sync(0xFFFFFFFFu, claim, 0);
+    unsigned taken = per_claim;
+    const unsigned dn_base = G * per_claim;  // first claims static, as for gate|up
+    claim = blockIdx.x * per_claim;
     while (claim < n_down && !aborted(S)) {
       unsigned nx = n_down;
-      if (lane == 0 && taken < cap) nx = atomicAdd(p.down_claims, per_claim);
+      if (lane == 0 && taken < cap) nx = dn_base + atomicAdd(p.down_claims, per_claim);
       taken += per_claim;
       const unsigned end = min(claim + per_claim, n_down);
       for (unsigned b = claim; b < end && !aborted(S); ++b, ++j)
