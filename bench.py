@@ -386,6 +386,31 @@ def cpu_baseline(name: str, budget_s: float = 10.0):
     return oracle_steps(name, steps=1000, warmup=1, budget_s=budget_s)
 
 
+def collectives(dist, device):
+    """The replicas' timing collectives for any backend (NCCL on GPUs, gloo in
+    the CPU tests): a barrier, and the maximum of a float over the ranks."""
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_all(v):
+        if dist is None:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, max_all
+
+
+def whole_job_tokens_per_s(world: int, T: int, ms_max: float) -> float:
+    """Every rank runs T tokens per step; the job's step time is the slowest
+    rank's, so the whole job moves world * T tokens per ms_max."""
+    return world * T / (ms_max * 1e-3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -437,16 +462,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_all(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_all = collectives(dist, dev)
 
     pk = peaks()
     read_gbs = read_peak_gbs(torch, dev) if world == 1 or rank == 0 else None
@@ -470,7 +486,7 @@ def main():
         t_tc = flops / (pk["bf16_tflops"] * 1e12)
         k_dom = int(np.argmax(per_kernel))
         r = {
-            "tokens_per_s": world * T / (ms * 1e-3), "ms_per_step": ms,
+            "tokens_per_s": whole_job_tokens_per_s(world, T, ms), "ms_per_step": ms,
             "T": T, "n_active_experts": n_act, "algorithmic_bytes": bytes_step,
             "achieved_gbs": gbs, "frac_hbm_measured": gbs / pk["hbm_gbs"],
             "frac_hbm_8000": gbs / 8000.0, "tflops": tfs,
@@ -490,7 +506,8 @@ def main():
             r["_kernel"] = (b.kernel_names[k_dom], per_kernel[k_dom], kb)
             e2e_s, bi, bo = b.e2e(args.steps, args.warmup)
             e2e_s = max_all(e2e_s)
-            r["e2e"] = {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+            r["e2e"] = {"value": whole_job_tokens_per_s(world, T, e2e_s * 1e3),
+                        "unit": "tokens/s", "h2d_bytes_per_step": bi,
                         "d2h_bytes_per_step": bo}
             r["gpu_launches"] = args.steps * b.nk
             head = r
