@@ -770,9 +770,9 @@ down_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
 // (e == kE, B rows indexed by token), the item totals and slot_of = -1 for
 // entries that name no expert.
 constexpr int kLiThreads = 1024;
-constexpr int kLiPer = 16;  // entries per thread and pass
+constexpr int kLiPer = 8;  // entries per thread and pass (two CTAs of 1024 threads per SM)
 
-__global__ void __launch_bounds__(kLiThreads)
+__global__ void __launch_bounds__(kLiThreads, 2)
 lists_items_kernel(const int32_t *__restrict__ ids, int T, Lists L, int I, int Is, int H,
                    int4 *__restrict__ gu, int *__restrict__ n_gu, int4 *__restrict__ dn,
                    int *__restrict__ n_dn) {
