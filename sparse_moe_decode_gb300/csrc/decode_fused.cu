@@ -598,6 +598,56 @@ __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedPara
     for (int t2 = tid; t2 < p.T; t2 += kFConsumers) S.sg[t2] = __ldcg(p.sel_sg + t2);
   }
   ptx::named_barrier(1, kFConsumers);
+  if (p.T * kK <= 32) {
+    // Up to 32 (token, slot) entries: one warp sorts the keys (expert, entry)
+    // with a bitonic network over its lanes; the sorted order is the list
+    // order (experts ascending, tokens ascending within an expert, as the
+    // general path below builds it), and each run of one expert gives its
+    // count, offset and place in the active list.
+    if (cwarp == 0) {
+      const int n = p.T * kK;
+      int e0 = kE;  // entries naming no expert (and padding lanes) sort last
+      if (lane < n) {
+        const int v = S.ids[lane / kK][lane % kK];
+        if (v >= 0) e0 = v;
+      }
+      unsigned key = (static_cast<unsigned>(e0) << 8) | static_cast<unsigned>(lane);
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+          const unsigned other = __shfl_xor_sync(0xFFFFFFFFu, key, jj);
+          const bool keep_min = ((lane & jj) == 0) == ((lane & k) == 0);
+          key = keep_min ? min(key, other) : max(key, other);
+        }
+      const int e = static_cast<int>(key >> 8), i = static_cast<int>(key & 0xFFu);
+      const bool valid = e < kE;
+      const unsigned valid_mask = __ballot_sync(0xFFFFFFFFu, valid);
+      const int n_valid = __popc(valid_mask);
+      const int prev = __shfl_up_sync(0xFFFFFFFFu, e, 1);
+      const bool start = valid && (lane == 0 || prev != e);
+      const unsigned starts = __ballot_sync(0xFFFFFFFFu, start);
+      if (valid) {
+        S.perm[lane] = i;
+        S.slot_of[i / kK][i % kK] = lane;
+      } else if (i < n) {
+        S.slot_of[i / kK][i % kK] = -1;
+      }
+      if (start) {
+        const unsigned above = lane == 31 ? 0u : starts & ~((2u << lane) - 1u);
+        const int next = above ? __ffs(above) - 1 : n_valid;
+        S.counts[e] = next - lane;
+        S.offsets[e] = lane;
+        S.active[1 + __popc(starts & ((1u << lane) - 1u))] = e;
+      }
+      if (lane == 0) {
+        S.active[0] = __popc(starts);
+        S.offsets[kE] = n_valid;
+      }
+    }
+    ptx::named_barrier(1, kFConsumers);
+    return;
+  }
   for (int i = tid; i < p.T * kK; i += kFConsumers) {
     const int t = i / kK, e = S.ids[t][i % kK];
     if (e >= 0) {

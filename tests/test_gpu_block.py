@@ -153,9 +153,18 @@ def test_block_nonfinite_input_sets_status_and_keeps_shared(env):
     blk = moe.MoEBlock(dims.H, dims.I, dims.Is, wd, T_max=3, device=dev)
     ids = torch.empty((3, 8), dtype=torch.int32, device=dev)
     out = torch.empty((3, dims.H), dtype=torch.int16, device=dev)
-    blk.forward(to_dev(x, dev), out=out, ids=ids)
+    lg = torch.empty((3, 256), dtype=torch.float32, device=dev)
+    gl = torch.empty((3,), dtype=torch.float32, device=dev)
+    blk.forward(to_dev(x, dev), out=out, ids=ids, logits=lg, gate_logit=gl)
     assert blk.status() & moe.DEV_NONFINITE
     assert (ids[1].cpu().numpy() == -1).all() and (ids[0].cpu().numpy() >= 0).all()
+    # the finite tokens are computed as usual, the other one gets only the
+    # shared expert (whose gate is finite here only if its logit is)
+    ref = oracle.block_forward(dims.as_dict(), w, x, tokens=np.array([0, 2], np.int32),
+                               route_logits=lg.cpu().numpy(), route_gate=gl.cpu().numpy(),
+                               nthreads=ncpu(), want=("out",))
+    assert np.array_equal(ids.cpu().numpy()[[0, 2]], ref["ids"][[0, 2]])
+    assert_out_close(bits(out)[[0, 2]], ref["out"][[0, 2]], "pr1")
     blk.clear_status()
     assert blk.status() == 0
 
