@@ -155,12 +155,13 @@ moe_status moe_combine(const moe_dims *dims, int T, const float *y,
 /* A1..A7 in one call: out [T][H] bf16 from x [T][H] bf16.  Optional outputs
  * (each nullable): ids_out [T][8], weights_out [T][8], logits_out [T][E],
  * gate_logit_out [T].  Routes, chosen by sizes only: T <= 64 with
- * hidden <= 2048 (a multiple of 256) and intermediate sizes <= 2048 runs one
+ * hidden <= 2048 (a multiple of 512) and intermediate sizes <= 2048 runs one
  * persistent cooperative kernel (one CTA per SM, bounded grid barriers);
- * other T < 128 run separate weight-streaming kernels; T >= 128 runs tcgen05
+ * other T <= 64 run separate weight-streaming kernels; T >= 65 runs tcgen05
  * grouped GEMMs.  All routes meet the same tolerance and route on the same
  * fp32 logits.  The environment variable MOE_DECODE_ROUTE=gemv (read once
- * per process) forces the separate kernels below T = 128, for diagnostics.  For large T the routed terms are summed
+ * per process) forces the separate kernels for T <= 64, for diagnostics.
+ * For large T the routed terms are summed
  * with fp32 atomics, so the last fp32 bit of an unrounded sum (and, rarely,
  * the bf16 rounding of out) may vary between runs. */
 moe_status moe_block_forward(const moe_dims *dims, const moe_weights *w,

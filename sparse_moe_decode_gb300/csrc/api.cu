@@ -61,8 +61,11 @@ struct Layout {
 };
 
 // Token count from which moe_block_forward runs the tcgen05 grouped GEMMs
-// instead of the weight-streaming kernels.
-constexpr int kTcMinT = 128;
+// instead of the weight-streaming kernels: measured on GB300 at H = 2048,
+// I = 512, the grouped GEMMs take 271 us at T = 128 and about as long down
+// to T = 65, where the separate weight-streaming kernels took 761 us (and
+// 1064 us at T = 127).
+constexpr int kTcMinT = 65;
 
 // Routes of moe_block_forward, chosen by sizes only (so that workspace sizes
 // never depend on the device): the fused persistent decode kernel, the
