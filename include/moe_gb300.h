@@ -3,16 +3,18 @@
  *
  * The block is the MoE layer of a hybrid Qwen-style model at serving time:
  *   A1  router GEMV: 256 expert logits plus one shared-expert gate logit
- *       per token (the "T x 257" rows of the S1/S2 router kernels in
+ *       per token (the T x 257 rows of the S1/S2 router kernels in
  *       ninfer-windows PR #8, roofline paragraph);
- *   A2  per-token top-8 under the total order "greater logit wins, lower
- *       expert id breaks a tie", softmax over the 8 selected logits, sigmoid
+ *   A2  per-token top-8 under a total order (the larger logit first, the
+ *       lower expert id first among equal logits), softmax over the 8
+ *       selected logits, sigmoid
  *       of the shared gate logit (PR #8, paragraphs on the warp merge network,
  *       sparse_moe_ranked_better and the untouched selector tail);
  *   A3  token -> expert lists (PR #8, the prefill select_count kernel);
  *   A4  int8 group-128 expert gate|up GEMV + SwiGLU, activations in bf16
- *       (ninfer 0.9.0 release notes, "W8 SwiGLU" route table row;
- *       ninfer-tp2 v0.2.3, "A16 SwiGLU and down projections");
+ *       (ninfer 0.9.0 release notes, the W8 SwiGLU row of the route table;
+ *       ninfer-tp2 v0.2.3, 16-bit activations in the SwiGLU and down
+ *       projections);
  *   A5  int8 group-128 expert down projection;
  *   A6  the shared expert (A4 + A5 on every token) scaled by the gate;
  *   A7  weighted combine into a bf16 output row per token.
