@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_select_topk.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
             L.oracle_select_topk.restype = i32
             L.oracle_expert_lists.argtypes = [i32, i32, i32, P, P, P, P]
+            L.oracle_merge_topk.argtypes = [i32, i32, i32, P, P, P, P]
+            L.oracle_merge_topk.restype = i32
             L.oracle_w8_gemv.argtypes = [i32, i32, i32, P, P, P, P]
             L.oracle_swiglu.argtypes = [i32, P, P, P]
             L.oracle_combine.argtypes = [i32, i32, P, P, P, ctypes.c_double, P, P]
@@ -121,6 +123,32 @@ def select_topk(logits, gate_logit=None, K: int = 8):
     bad = lib().oracle_select_topk(T, E, K, E, _p(logits), _p(g), _p(ids), _p(w),
                                    _p(sg))
     return ids, w, sg, bad
+
+
+def candidates_topk(logits, K: int):
+    """Wide top-k candidates: ids [T][K] int32 in rank order and their fp32
+    values [T][K] (the row's entries at those ids); a non-finite row gets
+    ids -1 and values 0.  Returns (ids, values, bad)."""
+    logits = _c(logits, np.float32)
+    T, N = logits.shape
+    ids, _, _, bad = select_topk(logits, K=K)
+    vals = np.zeros((T, K), np.float32)
+    ok = ids[:, 0] >= 0
+    vals[ok] = np.take_along_axis(logits[ok], ids[ok].astype(np.int64), axis=1)
+    return ids, vals, bad
+
+
+def merge_topk(ids, values, K: int):
+    """Exact merge: ids/values [T][n_lists][K] candidate lists -> the K best
+    pairs of each row's union, ids [T][K] int32, values [T][K] fp32."""
+    ids = _c(ids, np.int32)
+    values = _c(values, np.float32)
+    T, n_lists, k_in = ids.shape
+    assert k_in == K and values.shape == ids.shape
+    out_i = np.empty((T, K), np.int32)
+    out_v = np.empty((T, K), np.float32)
+    bad = lib().oracle_merge_topk(T, n_lists, K, _p(ids), _p(values), _p(out_i), _p(out_v))
+    return out_i, out_v, bad
 
 
 def expert_lists(ids, E: int):

@@ -136,6 +136,41 @@ int oracle_select_topk(int T, int E, int K, int ld, const float *logits,
   return bad;
 }
 
+/* ---------------------------------------- candidate lists: exact merge */
+
+int oracle_merge_topk(int T, int n_lists, int K, const int32_t *ids,
+                      const float *values, int32_t *ids_out, float *values_out) {
+  const int n = n_lists * K;
+  int bad = 0;
+  ranked *all = (ranked *)malloc(sizeof(ranked) * (size_t)n);
+  for (int t = 0; t < T; ++t) {
+    const int32_t *ri = ids + (size_t)t * n;
+    const float *rv = values + (size_t)t * n;
+    int invalid = 0;
+    for (int i = 0; i < n; ++i) {
+      if (ri[i] < 0) invalid = 1;
+      all[i].v = rv[i];
+      all[i].id = ri[i];
+    }
+    if (invalid) {
+      for (int j = 0; j < K; ++j) {
+        ids_out[(size_t)t * K + j] = -1;
+        values_out[(size_t)t * K + j] = 0.0f;
+      }
+      ++bad;
+      continue;
+    }
+    /* the union sorted under the same total order as the selection */
+    qsort(all, (size_t)n, sizeof(ranked), ranked_cmp);
+    for (int j = 0; j < K; ++j) {
+      ids_out[(size_t)t * K + j] = all[j].id;
+      values_out[(size_t)t * K + j] = all[j].v;
+    }
+  }
+  free(all);
+  return bad;
+}
+
 /* ----------------------------------------------------- A3 expert lists */
 
 void oracle_expert_lists(int T, int E, int K, const int32_t *ids,

@@ -67,6 +67,21 @@ int oracle_select_topk(int T, int E, int K, int ld, const float *logits,
                        const float *gate_logit, int32_t *ids, double *weights,
                        double *sgate);
 
+/* Wide top-k candidates and their exact merge (the candidate selector of
+ * the DFlash2 drafter: GPU top-k with at most 16 candidates, lucebox
+ * commit list, "candidate selector head"; a vocabulary split across two
+ * GPUs joined by an exact top-16 merge, ninfer-tp2 v0.4.0 notes).  The
+ * selection itself is oracle_select_topk on rows of any width (ids only are
+ * used; the values are the row's entries at those ids).
+ *
+ * oracle_merge_topk: row t holds n_lists candidate lists of K (value, id)
+ * pairs each, at values/ids + t*n_lists*K; the output is the K best pairs of
+ * their union under the selector's total order, in rank order.  An id < 0
+ * anywhere in the row (a list from a non-finite row) makes the output row
+ * ids -1, values 0.  Returns the number of such rows. */
+int oracle_merge_topk(int T, int n_lists, int K, const int32_t *ids,
+                      const float *values, int32_t *ids_out, float *values_out);
+
 /* A3 token -> expert lists: counts[e] = #(t,j) with ids[t][j]==e,
  * offsets[0..E] exclusive scan of counts, perm = the entries t*K+j sorted by
  * (expert, t, j).  Entries with id < 0 are skipped. */

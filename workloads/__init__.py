@@ -250,6 +250,24 @@ def make_selector_logits(T: int, E: int = 256, seed: int | None = None):
     return out
 
 
+# Candidate selection over a vocabulary: 8 block positions (a draft of 7
+# tokens plus the anchor) against a 151,936-wide lm_head row.
+CANDIDATES_T, CANDIDATES_N, CANDIDATES_K = 8, 151936, 16
+
+
+def make_candidate_logits(T: int, N: int, seed: int):
+    """Wide rows: even t ~ 3*N(0,1) (fp32), odd t integers in [-8, 8] (many
+    ties, so the lower-id rule decides most places)."""
+    out = np.empty((T, N), np.float32)
+    for t in range(T):
+        k = stream_key(seed, "logits", 1000 + t)
+        if t % 2 == 0:
+            out[t] = (3.0 * normal(N, k)).astype(np.float32)
+        else:
+            out[t] = int_uniform(N, k, -8, 8).astype(np.float32)
+    return out
+
+
 def workload_inputs(name: str, T: int | None = None, seed: int | None = None):
     """(dims, weights, x, info) of a named workload, T/seed overridable."""
     wl = WORKLOADS[name]
