@@ -22,6 +22,8 @@ Timing protocol:
   * cpu_baseline: the fp64 oracle on this host's cores, on a bounded sample.
 Multi-GPU: replicas only (the block has no exchange step); each rank runs
 the same workload on its own GPU and `value` sums the ranks' tokens.
+Unless --only is given, `workloads` also times the wide-row top-16 candidate
+selector (T = 8 and 64 rows of a 151,936-wide vocabulary, L2-cold).
 """
 from __future__ import annotations
 
@@ -345,6 +347,48 @@ class Bench:
         return t / steps, 2 * self.T * self.d.H, 2 * self.T * self.d.H
 
 
+def bench_candidates(moe, torch, dev, T: int, steps: int, warmup: int, peak_gbs: float):
+    """Wide-row top-16 candidates (the drafter's lm_head candidate selector):
+    T rows of the 151,936-wide vocabulary.  R rotating input buffers, more
+    than twice L2 in all, captured as R calls in one CUDA graph; per-call
+    time = replay time / R."""
+    N, k = W.CANDIDATES_N, W.CANDIDATES_K
+    row_bytes = N * 4
+    R = max(8, -(-300_000_000 // (T * row_bytes)))
+    bufs = [torch.from_numpy(W.make_candidate_logits(T, N, seed=500 + r)).to(dev)
+            for r in range(min(R, 4))]
+    bufs += [bufs[r % len(bufs)].clone() for r in range(len(bufs), R)]
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    vals = torch.empty((T, k), dtype=torch.float32, device=dev)
+    ws_bytes = moe.moe_topk_workspace_bytes(T, N)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for r in range(R):  # eager pass: checks the calls before capture
+            moe.moe_topk_candidates(bufs[r], T, N, N, k, ids, vals, ws, ws_bytes, s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for r in range(R):
+                moe.moe_topk_candidates(bufs[r], T, N, N, k, ids, vals, ws, ws_bytes, s)
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(ws) == 0
+    us = e0.elapsed_time(e1) * 1e3 / (steps * R)
+    nbytes = T * row_bytes + T * k * 8
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"rows_per_s": T / (us * 1e-6), "us_per_call": us, "T": T, "N": N, "k": k,
+            "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "frac_hbm_measured": gbs / peak_gbs,
+            "kernels_per_call": 2, "l2": "cold: %d rotating inputs of %.1f MB" % (R, T * row_bytes / 1e6)}
+
+
 def _oracle_inputs(name: str, n: int):
     wl = W.WORKLOADS[name]
     w = W.make_weights(wl.dims, wl.seed)
@@ -515,6 +559,10 @@ def main():
         del b
         torch.cuda.empty_cache()
 
+    if not args.only:
+        for Tc in (W.CANDIDATES_T, 64):
+            results["candidates_T%d_N%d_k%d" % (Tc, W.CANDIDATES_N, W.CANDIDATES_K)] = \
+                bench_candidates(moe, torch, dev, Tc, args.steps, args.warmup, pk["hbm_gbs"])
     if rank != 0:
         return
     kname, kms, kbytes = head.pop("_kernel")

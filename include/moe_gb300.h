@@ -217,6 +217,38 @@ moe_status moe_block_forward_noalloc(const moe_dims *dims, const moe_weights *w,
                                      const moe_bf16 *x, int T, moe_bf16 *out,
                                      void *stream);
 
+/* Candidate selection over wide rows (the drafter's top-k lm_head
+ * candidates, k raised from 8 to 16: lucebox commit list, "candidate
+ * selector head"), and the exact merge that joins vocabulary shards
+ * (ninfer-tp2 v0.4.0 notes: the proposal head split by vocabulary, "exact
+ * top-16 merge").  Same order as moe_select_top8: greater value wins, the
+ * lower index breaks a tie, -0 ties +0.  Every k in 1..16 is served; other
+ * k return MOE_ERR_UNSUPPORTED (never a silent default).
+ *
+ * moe_topk_candidates: for each row t (at logits + t*ld, N fp32 entries,
+ * ld >= N, ld a multiple of 4, logits 16-byte aligned), ids[t][0..k-1] =
+ * the k best column indices in rank order and values[t][j] =
+ * logits[t][ids[t][j]] (bit for bit).  k <= N <= 2^24.  A row holding NaN
+ * or +-inf gets ids -1 and values 0 and sets MOE_DEV_NONFINITE.  The
+ * workspace (moe_topk_workspace_bytes) holds the status word and one run of
+ * 16 keys per 8192 columns of each row.  ids [T][k] int32, values [T][k]. */
+size_t moe_topk_workspace_bytes(int T, int N);
+moe_status moe_topk_candidates(const float *logits, int T, int ld, int N, int k,
+                               int32_t *ids, float *values, void *workspace,
+                               size_t ws_bytes, void *stream);
+
+/* moe_topk_merge: row t holds n_lists candidate lists of k (id, value)
+ * pairs at ids/values + t*n_lists*k (any order inside a list; the ids of a
+ * row distinct and >= 0, e.g. the per-shard results of moe_topk_candidates
+ * with each shard's column offset added).  ids_out[t][0..k-1] / values_out =
+ * the k best pairs of the row's union in rank order, exact whenever each
+ * list holds its shard's top k.  A row with any id < 0 gets ids -1 and
+ * values 0 and sets MOE_DEV_NONFINITE.  The workspace holds only the status
+ * word (ws_bytes >= 256).  1 <= n_lists <= 65536. */
+moe_status moe_topk_merge(const int32_t *ids, const float *values, int T, int n_lists,
+                          int k, int32_t *ids_out, float *values_out,
+                          void *workspace, size_t ws_bytes, void *stream);
+
 /* Copy the device status word to *bits (synchronises the stream). */
 moe_status moe_read_status(const void *workspace, void *stream, uint32_t *bits);
 /* Zero the first 256 bytes of the workspace: the device status word and the

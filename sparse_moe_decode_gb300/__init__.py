@@ -27,7 +27,8 @@ __all__ = [
     "moe_workspace_bytes", "moe_read_status", "moe_clear_status", "MoEBlock",
     "DEV_NONFINITE", "DEV_BAD_EXPERT", "DEV_TIMEOUT", "EXPORTS",
     "moe_block_forward_profiled", "moe_block_kernel_count", "moe_block_kernel_name",
-    "moe_block_forward_noalloc",
+    "moe_block_forward_noalloc", "moe_topk_workspace_bytes", "moe_topk_candidates",
+    "moe_topk_merge",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -43,7 +44,8 @@ EXPORTS = (
     "moe_block_forward", "moe_block_forward_host", "moe_read_status",
     "moe_clear_status", "moe_status_string", "moe_abi_version",
     "moe_block_forward_profiled", "moe_block_kernel_count", "moe_block_kernel_name",
-    "moe_block_forward_noalloc",
+    "moe_block_forward_noalloc", "moe_topk_workspace_bytes", "moe_topk_candidates",
+    "moe_topk_merge",
 )
 
 
@@ -105,6 +107,9 @@ def lib() -> ctypes.CDLL:
                 "moe_block_kernel_count": (I, [DP, I]),
                 "moe_block_kernel_name": (ctypes.c_char_p, [DP, I, I]),
                 "moe_block_forward_noalloc": (I, [DP, WP, P, I, P, P]),
+                "moe_topk_workspace_bytes": (Z, [I, I]),
+                "moe_topk_candidates": (I, [P, I, I, I, I, P, P, P, Z, P]),
+                "moe_topk_merge": (I, [P, P, I, I, I, P, P, P, Z, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -226,6 +231,23 @@ def moe_block_forward_noalloc(dims, weights: Weights, x, T, out, stream=None):
     _check(lib().moe_block_forward_noalloc(ctypes.byref(dims), ctypes.byref(weights), _a(x),
                                            int(T), _a(out), _s(stream)),
            "moe_block_forward_noalloc")
+
+
+def moe_topk_workspace_bytes(T, N) -> int:
+    return int(lib().moe_topk_workspace_bytes(int(T), int(N)))
+
+
+def moe_topk_candidates(logits, T, ld, N, k, ids, values, workspace, ws_bytes, stream=None):
+    _check(lib().moe_topk_candidates(_a(logits), int(T), int(ld), int(N), int(k), _a(ids),
+                                     _a(values), _a(workspace), int(ws_bytes), _s(stream)),
+           "moe_topk_candidates")
+
+
+def moe_topk_merge(ids, values, T, n_lists, k, ids_out, values_out, workspace, ws_bytes,
+                   stream=None):
+    _check(lib().moe_topk_merge(_a(ids), _a(values), int(T), int(n_lists), int(k), _a(ids_out),
+                                _a(values_out), _a(workspace), int(ws_bytes), _s(stream)),
+           "moe_topk_merge")
 
 
 def moe_read_status(workspace, stream=None) -> int:

@@ -50,6 +50,11 @@ bool opt_ok(const void *p) { return p == nullptr || aligned(p, 16); }
 
 size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// candidate selection: run length (the largest k), widest row, most lists
+constexpr int kTopkRun = 16;
+constexpr int kTopkMaxN = 1 << 24;
+constexpr int kTopkMaxLists = 65536;
+
 // Workspace carving for a call with T tokens; offsets are 256-byte aligned
 // and grow monotonically with T, so a workspace sized for T_max serves every
 // T <= T_max.
@@ -454,6 +459,40 @@ const char *moe_block_kernel_name(const moe_dims *dims, int T, int i) {
   if (r == kRouteFused) return kFusedStageNames[i];
   if (r == kRouteGemv) return kStageNames[i];
   return kTcStageNames[i];
+}
+
+size_t moe_topk_workspace_bytes(int T, int N) {
+  if (T < 0 || T > kMaxT || N < 1 || N > kTopkMaxN) return 0;
+  return 256 + up256(static_cast<size_t>(T) * topk_chunks(N) * kTopkRun * sizeof(uint64_t));
+}
+
+moe_status moe_topk_candidates(const float *logits, int T, int ld, int N, int k, int32_t *ids,
+                               float *values, void *workspace, size_t ws_bytes, void *stream) {
+  if (T < 0 || N < 1 || ld < N || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kTopkRun || T > kMaxT || N > kTopkMaxN) return MOE_ERR_UNSUPPORTED;
+  if (k > N) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_topk_workspace_bytes(T, N)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(logits) || ld % 4 || !ptr_ok(ids) || !ptr_ok(values)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_topk(logits, T, ld, N, k, ids, values,
+                                 at<uint64_t>(workspace, 256), static_cast<uint32_t *>(workspace),
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_topk_merge(const int32_t *ids, const float *values, int T, int n_lists, int k,
+                          int32_t *ids_out, float *values_out, void *workspace, size_t ws_bytes,
+                          void *stream) {
+  if (T < 0 || n_lists < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (k > kTopkRun || T > kMaxT || n_lists > kTopkMaxLists) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(ids) || !ptr_ok(values) || !ptr_ok(ids_out) || !ptr_ok(values_out))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_topk_merge(ids, values, T, n_lists, k, ids_out, values_out,
+                                       static_cast<uint32_t *>(workspace),
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_read_status(const void *workspace, void *stream, uint32_t *bits) {

@@ -38,6 +38,15 @@ cudaError_t launch_select(const float *logits, int T, int ld, const float *gate_
                           const moe_bf16 *w_gate = nullptr, int H = 0,
                           float *gate_out = nullptr, int32_t *counts = nullptr);
 
+// Wide-row top-k candidates (topk.cu): runs holds T * topk_chunks(N) runs
+// of 16 keys.  The merge takes caller lists of (id, value) pairs.
+int topk_chunks(int N);
+cudaError_t launch_topk(const float *logits, int T, int ld, int N, int k, int32_t *ids,
+                        float *values, uint64_t *runs, uint32_t *status, cudaStream_t s);
+cudaError_t launch_topk_merge(const int32_t *ids, const float *values, int T, int n_lists,
+                              int k, int32_t *ids_out, float *values_out, uint32_t *status,
+                              cudaStream_t s);
+
 // A3: deterministic counting sort of the T*K entries (single CTA).
 cudaError_t launch_lists(const int32_t *ids, int T, Lists L, uint32_t *status, cudaStream_t s);
 

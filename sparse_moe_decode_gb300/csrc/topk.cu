@@ -1,0 +1,337 @@
+// topk.cu -- exact top-k candidates over wide rows, and the exact merge of
+// candidate lists (k <= 16).
+//
+// What it computes: the candidate selector of the DFlash2 drafter takes the
+// top-k lm_head entries of each block position on the GPU, with k raised
+// from 8 to 16 (lucebox commit list, "candidate selector head"); the
+// two-GPU drafter splits the vocabulary and joins the halves with an exact
+// top-16 merge (ninfer-tp2 v0.4.0 notes).  The order is the MoE selector's:
+// greater value wins, the lower index breaks a tie, -0 ties +0
+// (sparse_moe_ranked_better in ninfer-windows PR #8; the split proposal head
+// of ninfer-tp2 v0.4.x sends ties to the lower row the same way).  Every k
+// from 1 to 16 is served by the same code; there are no per-k instances to
+// leave holes (the lucebox fix for K = 9..11 and 13..15 returning scratch).
+//
+// GB300 form.  A (value, index) pair is one 64-bit key whose unsigned order
+// is the selector's order: the high word is the value's bits made
+// order-preserving (-0 first mapped to +0), the low word the complement of
+// the index, so a lower index gives a larger key.  Key 0 is below every real
+// key and pads short runs.
+//   phase 1 (topk_chunk_kernel): one CTA per 8192 columns of a row; each lane
+//     streams 32 values (eight coalesced 16-byte loads, all in flight at
+//     once), sorts two runs of 16 with a bitonic network in registers and
+//     merges them; five xor-shuffle levels merge the warp's 32 runs; warp 0
+//     merges the CTA's 8 warp runs from shared memory and writes one sorted
+//     run of 16 keys per CTA.  HBM-bound: each logit is read once.
+//   phase 2 (topk_merge_kernel): one CTA per row; lanes fold the row's runs
+//     in, warps merge by shuffles, warp 0 merges the warp runs and writes the
+//     first k.  The same kernel merges caller lists of (id, value) pairs.
+// A row holding NaN or +-inf is a precondition violation, as for the MoE
+// selector: its ids are -1, its values 0, and MOE_DEV_NONFINITE is set.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRun = 16;                              // run length: the largest k served
+constexpr int kTkThreads = 256;                       // 8 warps
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kTkVec = 8;                             // 16-byte loads per lane
+constexpr int kTkWarpCols = 32 * 4 * kTkVec;          // 1024 columns per warp
+constexpr int kTkCtaCols = kTkWarps * kTkWarpCols;    // 8192 columns per CTA
+// The run written for a chunk that held a non-finite value (or folded in for
+// a caller list with a negative id): every real key has a low word >= 2^31
+// (indices < 2^31), so key 1 is never a real entry.
+constexpr uint64_t kInvalidKey = 1ull;
+
+__device__ __forceinline__ uint64_t cand_key(float v, uint32_t id) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;                          // -0 ties +0
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);      // order-preserving
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~id);
+}
+
+__device__ __forceinline__ int32_t cand_id(uint64_t k) {
+  return static_cast<int32_t>(~static_cast<uint32_t>(k));
+}
+
+__device__ __forceinline__ uint64_t kmax(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+// Candidate space of one warp: at most 16 lanes (or lists) reach the floor,
+// with 32 (or 16) keys each, after the warp's running best 16.
+constexpr int kTkCand = kRun + 16 * 32;
+
+struct TopkSmem {
+  uint64_t cand[kTkWarps][kTkCand];
+  uint64_t top[kTkWarps][kRun];       // each warp's best 16 by rank (0 = none)
+  uint64_t lane_max[kTkWarps][32];
+  uint64_t out[kRun];                 // the CTA's best 16 by rank
+  uint64_t floor_key[kTkWarps];
+};
+
+// rank of x among the n keys at c (keys distinct except 0): the number of
+// larger keys.  Broadcast reads of shared memory, four compares in flight.
+__device__ __forceinline__ int rank_in(const uint64_t *c, int n, uint64_t x) {
+  int r = 0, f = 0;
+  for (; f + 4 <= n; f += 4)
+    r += (c[f] > x) + (c[f + 1] > x) + (c[f + 2] > x) + (c[f + 3] > x);
+  for (; f < n; ++f) r += c[f] > x;
+  return r;
+}
+
+// The warp's best 16 of its n candidates in S.cand[warp] into S.top[warp]
+// (slot = rank; a slot no key reaches keeps 0).  Keys are distinct, so the
+// ranks are.  Ends with the warp synchronised.
+__device__ __forceinline__ void warp_rank_top(TopkSmem &S, int warp, int lane, int n) {
+  __syncwarp();
+  if (lane < kRun) S.top[warp][lane] = 0ull;
+  __syncwarp();
+  for (int e = lane; e < n; e += 32) {
+    const uint64_t x = S.cand[warp][e];
+    const int r = rank_in(S.cand[warp], n, x);
+    if (r < kRun) S.top[warp][r] = x;
+  }
+  __syncwarp();
+}
+
+// Appends the keys of this lane selected by mask (bit i: keys[i]) to
+// S.cand[warp] after `start` entries; returns the new total.
+template <int M>
+__device__ __forceinline__ int warp_append(TopkSmem &S, int warp, int lane, int start,
+                                           const uint64_t (&keys)[M], uint32_t mask) {
+  const int c = __popc(mask);
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  const int total = start + __shfl_sync(0xFFFFFFFFu, incl, 31);
+  int off = start + incl - c;
+#pragma unroll
+  for (int i = 0; i < M; ++i)
+    if ((mask >> i) & 1u) S.cand[warp][off++] = keys[i];
+  return total;
+}
+
+// The CTA's best 16 of the warps' S.top entries into S.out, by all threads
+// (entry tid < 128 ranks itself against the 128).  Ends synchronised.
+__device__ __forceinline__ void cta_rank_top(TopkSmem &S) {
+  if (threadIdx.x < kRun) S.out[threadIdx.x] = 0ull;
+  __syncthreads();
+  const uint64_t *all = &S.top[0][0];
+  if (threadIdx.x < kTkWarps * kRun) {
+    const uint64_t x = all[threadIdx.x];
+    if (x != 0ull) {
+      const int r = rank_in(all, kTkWarps * kRun, x);
+      if (r < kRun) S.out[r] = x;
+    }
+  }
+  __syncthreads();
+}
+
+// Phase 1: the sorted best 16 keys of each 8192-column chunk of each row.
+// Block b covers row b / n_cta, columns (b % n_cta) * 8192 ...; warp w the
+// 1024 columns from there + 1024 w; lane l the float4 at l + 32 i of them.
+// The 16th best of the warp's 32 lane maxima bounds the warp's 16th best
+// from below (16 lanes each hold a key at least that large), so only keys
+// at or above it are candidates, and only the 16 lanes whose maxima reach
+// it hold any.
+__global__ void __launch_bounds__(kTkThreads) topk_chunk_kernel(
+    const float *__restrict__ logits, int ld, int N, int n_cta, uint64_t *__restrict__ runs) {
+  __shared__ TopkSmem S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x / n_cta, c = blockIdx.x - t * n_cta;
+  const float *row = logits + static_cast<size_t>(t) * ld;
+  const int base = c * kTkCtaCols + warp * kTkWarpCols + 4 * lane;
+  float4 q[kTkVec];
+  if (c * kTkCtaCols + (warp + 1) * kTkWarpCols <= N) {
+#pragma unroll
+    for (int i = 0; i < kTkVec; ++i)  // all loads in flight at once
+      q[i] = __ldcs(reinterpret_cast<const float4 *>(row + base + 128 * i));
+  } else {
+#pragma unroll
+    for (int i = 0; i < kTkVec; ++i) {
+      const int col = base + 128 * i;
+      q[i].x = col < N ? __ldcs(row + col) : 0.0f;
+      q[i].y = col + 1 < N ? __ldcs(row + col + 1) : 0.0f;
+      q[i].z = col + 2 < N ? __ldcs(row + col + 2) : 0.0f;
+      q[i].w = col + 3 < N ? __ldcs(row + col + 3) : 0.0f;
+    }
+  }
+  bool bad = false;
+  uint64_t keys[4 * kTkVec];
+  uint64_t mk = 0ull;
+#pragma unroll
+  for (int i = 0; i < kTkVec; ++i) {
+    const float v[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int col = base + 128 * i + e;
+      keys[4 * i + e] = 0ull;
+      if (col < N) {
+        bad |= !isfinite(v[e]);
+        keys[4 * i + e] = cand_key(v[e], static_cast<uint32_t>(col));
+        mk = kmax(mk, keys[4 * i + e]);
+      }
+    }
+  }
+  // the floor: the lane maximum ranked 15th (0 when fewer than 16 lanes
+  // hold columns; zero maxima all rank after the real ones)
+  S.lane_max[warp][lane] = mk;
+  if (lane == 0) S.floor_key[warp] = 0ull;
+  __syncwarp();
+  if (mk != 0ull && rank_in(S.lane_max[warp], 32, mk) == kRun - 1) S.floor_key[warp] = mk;
+  __syncwarp();
+  const uint64_t fl = S.floor_key[warp];
+  uint32_t mask = 0u;
+#pragma unroll
+  for (int i = 0; i < 4 * kTkVec; ++i)
+    if (keys[i] != 0ull && keys[i] >= fl) mask |= 1u << i;
+  const int n = warp_append(S, warp, lane, 0, keys, mask);
+  warp_rank_top(S, warp, lane, n);
+  bad = __syncthreads_or(bad);
+  cta_rank_top(S);
+  if (threadIdx.x < kRun)
+    runs[(static_cast<size_t>(t) * n_cta + c) * kRun + threadIdx.x] =
+        bad ? kInvalidKey : S.out[threadIdx.x];
+}
+
+// Phase 2: one CTA per row folds the row's n_lists lists into the best k.
+// PAIRS = false: runs of 16 sorted keys from phase 1; the values are read
+// back from the row (so a selected -0.0 comes back as -0.0).  PAIRS = true:
+// caller lists of k (id, value) pairs in any order; the values are copied
+// from the entry whose id was selected.  The best k-th key of any list
+// bounds the row's k-th best from below; only keys at or above it are
+// candidates.  Each warp takes 32 lists per pass and keeps its best 16.
+template <bool PAIRS>
+__global__ void __launch_bounds__(kTkThreads) topk_merge_kernel(
+    const uint64_t *__restrict__ runs, const int32_t *__restrict__ in_ids,
+    const float *__restrict__ in_vals, int n_lists, int k, const float *__restrict__ logits,
+    int ld, int N, int32_t *__restrict__ ids_out, float *__restrict__ vals_out,
+    uint32_t *status) {
+  __shared__ TopkSmem S;
+  __shared__ int32_t s_ids[kRun];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  const size_t row0 = static_cast<size_t>(t) * n_lists;
+  // a list's keys (0 past its end), its k-th best, and whether it is valid
+  auto load_list = [&](int j, uint64_t (&b)[kRun], bool &bad_list) -> uint64_t {
+#pragma unroll
+    for (int i = 0; i < kRun; ++i) b[i] = 0ull;
+    bad_list = false;
+    if (j >= n_lists) return 0ull;
+    if (!PAIRS) {
+      const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(runs + (row0 + j) * kRun);
+#pragma unroll
+      for (int i = 0; i < kRun; i += 2) {
+        const ulonglong2 u = __ldcg(src + i / 2);
+        b[i] = u.x;
+        b[i + 1] = u.y;
+      }
+      bad_list = b[0] == kInvalidKey;
+      uint64_t kth = 0ull;
+#pragma unroll
+      for (int i = 0; i < kRun; ++i)
+        if (i == k - 1) kth = b[i];
+      return kth;
+    }
+    const size_t o = (row0 + j) * k;
+    uint64_t lo = ~0ull;
+#pragma unroll
+    for (int i = 0; i < kRun; ++i)
+      if (i < k) {
+        const int32_t id = in_ids[o + i];
+        bad_list |= id < 0;
+        b[i] = cand_key(in_vals[o + i], static_cast<uint32_t>(id));
+        lo = b[i] < lo ? b[i] : lo;
+      }
+    return lo;  // k entries: the smallest is the list's k-th best
+  };
+  uint64_t fl = 0ull;
+  bool bad = false;
+  for (int j = threadIdx.x; j < n_lists; j += kTkThreads) {
+    uint64_t b[kRun];
+    bool bl;
+    fl = kmax(fl, load_list(j, b, bl));
+    bad |= bl;
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) fl = kmax(fl, __shfl_xor_sync(0xFFFFFFFFu, fl, m));
+  if (lane == 0) S.floor_key[warp] = fl;
+  if (lane < kRun) S.top[warp][lane] = 0ull;
+  bad = __syncthreads_or(bad);
+  fl = 0ull;
+#pragma unroll
+  for (int w = 0; w < kTkWarps; ++w) fl = kmax(fl, S.floor_key[w]);
+  if (!bad) {
+    for (int j0 = warp * 32; j0 < n_lists; j0 += kTkThreads) {
+      uint64_t b[kRun];
+      bool bl;
+      load_list(j0 + lane, b, bl);
+      uint32_t mask = 0u;
+#pragma unroll
+      for (int i = 0; i < kRun; ++i)
+        if (b[i] != 0ull && b[i] >= fl) mask |= 1u << i;
+      // the running best 16 first, then this pass's candidates
+      __syncwarp();
+      if (lane < kRun) S.cand[warp][lane] = S.top[warp][lane];
+      const int n = warp_append(S, warp, lane, kRun, b, mask);
+      warp_rank_top(S, warp, lane, n);
+    }
+  }
+  __syncthreads();
+  cta_rank_top(S);
+  if (warp == 0) {
+    const uint64_t r = lane < kRun ? S.out[lane] : 0ull;
+    if (lane < k) {
+      const int32_t id = bad ? -1 : cand_id(r);
+      ids_out[static_cast<size_t>(t) * k + lane] = id;
+      // N >= k real keys reach every row's best k, so the id is a column of
+      // the row; the bound is checked all the same before the read
+      if (!PAIRS)
+        vals_out[static_cast<size_t>(t) * k + lane] =
+            (id >= 0 && id < N) ? __ldcs(logits + static_cast<size_t>(t) * ld + id) : 0.0f;
+      else if (bad)
+        vals_out[static_cast<size_t>(t) * k + lane] = 0.0f;
+      s_ids[lane] = id;
+    }
+    if (bad && lane == 0) set_status(status, MOE_DEV_NONFINITE);
+  }
+  if (PAIRS && !bad) {
+    __syncthreads();
+    // ids within a row are distinct, so exactly one entry matches each slot
+    const size_t o = row0 * k;
+    for (int e = threadIdx.x; e < n_lists * k; e += kTkThreads) {
+      const int32_t id = in_ids[o + e];
+      for (int j = 0; j < k; ++j)
+        if (s_ids[j] == id) vals_out[static_cast<size_t>(t) * k + j] = in_vals[o + e];
+    }
+  }
+}
+
+}  // namespace
+
+int topk_chunks(int N) { return (N + kTkCtaCols - 1) / kTkCtaCols; }
+
+cudaError_t launch_topk(const float *logits, int T, int ld, int N, int k, int32_t *ids,
+                        float *values, uint64_t *runs, uint32_t *status, cudaStream_t s) {
+  const int n_cta = topk_chunks(N);
+  topk_chunk_kernel<<<T * n_cta, kTkThreads, 0, s>>>(logits, ld, N, n_cta, runs);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<false><<<T, kTkThreads, 0, s>>>(runs, nullptr, nullptr, n_cta, k, logits,
+                                                    ld, N, ids, values, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_merge(const int32_t *ids, const float *values, int T, int n_lists,
+                              int k, int32_t *ids_out, float *values_out, uint32_t *status,
+                              cudaStream_t s) {
+  topk_merge_kernel<true><<<T, kTkThreads, 0, s>>>(nullptr, ids, values, n_lists, k, nullptr, 0,
+                                                   0, ids_out, values_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

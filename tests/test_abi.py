@@ -110,3 +110,34 @@ def test_product_package_does_not_import_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in src and "moe_oracle" not in src, fn
+
+
+def test_topk_host_checks(moe):
+    L = moe.lib()
+    fake = 1 << 20  # aligned fake addresses are never dereferenced on these paths
+    ws = moe.moe_topk_workspace_bytes(8, 151936)
+    assert ws == 256 + ((8 * 19 * 16 * 8 + 255) // 256) * 256
+    assert moe.moe_topk_workspace_bytes(8, (1 << 24) + 1) == 0
+    assert moe.moe_topk_workspace_bytes(-1, 100) == 0
+
+    def cand(T=8, ld=151936, N=151936, k=16, ws_bytes=ws, logits=fake):
+        return L.moe_topk_candidates(logits, T, ld, N, k, fake, fake, fake, ws_bytes, None)
+
+    assert cand(T=0) == moe.MOE_OK
+    assert cand(k=0) == moe.MOE_ERR_INVALID_ARG
+    assert cand(k=17) == moe.MOE_ERR_UNSUPPORTED
+    assert cand(N=10, ld=12, k=11) == moe.MOE_ERR_INVALID_ARG
+    assert cand(ld=151932) == moe.MOE_ERR_INVALID_ARG
+    assert cand(ld=151937) == moe.MOE_ERR_INVALID_ARG  # ld not a multiple of 4
+    assert cand(logits=fake + 4) == moe.MOE_ERR_INVALID_ARG
+    assert cand(ws_bytes=ws - 1) == moe.MOE_ERR_WORKSPACE
+    assert cand(N=(1 << 24) + 4, ld=(1 << 24) + 4) == moe.MOE_ERR_UNSUPPORTED
+
+    def merge(T=8, n_lists=2, k=16, ws_bytes=256):
+        return L.moe_topk_merge(fake, fake, T, n_lists, k, fake, fake, fake, ws_bytes, None)
+
+    assert merge(T=0) == moe.MOE_OK
+    assert merge(n_lists=0) == moe.MOE_ERR_INVALID_ARG
+    assert merge(k=17) == moe.MOE_ERR_UNSUPPORTED
+    assert merge(n_lists=65537) == moe.MOE_ERR_UNSUPPORTED
+    assert merge(ws_bytes=255) == moe.MOE_ERR_WORKSPACE
