@@ -231,7 +231,7 @@ moe_status moe_block_forward_noalloc(const moe_dims *dims, const moe_weights *w,
  * logits[t][ids[t][j]] (bit for bit).  k <= N <= 2^24.  A row holding NaN
  * or +-inf gets ids -1 and values 0 and sets MOE_DEV_NONFINITE.  The
  * workspace (moe_topk_workspace_bytes) holds the status word and one run of
- * 16 keys per 8192 columns of each row.  ids [T][k] int32, values [T][k]. */
+ * 16 keys per 1024 columns of each row.  ids [T][k] int32, values [T][k]. */
 size_t moe_topk_workspace_bytes(int T, int N);
 moe_status moe_topk_candidates(const float *logits, int T, int ld, int N, int k,
                                int32_t *ids, float *values, void *workspace,

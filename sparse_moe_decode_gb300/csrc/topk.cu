@@ -17,15 +17,19 @@
 // order-preserving (-0 first mapped to +0), the low word the complement of
 // the index, so a lower index gives a larger key.  Key 0 is below every real
 // key and pads short runs.
-//   phase 1 (topk_chunk_kernel): one CTA per 8192 columns of a row; each lane
-//     streams 32 values (eight coalesced 16-byte loads, all in flight at
-//     once), sorts two runs of 16 with a bitonic network in registers and
-//     merges them; five xor-shuffle levels merge the warp's 32 runs; warp 0
-//     merges the CTA's 8 warp runs from shared memory and writes one sorted
-//     run of 16 keys per CTA.  HBM-bound: each logit is read once.
-//   phase 2 (topk_merge_kernel): one CTA per row; lanes fold the row's runs
-//     in, warps merge by shuffles, warp 0 merges the warp runs and writes the
-//     first k.  The same kernel merges caller lists of (id, value) pairs.
+//   phase 1 (topk_chunk_kernel): one warp per 1024 columns of a row; each
+//     lane streams 32 values (eight coalesced 16-byte loads, all in flight at
+//     once) and keeps their order-preserving 32-bit images.  The lane maxima
+//     give a floor (the 16th best of them), the keys at or above it are
+//     appended to the warp's candidate list in shared memory, and each
+//     candidate's rank is the number of larger candidates; ranks 0..15 are
+//     the chunk's best 16, written as one sorted run.  No barrier spans
+//     warps; each logit is read once (HBM-bound).
+//   phase 2 (topk_merge_kernel): one CTA per row; the best k-th key of any
+//     run is a floor for the row, warps append the keys at or above it (32
+//     runs per pass) and rank them, and the CTA ranks the warps' best 16 to
+//     give the first k.  The same kernel merges caller lists of (id, value)
+//     pairs.
 // A row holding NaN or +-inf is a precondition violation, as for the MoE
 // selector: its ids are -1, its values 0, and MOE_DEV_NONFINITE is set.
 #include "common.cuh"
@@ -39,7 +43,6 @@ constexpr int kTkThreads = 256;                       // 8 warps
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkVec = 8;                             // 16-byte loads per lane
 constexpr int kTkWarpCols = 32 * 4 * kTkVec;          // 1024 columns per warp
-constexpr int kTkCtaCols = kTkWarps * kTkWarpCols;    // 8192 columns per CTA
 // The run written for a chunk that held a non-finite value (or folded in for
 // a caller list with a negative id): every real key has a low word >= 2^31
 // (indices < 2^31), so key 1 is never a real entry.
@@ -131,22 +134,25 @@ __device__ __forceinline__ void cta_rank_top(TopkSmem &S) {
   __syncthreads();
 }
 
-// Phase 1: the sorted best 16 keys of each 8192-column chunk of each row.
-// Block b covers row b / n_cta, columns (b % n_cta) * 8192 ...; warp w the
-// 1024 columns from there + 1024 w; lane l the float4 at l + 32 i of them.
-// The 16th best of the warp's 32 lane maxima bounds the warp's 16th best
-// from below (16 lanes each hold a key at least that large), so only keys
-// at or above it are candidates, and only the 16 lanes whose maxima reach
-// it hold any.
-__global__ void __launch_bounds__(kTkThreads) topk_chunk_kernel(
-    const float *__restrict__ logits, int ld, int N, int n_cta, uint64_t *__restrict__ runs) {
+// Phase 1: the sorted best 16 keys of each 1024-column chunk of each row,
+// one warp per chunk and no barrier across warps.  Warp g of the grid takes
+// row g / n_wc, columns (g % n_wc) * 1024 ...; lane l the float4 at l + 32 i
+// of them.  The 16th best of the warp's 32 lane maxima bounds the chunk's
+// 16th best from below (16 lanes each hold a key at least that large), so
+// only keys at or above it are candidates, and only the 16 lanes whose
+// maxima reach it hold any (at most 512 candidates).
+__global__ void __launch_bounds__(kTkThreads, 4) topk_chunk_kernel(
+    const float *__restrict__ logits, int ld, int N, int n_wc, int n_warps,
+    uint64_t *__restrict__ runs) {
   __shared__ TopkSmem S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x / n_cta, c = blockIdx.x - t * n_cta;
+  const int g = blockIdx.x * kTkWarps + warp;
+  if (g >= n_warps) return;  // whole warps only: nothing below syncs the CTA
+  const int t = g / n_wc, c = g - t * n_wc;
   const float *row = logits + static_cast<size_t>(t) * ld;
-  const int base = c * kTkCtaCols + warp * kTkWarpCols + 4 * lane;
+  const int base = c * kTkWarpCols + 4 * lane;
   float4 q[kTkVec];
-  if (c * kTkCtaCols + (warp + 1) * kTkWarpCols <= N) {
+  if ((c + 1) * kTkWarpCols <= N) {
 #pragma unroll
     for (int i = 0; i < kTkVec; ++i)  // all loads in flight at once
       q[i] = __ldcs(reinterpret_cast<const float4 *>(row + base + 128 * i));
@@ -160,23 +166,38 @@ __global__ void __launch_bounds__(kTkThreads) topk_chunk_kernel(
       q[i].w = col + 3 < N ? __ldcs(row + col + 3) : 0.0f;
     }
   }
-  bool bad = false;
-  uint64_t keys[4 * kTkVec];
-  uint64_t mk = 0ull;
+  // order-preserving 32-bit images of the values (-0 lifted onto +0, its
+  // neighbour in this order); a key is (image, ~column)
+  uint32_t o[4 * kTkVec];
+  uint32_t expo = 0u, mo = 0u;
+  int first = -1;
 #pragma unroll
   for (int i = 0; i < kTkVec; ++i) {
     const float v[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int col = base + 128 * i + e;
-      keys[4 * i + e] = 0ull;
-      if (col < N) {
-        bad |= !isfinite(v[e]);
-        keys[4 * i + e] = cand_key(v[e], static_cast<uint32_t>(col));
-        mk = kmax(mk, keys[4 * i + e]);
-      }
+      const uint32_t u = __float_as_uint(v[e]);
+      expo = max(expo, u & 0x7F800000u);  // columns past N were loaded as +0
+      uint32_t w = u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+      w += w == 0x7FFFFFFFu;
+      o[4 * i + e] = w;
     }
   }
+  if ((c + 1) * kTkWarpCols > N) {
+#pragma unroll
+    for (int i = 0; i < 4 * kTkVec; ++i)  // 0: below the image of any value (-inf's is 0x007FFFFF)
+      if (base + 128 * (i / 4) + (i % 4) >= N) o[i] = 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < 4 * kTkVec; ++i) mo = max(mo, o[i]);
+  bool bad = expo == 0x7F800000u;  // an in-range NaN or +-inf
+  // the lane's best key: its largest image at its lowest column holding it
+#pragma unroll
+  for (int i = 4 * kTkVec - 1; i >= 0; --i)
+    if (o[i] == mo) first = i;
+  const uint64_t mk = mo == 0u ? 0ull
+      : (static_cast<uint64_t>(mo) << 32) |
+            static_cast<uint32_t>(~static_cast<uint32_t>(base + 128 * (first / 4) + (first % 4)));
   // the floor: the lane maximum ranked 15th (0 when fewer than 16 lanes
   // hold columns; zero maxima all rank after the real ones)
   S.lane_max[warp][lane] = mk;
@@ -185,17 +206,35 @@ __global__ void __launch_bounds__(kTkThreads) topk_chunk_kernel(
   if (mk != 0ull && rank_in(S.lane_max[warp], 32, mk) == kRun - 1) S.floor_key[warp] = mk;
   __syncwarp();
   const uint64_t fl = S.floor_key[warp];
+  const uint32_t fo = static_cast<uint32_t>(fl >> 32);
+  const int fcol = static_cast<int>(~static_cast<uint32_t>(fl));  // -1 when fl == 0
+  // candidates: key >= floor, i.e. a larger image, or the same image at a
+  // column no higher than the floor's
   uint32_t mask = 0u;
 #pragma unroll
+  for (int i = 0; i < 4 * kTkVec; ++i) {
+    const int col = base + 128 * (i / 4) + (i % 4);
+    if (o[i] != 0u && (o[i] > fo || (o[i] == fo && (fl == 0ull || col <= fcol)))) mask |= 1u << i;
+  }
+  // append the candidates' keys to the warp's list
+  const int cnt = __popc(mask);
+  int incl = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  const int n = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  int off = incl - cnt;
+#pragma unroll
   for (int i = 0; i < 4 * kTkVec; ++i)
-    if (keys[i] != 0ull && keys[i] >= fl) mask |= 1u << i;
-  const int n = warp_append(S, warp, lane, 0, keys, mask);
+    if ((mask >> i) & 1u)
+      S.cand[warp][off++] = (static_cast<uint64_t>(o[i]) << 32) |
+                            static_cast<uint32_t>(~static_cast<uint32_t>(base + 128 * (i / 4) + (i % 4)));
   warp_rank_top(S, warp, lane, n);
-  bad = __syncthreads_or(bad);
-  cta_rank_top(S);
-  if (threadIdx.x < kRun)
-    runs[(static_cast<size_t>(t) * n_cta + c) * kRun + threadIdx.x] =
-        bad ? kInvalidKey : S.out[threadIdx.x];
+  bad = __any_sync(0xFFFFFFFFu, bad);
+  if (lane < kRun)
+    runs[(static_cast<size_t>(t) * n_wc + c) * kRun + lane] = bad ? kInvalidKey : S.top[warp][lane];
 }
 
 // Phase 2: one CTA per row folds the row's n_lists lists into the best k.
@@ -203,8 +242,9 @@ __global__ void __launch_bounds__(kTkThreads) topk_chunk_kernel(
 // back from the row (so a selected -0.0 comes back as -0.0).  PAIRS = true:
 // caller lists of k (id, value) pairs in any order; the values are copied
 // from the entry whose id was selected.  The best k-th key of any list
-// bounds the row's k-th best from below; only keys at or above it are
-// candidates.  Each warp takes 32 lists per pass and keeps its best 16.
+// bounds the row's k-th best from below, and so does the k-th best head of
+// any 32 lists; only keys at or above the larger floor are candidates.  Each
+// warp takes 32 lists per pass and keeps its best 16.
 template <bool PAIRS>
 __global__ void __launch_bounds__(kTkThreads) topk_merge_kernel(
     const uint64_t *__restrict__ runs, const int32_t *__restrict__ in_ids,
@@ -249,13 +289,23 @@ __global__ void __launch_bounds__(kTkThreads) topk_merge_kernel(
       }
     return lo;  // k entries: the smallest is the list's k-th best
   };
+  // Two floors, both at most the row's k-th best: a list's k-th best key,
+  // and the k-th best of the heads (best keys) of 32 lists, since k lists
+  // each hold a key at least that large.  The larger of all is used.
   uint64_t fl = 0ull;
   bool bad = false;
-  for (int j = threadIdx.x; j < n_lists; j += kTkThreads) {
+  for (int j0 = warp * 32; j0 < n_lists; j0 += kTkThreads) {
     uint64_t b[kRun];
     bool bl;
-    fl = kmax(fl, load_list(j, b, bl));
+    fl = kmax(fl, load_list(j0 + lane, b, bl));
     bad |= bl;
+    uint64_t head = 0ull;
+#pragma unroll
+    for (int i = 0; i < kRun; ++i) head = kmax(head, b[i]);
+    __syncwarp();
+    S.lane_max[warp][lane] = head;
+    __syncwarp();
+    if (head != 0ull && rank_in(S.lane_max[warp], 32, head) == k - 1) fl = kmax(fl, head);
   }
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) fl = kmax(fl, __shfl_xor_sync(0xFFFFFFFFu, fl, m));
@@ -313,15 +363,17 @@ __global__ void __launch_bounds__(kTkThreads) topk_merge_kernel(
 
 }  // namespace
 
-int topk_chunks(int N) { return (N + kTkCtaCols - 1) / kTkCtaCols; }
+int topk_chunks(int N) { return (N + kTkWarpCols - 1) / kTkWarpCols; }
 
 cudaError_t launch_topk(const float *logits, int T, int ld, int N, int k, int32_t *ids,
                         float *values, uint64_t *runs, uint32_t *status, cudaStream_t s) {
-  const int n_cta = topk_chunks(N);
-  topk_chunk_kernel<<<T * n_cta, kTkThreads, 0, s>>>(logits, ld, N, n_cta, runs);
+  const int n_wc = topk_chunks(N);
+  const int n_warps = T * n_wc;
+  topk_chunk_kernel<<<(n_warps + kTkWarps - 1) / kTkWarps, kTkThreads, 0, s>>>(
+      logits, ld, N, n_wc, n_warps, runs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<false><<<T, kTkThreads, 0, s>>>(runs, nullptr, nullptr, n_cta, k, logits,
+  topk_merge_kernel<false><<<T, kTkThreads, 0, s>>>(runs, nullptr, nullptr, n_wc, k, logits,
                                                     ld, N, ids, values, status);
   return cudaGetLastError();
 }

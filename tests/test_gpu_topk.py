@@ -60,7 +60,7 @@ def check(env, rows, k, ld=None):
     return ids, vals
 
 
-# widths around the 1024-column warp and 8192-column CTA chunks, ragged tails
+# widths around the 1024-column warp chunks and the 8-warp CTA, ragged tails
 @pytest.mark.parametrize("N", [16, 100, 1023, 1024, 1025, 8191, 8192, 8193, 20011, 65536 + 12])
 @pytest.mark.parametrize("k", [1, 8, 9, 13, 16])
 def test_candidates_match_oracle(env, N, k):
