@@ -166,21 +166,20 @@ __global__ void __launch_bounds__(kTkThreads, 4) topk_chunk_kernel(
       q[i].w = col + 3 < N ? __ldcs(row + col + 3) : 0.0f;
     }
   }
-  // order-preserving 32-bit images of the values (-0 lifted onto +0, its
-  // neighbour in this order); a key is (image, ~column)
+  // order-preserving 32-bit images of the values; adding +0 first turns -0
+  // into +0 (the two tie), and leaves every other value as it is
   uint32_t o[4 * kTkVec];
-  uint32_t expo = 0u, mo = 0u;
+  uint32_t mo = 0u, mn = ~0u;
   int first = -1;
 #pragma unroll
   for (int i = 0; i < kTkVec; ++i) {
     const float v[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t u = __float_as_uint(v[e]);
-      expo = max(expo, u & 0x7F800000u);  // columns past N were loaded as +0
-      uint32_t w = u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
-      w += w == 0x7FFFFFFFu;
+      const uint32_t u = __float_as_uint(v[e] + 0.0f);
+      const uint32_t w = u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
       o[4 * i + e] = w;
+      mn = min(mn, w);  // columns past N were loaded as +0: finite
     }
   }
   if ((c + 1) * kTkWarpCols > N) {
@@ -190,7 +189,8 @@ __global__ void __launch_bounds__(kTkThreads, 4) topk_chunk_kernel(
   }
 #pragma unroll
   for (int i = 0; i < 4 * kTkVec; ++i) mo = max(mo, o[i]);
-  bool bad = expo == 0x7F800000u;  // an in-range NaN or +-inf
+  // NaN and +-inf are the images at or above +inf's and at or below -inf's
+  bool bad = mo >= 0xFF800000u || mn <= 0x007FFFFFu;
   // the lane's best key: its largest image at its lowest column holding it
 #pragma unroll
   for (int i = 4 * kTkVec - 1; i >= 0; --i)
@@ -210,12 +210,13 @@ __global__ void __launch_bounds__(kTkThreads, 4) topk_chunk_kernel(
   const int fcol = static_cast<int>(~static_cast<uint32_t>(fl));  // -1 when fl == 0
   // candidates: key >= floor, i.e. a larger image, or the same image at a
   // column no higher than the floor's
+  // (with no floor, fo = 0 and fcol = -1: every image above 0, i.e. every
+  // column below N, passes)
+  const int dcol = fcol - base;
   uint32_t mask = 0u;
 #pragma unroll
-  for (int i = 0; i < 4 * kTkVec; ++i) {
-    const int col = base + 128 * (i / 4) + (i % 4);
-    if (o[i] != 0u && (o[i] > fo || (o[i] == fo && (fl == 0ull || col <= fcol)))) mask |= 1u << i;
-  }
+  for (int i = 0; i < 4 * kTkVec; ++i)
+    if (o[i] > fo || (o[i] == fo && 128 * (i / 4) + (i % 4) <= dcol)) mask |= 1u << i;
   // append the candidates' keys to the warp's list
   const int cnt = __popc(mask);
   int incl = cnt;
