@@ -389,6 +389,27 @@ def bench_candidates(moe, torch, dev, T: int, steps: int, warmup: int, peak_gbs:
             "kernels_per_call": 2, "l2": "cold: %d rotating inputs of %.1f MB" % (R, T * row_bytes / 1e6)}
 
 
+def candidates_main(args, rank: int):
+    """--workload candidates: the top-16 candidate selector alone (replicas
+    on several GPUs, like the block)."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    import sparse_moe_decode_gb300 as moe
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    r = bench_candidates(moe, torch, dev, args.cand_T, args.steps, args.warmup, pk["hbm_gbs"])
+    if rank == 0:
+        print(json.dumps({"metric": "candidate_rows_per_s", "value": r["rows_per_s"],
+                          "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": r["us_per_call"] * 1e-3,
+                          "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+                          "config": {"workload": "candidates_T%d_N%d_k%d" % (
+                              r["T"], r["N"], r["k"]), "l2": r["l2"]},
+                          "candidates": r}))
+
+
 def _oracle_inputs(name: str, n: int):
     wl = W.WORKLOADS[name]
     w = W.make_weights(wl.dims, wl.seed)
@@ -461,7 +482,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOAD_T), default="verify")
+    ap.add_argument("--workload", choices=list(WORKLOAD_T) + ["candidates"], default="verify",
+                    help="'candidates': only the top-16 candidate selector, one JSON line")
+    ap.add_argument("--cand-T", type=int, default=W.CANDIDATES_T,
+                    help="rows of the candidate selector for --workload candidates")
     ap.add_argument("--only", action="store_true", help="time only --workload")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--banks", type=int, default=0,
@@ -473,6 +497,13 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.workload == "candidates":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the candidate selector has "
+                              "no reference arm; its oracle is timed only in the tests"}))
+            return
+        return candidates_main(args, rank)
 
     if args.impl == "reference":
         # the oracle is the reference arm: rank 0 only, host cores
