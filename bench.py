@@ -182,6 +182,25 @@ MEASURED_TRAFFIC = {
 }
 
 
+# The candidate selector's first kernel, captured at 64 rows (the runs it
+# writes stay in L2; the merge kernel reads them there): DRAM bytes per row.
+CANDIDATES_TRAFFIC = {"bytes_per_row": 38.92e6 / 64, "rows_captured": 64,
+                      "sources": ["topk.cu", "common.cuh"], "sha256_16": "3b6ce43ced0d7065",
+                      "profile": "profiles/topk_chunk_candidates_T64.md"}
+
+
+def candidates_traffic(T: int):
+    """DRAM bytes of one candidate-selection call of T rows, from the capture
+    at 64 rows scaled by rows (each row is read once), or None when the
+    kernel's sources changed since."""
+    m = CANDIDATES_TRAFFIC
+    h = hashlib.sha256()
+    for f in m["sources"]:
+        with open(os.path.join(HERE, "sparse_moe_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return m["bytes_per_row"] * T if h.hexdigest()[:16] == m["sha256_16"] else None
+
+
 def measured_traffic(kname: str, workload: str):
     """The captured traffic of kname on this workload, or None when there is
     no capture or the kernel's sources changed since it was taken."""
@@ -401,13 +420,20 @@ def candidates_main(args, rank: int):
     pk = peaks()
     r = bench_candidates(moe, torch, dev, args.cand_T, args.steps, args.warmup, pk["hbm_gbs"])
     if rank == 0:
+        cb = oracle_candidates(args.cand_T, budget_s=args.cpu_budget)
         print(json.dumps({"metric": "candidate_rows_per_s", "value": r["rows_per_s"],
                           "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
                           "warmup": args.warmup, "ms_per_step": r["us_per_call"] * 1e-3,
                           "higher_is_better": True, "dtype": "f32", "data": "synthetic",
                           "config": {"workload": "candidates_T%d_N%d_k%d" % (
                               r["T"], r["N"], r["k"]), "l2": r["l2"]},
-                          "candidates": r}))
+                          "roofline": {"bound": "hbm", "kernel": "topk_chunk + topk_merge",
+                                       "achieved": r["achieved_gbs"], "peak": pk["hbm_gbs"],
+                                       "unit": "GB/s", "frac": r["frac_hbm_measured"],
+                                       "traffic": candidates_traffic(r["T"]),
+                                       "traffic_src": "ncu capture at 64 rows, scaled by rows",
+                                       "peak_src": pk["src"]},
+                          "cpu_baseline": cb, "candidates": r}))
 
 
 def _oracle_inputs(name: str, n: int):
@@ -445,6 +471,25 @@ def oracle_steps(name: str, steps: int, warmup: int, budget_s: float | None = No
     return {"value": done * cores / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": "%d steps x %d tokens drawn like the %s batch (T=%d) through the fp64 "
                       "oracle, %d threads, %.1f s" % (done, cores, LABEL[name], T, cores, dt)}
+
+
+def oracle_candidates(T: int, budget_s: float = 10.0):
+    """The oracle's top-16 selection (a full sort of each row) on rows of the
+    candidate workload, one row at a time, until the budget is spent."""
+    import oracle
+    rows = W.make_candidate_logits(min(T, 4), W.CANDIDATES_N, seed=500)
+    oracle.candidates_topk(rows[:1], W.CANDIDATES_K)  # builds and loads the library
+    t0 = time.perf_counter()
+    done = 0
+    while done < 1000:
+        oracle.candidates_topk(rows[done % rows.shape[0]][None, :], W.CANDIDATES_K)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": "%d rows of %d fp32 logits, top-%d by a full qsort in the fp64 oracle "
+                      "library, 1 thread, %.1f s" % (done, W.CANDIDATES_N, W.CANDIDATES_K, dt)}
 
 
 def cpu_baseline(name: str, budget_s: float = 10.0):
@@ -500,8 +545,18 @@ def main():
 
     if args.workload == "candidates":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the candidate selector has "
-                              "no reference arm; its oracle is timed only in the tests"}))
+            if rank == 0:
+                cb = oracle_candidates(args.cand_T, budget_s=max(args.cpu_budget, 1.0))
+                print(json.dumps({
+                    "impl": "reference", "metric": "candidate_rows_per_s", "value": cb["value"],
+                    "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+                    "warmup": args.warmup, "ms_per_step": 1e3 / cb["value"],
+                    "higher_is_better": True, "dtype": "f64", "data": "synthetic",
+                    "config": {"workload": "candidates_T%d_N%d_k%d" % (
+                        args.cand_T, W.CANDIDATES_N, W.CANDIDATES_K)},
+                    "cpu_baseline": cb,
+                    "e2e": {"value": cb["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}))
             return
         return candidates_main(args, rank)
 

@@ -57,3 +57,20 @@ def test_single_process_needs_no_collective():
     barrier()
     assert max_all(3.5) == 3.5
     assert abs(bench.whole_job_tokens_per_s(1, 1, 0.025) - 40000.0) < 1e-6
+
+
+def test_candidates_reference_arm_times_the_oracle():
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--workload", "candidates", "--cand-T", "2", "--cpu-budget", "1",
+                          "--steps", "2", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=300, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == "candidate_rows_per_s"
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "candidates_T2_N151936_k16"
