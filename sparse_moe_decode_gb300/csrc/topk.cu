@@ -61,8 +61,9 @@ __device__ __forceinline__ int32_t cand_id(uint64_t k) {
 
 __device__ __forceinline__ uint64_t kmax(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
-// Candidate space of one warp: at most 16 lanes (or lists) reach the floor,
-// with 32 (or 16) keys each, after the warp's running best 16.
+// Candidate space of one warp: 512 keys (in phase 1 at most 16 lanes reach
+// the floor, with 32 keys each; in phase 2 a pass takes 32 lists of at most
+// 16 keys), after the warp's running best 16.
 constexpr int kTkCand = kRun + 16 * 32;
 
 struct TopkSmem {

@@ -150,3 +150,27 @@ def test_merge_sentinel_rows(env):
     ri, rv, bad = oracle.merge_topk(li, lv, 16)
     assert bad == 1 and st == env[0].DEV_NONFINITE
     assert np.array_equal(mi, ri) and same_bits(mv, rv)
+
+
+def test_candidates_widest_row(env):
+    # the largest N the call takes (2^24 columns, one 64 MB row) and a ragged
+    # width just below it
+    for N in (1 << 24, (1 << 24) - 3):
+        rows = W.make_candidate_logits(1, N, seed=12)
+        check(env, rows, 16)
+
+
+@pytest.mark.parametrize("n_lists,k", [(65536, 1), (4096, 16)])
+def test_merge_most_lists(env, n_lists, k):
+    # the largest list count the merge takes, and 4096 lists of 16: lists
+    # of random distinct ids with values from a tie-heavy integer draw
+    T = 2
+    rng = np.random.default_rng(n_lists + k)
+    ids = np.stack([rng.permutation(n_lists * k * 4)[: n_lists * k] for _ in range(T)])
+    vals = rng.integers(-50, 50, size=(T, n_lists * k)).astype(np.float32)
+    li = ids.reshape(T, n_lists, k).astype(np.int32)
+    lv = vals.reshape(T, n_lists, k)
+    mi, mv, st = gpu_merge(env, li, lv)
+    ri, rv, bad = oracle.merge_topk(li, lv, k)
+    assert st == 0 and bad == 0
+    assert np.array_equal(mi, ri) and same_bits(mv, rv)
