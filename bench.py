@@ -185,7 +185,7 @@ MEASURED_TRAFFIC = {
 # The candidate selector's first kernel, captured at 64 rows (the runs it
 # writes stay in L2; the merge kernel reads them there): DRAM bytes per row.
 CANDIDATES_TRAFFIC = {"bytes_per_row": 38.92e6 / 64, "rows_captured": 64,
-                      "sources": ["topk.cu", "common.cuh"], "sha256_16": "5a8f71033c716511",
+                      "sources": ["topk.cu", "common.cuh"], "sha256_16": "976a791dcb403cf7",
                       "profile": "profiles/topk_chunk_candidates_T64.md"}
 
 

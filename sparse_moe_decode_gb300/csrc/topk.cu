@@ -244,9 +244,10 @@ __global__ void __launch_bounds__(kTkThreads, 4) topk_chunk_kernel(
 // back from the row (so a selected -0.0 comes back as -0.0).  PAIRS = true:
 // caller lists of k (id, value) pairs in any order; the values are copied
 // from the entry whose id was selected.  The best k-th key of any list
-// bounds the row's k-th best from below, and so does the k-th best head of
-// any 32 lists; only keys at or above the larger floor are candidates.  Each
-// warp takes 32 lists per pass and keeps its best 16.
+// bounds the row's k-th best from below, and so do the k-th best head of
+// any 32 lists and any k-th best found so far; only keys at or above the
+// largest are candidates.  Each warp takes 32 lists per pass and keeps its
+// best 16; one pass over the lists.
 template <bool PAIRS>
 __global__ void __launch_bounds__(kTkThreads) topk_merge_kernel(
     const uint64_t *__restrict__ runs, const int32_t *__restrict__ in_ids,
@@ -291,15 +292,16 @@ __global__ void __launch_bounds__(kTkThreads) topk_merge_kernel(
       }
     return lo;  // k entries: the smallest is the list's k-th best
   };
-  // Two floors, both at most the row's k-th best: a list's k-th best key,
-  // and the k-th best of the heads (best keys) of 32 lists, since k lists
-  // each hold a key at least that large.  The larger of all is used.
-  uint64_t fl = 0ull;
+  // One pass: each warp takes 32 lists at a time.  Three floors, each at
+  // most the row's k-th best: a list's k-th best key, the k-th best of the
+  // 32 lists' heads (k lists each hold a key at least that large), and the
+  // warp's running k-th best.  Keys at or above the largest are candidates.
   bool bad = false;
+  if (lane < kRun) S.top[warp][lane] = 0ull;
   for (int j0 = warp * 32; j0 < n_lists; j0 += kTkThreads) {
     uint64_t b[kRun];
     bool bl;
-    fl = kmax(fl, load_list(j0 + lane, b, bl));
+    uint64_t fl = load_list(j0 + lane, b, bl);
     bad |= bl;
     uint64_t head = 0ull;
 #pragma unroll
@@ -308,43 +310,37 @@ __global__ void __launch_bounds__(kTkThreads) topk_merge_kernel(
     S.lane_max[warp][lane] = head;
     __syncwarp();
     if (head != 0ull && rank_in(S.lane_max[warp], 32, head) == k - 1) fl = kmax(fl, head);
-  }
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) fl = kmax(fl, __shfl_xor_sync(0xFFFFFFFFu, fl, m));
-  if (lane == 0) S.floor_key[warp] = fl;
-  if (lane < kRun) S.top[warp][lane] = 0ull;
+    for (int m = 1; m < 32; m <<= 1) fl = kmax(fl, __shfl_xor_sync(0xFFFFFFFFu, fl, m));
+    fl = kmax(fl, S.top[warp][k - 1]);
+    uint32_t mask = 0u;
+#pragma unroll
+    for (int i = 0; i < kRun; ++i)
+      if (b[i] != 0ull && b[i] >= fl) mask |= 1u << i;
+    // the running best 16 first, then this pass's candidates
+    __syncwarp();
+    if (lane < kRun) S.cand[warp][lane] = S.top[warp][lane];
+    const int n = warp_append(S, warp, lane, kRun, b, mask);
+    warp_rank_top(S, warp, lane, n);
+  }
   bad = __syncthreads_or(bad);
-  fl = 0ull;
-#pragma unroll
-  for (int w = 0; w < kTkWarps; ++w) fl = kmax(fl, S.floor_key[w]);
-  if (!bad) {
-    for (int j0 = warp * 32; j0 < n_lists; j0 += kTkThreads) {
-      uint64_t b[kRun];
-      bool bl;
-      load_list(j0 + lane, b, bl);
-      uint32_t mask = 0u;
-#pragma unroll
-      for (int i = 0; i < kRun; ++i)
-        if (b[i] != 0ull && b[i] >= fl) mask |= 1u << i;
-      // the running best 16 first, then this pass's candidates
-      __syncwarp();
-      if (lane < kRun) S.cand[warp][lane] = S.top[warp][lane];
-      const int n = warp_append(S, warp, lane, kRun, b, mask);
-      warp_rank_top(S, warp, lane, n);
-    }
-  }
-  __syncthreads();
   cta_rank_top(S);
   if (warp == 0) {
     const uint64_t r = lane < kRun ? S.out[lane] : 0ull;
     if (lane < k) {
       const int32_t id = bad ? -1 : cand_id(r);
       ids_out[static_cast<size_t>(t) * k + lane] = id;
-      // N >= k real keys reach every row's best k, so the id is a column of
-      // the row; the bound is checked all the same before the read
-      if (!PAIRS)
-        vals_out[static_cast<size_t>(t) * k + lane] =
-            (id >= 0 && id < N) ? __ldcs(logits + static_cast<size_t>(t) * ld + id) : 0.0f;
+      // The value is the key's image inverted; the image is one-to-one but
+      // for -0, which shares +0's, so a selected zero is read back from the
+      // row for its sign.  (N >= k real keys reach every row's best k, so
+      // the id is a column of the row; the bound is checked all the same.)
+      if (!PAIRS) {
+        const uint32_t img = static_cast<uint32_t>(r >> 32);
+        float v = __uint_as_float((img & 0x80000000u) ? (img & 0x7FFFFFFFu) : ~img);
+        if (img == 0x80000000u)
+          v = (id >= 0 && id < N) ? __ldcs(logits + static_cast<size_t>(t) * ld + id) : 0.0f;
+        vals_out[static_cast<size_t>(t) * k + lane] = bad ? 0.0f : v;
+      }
       else if (bad)
         vals_out[static_cast<size_t>(t) * k + lane] = 0.0f;
       s_ids[lane] = id;
