@@ -366,7 +366,8 @@ class Bench:
         return t / steps, 2 * self.T * self.d.H, 2 * self.T * self.d.H
 
 
-def bench_candidates(moe, torch, dev, T: int, steps: int, warmup: int, peak_gbs: float):
+def bench_candidates(moe, torch, dev, T: int, steps: int, warmup: int, peak_gbs: float,
+                     barrier=lambda: None, max_all=lambda v: v, world: int = 1):
     """Wide-row top-16 candidates (the drafter's lm_head candidate selector):
     T rows of the 151,936-wide vocabulary.  R rotating input buffers, more
     than twice L2 in all, captured as R calls in one CUDA graph; per-call
@@ -392,6 +393,7 @@ def bench_candidates(moe, torch, dev, T: int, steps: int, warmup: int, peak_gbs:
         for _ in range(warmup):
             g.replay()
     torch.cuda.synchronize()
+    barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
         e0.record(s)
@@ -399,11 +401,12 @@ def bench_candidates(moe, torch, dev, T: int, steps: int, warmup: int, peak_gbs:
             g.replay()
         e1.record(s)
     torch.cuda.synchronize()
+    barrier()
     assert moe.moe_read_status(ws) == 0
-    us = e0.elapsed_time(e1) * 1e3 / (steps * R)
+    us = max_all(e0.elapsed_time(e1) * 1e3 / (steps * R))
     nbytes = T * row_bytes + T * k * 8
     gbs = nbytes / (us * 1e-6) / 1e9
-    return {"rows_per_s": T / (us * 1e-6), "us_per_call": us, "T": T, "N": N, "k": k,
+    return {"rows_per_s": world * T / (us * 1e-6), "us_per_call": us, "T": T, "N": N, "k": k,
             "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "frac_hbm_measured": gbs / peak_gbs,
             "kernels_per_call": 2, "l2": "cold: %d rotating inputs of %.1f MB" % (R, T * row_bytes / 1e6)}
 
@@ -415,14 +418,22 @@ def candidates_main(args, rank: int):
     import __graft_entry__ as g
     g.build()
     import sparse_moe_decode_gb300 as moe
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    barrier, max_all = collectives(dist, dev)
     pk = peaks()
-    r = bench_candidates(moe, torch, dev, args.cand_T, args.steps, args.warmup, pk["hbm_gbs"])
+    r = bench_candidates(moe, torch, dev, args.cand_T, args.steps, args.warmup, pk["hbm_gbs"],
+                         barrier, max_all, world)
     if rank == 0:
         cb = oracle_candidates(args.cand_T, budget_s=args.cpu_budget)
         print(json.dumps({"metric": "candidate_rows_per_s", "value": r["rows_per_s"],
-                          "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+                          "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+                          "scaling": "weak",
                           "warmup": args.warmup, "ms_per_step": r["us_per_call"] * 1e-3,
                           "higher_is_better": True, "dtype": "f32", "data": "synthetic",
                           "config": {"workload": "candidates_T%d_N%d_k%d" % (
@@ -648,7 +659,8 @@ def main():
     if not args.only:
         for Tc in (W.CANDIDATES_T, 64):
             results["candidates_T%d_N%d_k%d" % (Tc, W.CANDIDATES_N, W.CANDIDATES_K)] = \
-                bench_candidates(moe, torch, dev, Tc, args.steps, args.warmup, pk["hbm_gbs"])
+                bench_candidates(moe, torch, dev, Tc, args.steps, args.warmup, pk["hbm_gbs"],
+                                 barrier, max_all, world)
     if rank != 0:
         return
     kname, kms, kbytes = head.pop("_kernel")
