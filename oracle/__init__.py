@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_select_topk.restype = i32
             L.oracle_expert_lists.argtypes = [i32, i32, i32, P, P, P, P]
             L.oracle_merge_topk.argtypes = [i32, i32, i32, P, P, P, P]
+            L.oracle_add_rmsnorm.argtypes = [i32, i32, P, P, P, ctypes.c_double, P, P]
             L.oracle_merge_topk.restype = i32
             L.oracle_w8_gemv.argtypes = [i32, i32, i32, P, P, P, P]
             L.oracle_swiglu.argtypes = [i32, P, P, P]
@@ -123,6 +124,23 @@ def select_topk(logits, gate_logit=None, K: int = 8):
     bad = lib().oracle_select_topk(T, E, K, E, _p(logits), _p(g), _p(ids), _p(w),
                                    _p(sg))
     return ids, w, sg, bad
+
+
+def add_rmsnorm(resid_in, block, gamma, eps: float):
+    """Residual add then RMS norm times gamma: resid_out = bf16(resid_in +
+    block) and x_next = bf16(resid_out / sqrt(mean(resid_out^2) + eps) *
+    gamma), per token.  resid_in [T][H] and gamma [H] are bf16 bits, block
+    [T][H] the block's unrounded fp64 output.  Returns (resid_out, x_next)."""
+    resid_in = _c(resid_in, np.uint16)
+    block = _c(block, np.float64)
+    gamma = _c(gamma, np.uint16)
+    T, H = resid_in.shape
+    assert block.shape == (T, H) and gamma.shape == (H,)
+    r_out = np.empty((T, H), np.uint16)
+    x_next = np.empty((T, H), np.uint16)
+    lib().oracle_add_rmsnorm(T, H, _p(resid_in), _p(block), _p(gamma), float(eps), _p(r_out),
+                             _p(x_next))
+    return r_out, x_next
 
 
 def candidates_topk(logits, K: int):

@@ -136,6 +136,25 @@ int oracle_select_topk(int T, int E, int K, int ld, const float *logits,
   return bad;
 }
 
+/* ------------------------------- residual add, RMS norm, weight multiply */
+
+void oracle_add_rmsnorm(int T, int H, const uint16_t *resid_in, const double *block,
+                        const uint16_t *gamma, double eps, uint16_t *resid_out,
+                        uint16_t *x_next) {
+  for (int t = 0; t < T; ++t) {
+    const size_t o = (size_t)t * H;
+    double ss = 0.0;
+    for (int i = 0; i < H; ++i) {
+      resid_out[o + i] = oracle_f64_to_bf16(bf(resid_in[o + i]) + block[o + i]);
+      const double r = bf(resid_out[o + i]);
+      ss += r * r;
+    }
+    const double inv = 1.0 / sqrt(ss / (double)H + eps);
+    for (int i = 0; i < H; ++i)
+      x_next[o + i] = oracle_f64_to_bf16(bf(resid_out[o + i]) * inv * bf(gamma[i]));
+  }
+}
+
 /* ---------------------------------------- candidate lists: exact merge */
 
 int oracle_merge_topk(int T, int n_lists, int K, const int32_t *ids,

@@ -67,6 +67,18 @@ int oracle_select_topk(int T, int E, int K, int ld, const float *logits,
                        const float *gate_logit, int32_t *ids, double *weights,
                        double *sgate);
 
+/* The steps either side of the block (lucebox commit list, the fused
+ * DeltaNet decode kernels entry: an ADD + RMS_NORM + MUL fusion that keeps
+ * the residual sum beside the normalised output).  For each token t, with
+ * block[t] the block's unrounded output:
+ *   resid_out[t][i] = bf16(resid_in[t][i] + block[t][i])   (one rounding)
+ *   ms              = mean over i of resid_out[t][i]^2      (the bf16 values)
+ *   x_next[t][i]    = bf16(resid_out[t][i] / sqrt(ms + eps) * gamma[i])
+ * All in fp64.  resid_in, gamma, resid_out, x_next: bf16 bits. */
+void oracle_add_rmsnorm(int T, int H, const uint16_t *resid_in, const double *block,
+                        const uint16_t *gamma, double eps, uint16_t *resid_out,
+                        uint16_t *x_next);
+
 /* Wide top-k candidates and their exact merge (the candidate selector of
  * the DFlash2 drafter: GPU top-k with at most 16 candidates, lucebox
  * commit list, "candidate selector head"; a vocabulary split across two
