@@ -18,6 +18,10 @@
  *   A5  int8 group-128 expert down projection;
  *   A6  the shared expert (A4 + A5 on every token) scaled by the gate;
  *   A7  weighted combine into a bf16 output row per token.
+ * Beside the block: exact top-k (k <= 16) candidates over wide rows and the
+ * exact merge of per-shard candidate lists (the drafter's candidate
+ * selector: lucebox commit list; ninfer-tp2 v0.4.0, the vocabulary split
+ * with an exact top-16 merge).
  *
  * Conventions (all entry points):
  *   - extern "C", no C++ or CUDA types: device pointers are plain pointers,
