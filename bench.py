@@ -15,7 +15,9 @@ Timing protocol:
     banks touches exceed L2 (129 MB) many times over;
   * each step is one CUDA-graph replay of moe_block_forward; W warm-up steps,
     then exactly K timed steps between CUDA events, barrier + synchronize on
-    both sides, max over ranks;
+    both sides, max over ranks; an event after every step gives the median
+    and minimum step time beside the mean, and five replays on an idle
+    device give the single-call latency (`workloads`);
   * a second timed pass runs the profiled entry point (events between the
     block's kernels) to give the dominant kernel's average duration;
   * e2e: moe_block_forward_host with pinned host x/out, copies inside;
@@ -319,16 +321,34 @@ class Bench:
         with Clocks(clocks_index) as clk:
             torch.cuda.synchronize()
             barrier()
+            step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
             t_wall = time.perf_counter()
             with torch.cuda.stream(s):
                 e0.record(s)
                 for i in range(steps):
                     self.plain[i % self.R].replay()
+                    step_ev[i].record(s)
                 e1.record(s)
             torch.cuda.synchronize()
             t_wall = time.perf_counter() - t_wall
             barrier()
             ms = e0.elapsed_time(e1) / steps
+            per_step = [e0.elapsed_time(step_ev[0])] + [
+                step_ev[i - 1].elapsed_time(step_ev[i]) for i in range(1, steps)]
+            # single-call latency: one replay on an idle device, five times
+            single = []
+            for i in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                with torch.cuda.stream(s):
+                    a.record(s)
+                    self.plain[i % self.R].replay()
+                    b.record(s)
+                torch.cuda.synchronize()
+                single.append(a.elapsed_time(b))
+            self.step_stats = {"ms_median": float(statistics.median(per_step)),
+                               "ms_min": float(min(per_step)),
+                               "single_call_ms_median": float(statistics.median(single))}
             # profiled pass: the same K steps through the profiled entry point,
             # events between kernels; a bounded sleep kernel first lets the host
             # enqueue every step so kernels run back to back on the device
@@ -640,7 +660,7 @@ def main():
             "frac_roofline_time": max(t_hbm, t_tc) / (ms * 1e-3),
             "kernels_ms": {n: float(v) for n, v in zip(b.kernel_names, per_kernel)},
             "dominant_kernel": b.kernel_names[k_dom], "wall_s": wall, "clocks": clk,
-            "banks": banks,
+            "banks": banks, **b.step_stats,
         }
         if name == args.workload:
             kb = kernel_bytes(b.kernel_names[k_dom], d, T, n_act)
