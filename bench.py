@@ -335,14 +335,17 @@ class Bench:
             ms = e0.elapsed_time(e1) / steps
             per_step = [e0.elapsed_time(step_ev[0])] + [
                 step_ev[i - 1].elapsed_time(step_ev[i]) for i in range(1, steps)]
-            # single-call latency: one replay on an idle device, five times
+            # single-call latency: one replay on an idle device, five times,
+            # each of a bank replayed longest ago (the timed loop's last step
+            # used bank (steps - 1) % R, so bank (steps + i) % R was last read
+            # at least R - 5 steps ago, and L2 holds none of its bytes)
             single = []
             for i in range(5):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 torch.cuda.synchronize()
                 with torch.cuda.stream(s):
                     a.record(s)
-                    self.plain[i % self.R].replay()
+                    self.plain[(steps + i) % self.R].replay()
                     b.record(s)
                 torch.cuda.synchronize()
                 single.append(a.elapsed_time(b))
@@ -476,12 +479,14 @@ def _oracle_inputs(name: str, n: int):
     return wl.dims, w, x
 
 
-def oracle_steps(name: str, steps: int, warmup: int, budget_s: float | None = None):
-    """The oracle as it stands on this host's cores.  One step = `cores`
-    tokens of the workload's recipe through A1..A7 (fp64, one token per
-    thread).  With a budget, the number of steps is cut to fit it."""
+def oracle_steps(name: str, steps: int, warmup: int, budget_s: float | None = None,
+                 threads: int | None = None):
+    """The oracle as it stands on this host's cores (all of them, or
+    `threads`).  One step = `cores` tokens of the workload's recipe through
+    A1..A7 (fp64, one token per thread at a time).  With a budget, the
+    number of steps is cut to fit it."""
     import oracle
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     dims, w, x = _oracle_inputs(name, cores)
     toks = np.arange(cores, dtype=np.int32)
 
@@ -524,7 +529,12 @@ def oracle_candidates(T: int, budget_s: float = 10.0):
 
 
 def cpu_baseline(name: str, budget_s: float = 10.0):
-    return oracle_steps(name, steps=1000, warmup=1, budget_s=budget_s)
+    """The oracle on all host cores, with its one-thread figure beside it."""
+    cb = oracle_steps(name, steps=1000, warmup=1, budget_s=budget_s)
+    one = oracle_steps(name, steps=1000, warmup=0, budget_s=budget_s / 2, threads=1)
+    cb["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1,
+                           "sample": one["sample"]}
+    return cb
 
 
 def collectives(dist, device):

@@ -143,7 +143,10 @@ moe_status moe_build_expert_lists(const int32_t *ids, int T, int E,
  * e = ids[t][j] >= 0: h = bf16(silu(a_gate) * a_up) with a = W13_e x_t, and
  * y[t][j][:] = W2_e h (fp32).  Slot 8 holds the shared expert's output,
  * unscaled by its gate (zeros if shared_inter == 0).  Rows y[t][j] whose id
- * is negative are left unwritten.  y [T][9][H] fp32. */
+ * is negative are left unwritten; an id >= E sets MOE_DEV_BAD_EXPERT and
+ * its row is left unwritten.  y [T][9][H] fp32.  Routes by T as
+ * moe_block_forward does: weight-streaming kernels for T <= 64, the tcgen05
+ * grouped GEMMs (each slot's output stored once, no atomics) from T = 65. */
 moe_status moe_expert_swiglu_w8(const moe_dims *dims, const moe_weights *w,
                                 const moe_bf16 *x, int T, const int32_t *ids,
                                 float *y, void *workspace, size_t ws_bytes,
@@ -207,8 +210,11 @@ const char *moe_block_kernel_name(const moe_dims *dims, int T, int i);
  * pages: this is a packaging variant of the same block.  The caller passes
  * only inputs and outputs; the scratch is a 4 MiB array that the library
  * holds on every GPU that loads it, until the process exits.
- *   - A (dims, T) whose moe_workspace_bytes exceeds 4 MiB is rejected with
- *     MOE_ERR_WORKSPACE (at H = 2048, I = Is = 512 that allows T <= 64).
+ *   - A (dims, T) whose moe_workspace_bytes(dims, T) exceeds 4 MiB is
+ *     rejected with MOE_ERR_WORKSPACE (at H = 2048, I = Is = 512 that
+ *     admits T <= 38; at H = 512, I = Is = 128, T <= 247).
+ *   - Every other check of moe_block_forward (dims, T, weights, x, out) runs
+ *     first: a rejected call enqueues nothing and leaves the array as it was.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any

@@ -51,12 +51,27 @@ def stale() -> bool:
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     if not force and not stale():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    return _build(BUILD, LIB, [], verbose, ptxas_info)
+
+
+def build_variant(name: str, defines: dict) -> str:
+    """A test-only copy of the library compiled with extra -D definitions
+    (e.g. MOE_SABOTAGE), under _build/<name>/; never the product library."""
+    out = os.path.join(BUILD, name)
+    lib = os.path.join(out, "libmoe_gb300_%s.so" % name)
+    if os.path.exists(lib) and all(os.path.getmtime(p) <= os.path.getmtime(lib) for p in _deps()):
+        return lib
+    return _build(out, lib, ["-D%s=%s" % (k, v) for k, v in sorted(defines.items())])
+
+
+def _build(build_dir: str, lib_path: str, defs, verbose: bool = False,
+           ptxas_info: bool = False) -> str:
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + list(defs)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,13 +84,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log.strip():
                 sys.stderr.write(log)
-    tmp = LIB + ".%d.tmp" % os.getpid()
+    tmp = lib_path + ".%d.tmp" % os.getpid()
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

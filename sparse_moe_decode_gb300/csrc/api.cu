@@ -250,6 +250,18 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
 }
 
 }  // namespace
+
+moe_status block_forward_check(const moe_dims *d, const moe_weights *w, const moe_bf16 *x, int T,
+                               const moe_bf16 *out) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_weights(d, w, true, true)) != MOE_OK) return st;
+  if (T > 0 && (!ptr_ok(x) || !ptr_ok(out))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -353,7 +365,6 @@ moe_status moe_expert_swiglu_w8(const moe_dims *dims, const moe_weights *w, cons
   const int H = dims->hidden, I = dims->expert_inter, Is = dims->shared_inter;
   uint32_t *status = at<uint32_t>(workspace, L.status);
   const Lists lists = lists_in(workspace, L);
-  MOE_TRY(launch_lists(ids, T, lists, status, s));
   moe_bf16 *hr = at<moe_bf16>(workspace, L.h_routed);
   moe_bf16 *hs = at<moe_bf16>(workspace, L.h_shared);
   if (Is == 0) {
@@ -361,6 +372,19 @@ moe_status moe_expert_swiglu_w8(const moe_dims *dims, const moe_weights *w, cons
     MOE_TRY(cudaMemset2DAsync(y + static_cast<size_t>(kK) * H, sizeof(float) * (kK + 1) * H, 0,
                               sizeof(float) * H, T, s));
   }
+  if (T >= kTcMinT) {
+    // the tcgen05 grouped GEMMs of the block's prefill route, with the down
+    // kernel storing every slot's unweighted output instead of combining
+    Rec none{nullptr, s};
+    MOE_TRY(launch_expert_counts(ids, T, lists.counts, status, s));
+    MOE_TRY(launch_experts_tc(x, T, H, I, Is, *w, ids, lists, nullptr, nullptr,
+                              at<uint16_t>(workspace, L.xs), at<uint16_t>(workspace, L.x16),
+                              at<float>(workspace, L.xscale), at<float>(workspace, L.hscale), hr,
+                              hs, nullptr, nullptr, at<int4>(workspace, L.items),
+                              at<int>(workspace, L.counters), status, s, none, y));
+    return MOE_OK;
+  }
+  MOE_TRY(launch_lists(ids, T, lists, status, s));
   MOE_TRY(launch_gateup_simt(x, T, H, I, Is, *w, lists, hr, hs, s));
   MOE_TRY(launch_down_simt(T, H, I, Is, *w, lists, hr, hs, y, s));
   return MOE_OK;
@@ -383,16 +407,13 @@ moe_status moe_block_forward(const moe_dims *dims, const moe_weights *w, const m
                              int T, moe_bf16 *out, int32_t *ids_out, float *weights_out,
                              float *logits_out, float *gate_logit_out, void *workspace,
                              size_t ws_bytes, void *stream) {
-  moe_status st = check_dims(dims);
+  moe_status st = block_forward_check(dims, w, x, T, out);
   if (st != MOE_OK) return st;
-  if (T < 0) return MOE_ERR_INVALID_ARG;
-  if (T > kMaxT) return MOE_ERR_UNSUPPORTED;
-  if ((st = check_weights(dims, w, true, true)) != MOE_OK) return st;
   Layout L;
   if ((st = check_ws(dims, T, workspace, ws_bytes, L)) != MOE_OK) return st;
   if (T == 0) return MOE_OK;
-  if (!ptr_ok(x) || !ptr_ok(out) || !opt_ok(ids_out) || !opt_ok(weights_out) ||
-      !opt_ok(logits_out) || !opt_ok(gate_logit_out))
+  if (!opt_ok(ids_out) || !opt_ok(weights_out) || !opt_ok(logits_out) ||
+      !opt_ok(gate_logit_out))
     return MOE_ERR_INVALID_ARG;
   return block_forward_device(dims, w, x, T, out, ids_out, weights_out, logits_out,
                               gate_logit_out, workspace, L, static_cast<cudaStream_t>(stream));

@@ -120,6 +120,21 @@ __device__ __forceinline__ uint4 ld_nc(const void *p) {
   return r;
 }
 
+// Test-only builds.  A library compiled with MOE_SABOTAGE = n (never the
+// product library, which defines nothing) plants one known mistake, so that
+// the parity tests can show that they catch it: 1 moves the 8th selected id
+// to the next expert not already chosen, 2 swaps the softmax weights of
+// ranks 7 and 8 (0-based 6 and 7) without their ids, 3 drops the shared
+// expert's gate, 4 reads the next quantisation group's scale in gate|up.
+#ifndef MOE_SABOTAGE
+#define MOE_SABOTAGE 0
+#endif
+
+// The scale group a gate|up weight in group g (of ng) is dequantised with.
+__device__ __forceinline__ int gateup_scale_group(int g, int ng) {
+  return MOE_SABOTAGE == 4 ? (g + 1) % ng : g;
+}
+
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }

@@ -836,9 +836,10 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
             for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
           }
         }
-        const float slo0 = bf16_to_f32(s_gate[kk / kG]), shi0 = bf16_to_f32(s_up[kk / kG]);
-        const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[kk / kG + 1]) : 0.0f;
-        const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[kk / kG + 1]) : 0.0f;
+        const int g0 = gateup_scale_group(kk / kG, ng), g1 = gateup_scale_group(kk / kG + 1, ng);
+        const float slo0 = bf16_to_f32(s_gate[g0]), shi0 = bf16_to_f32(s_up[g0]);
+        const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[g1]) : 0.0f;
+        const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[g1]) : 0.0f;
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl) {
           if (sl >= ns4) break;

@@ -23,6 +23,11 @@ struct Lists {
   int32_t *active;   // [1+E]: active[0] = number of active experts, then ids
 };
 
+// The host-side checks of a moe_block_forward call other than its
+// workspace and optional outputs (dims, T, weights, x, out); no side effect.
+moe_status block_forward_check(const moe_dims *d, const moe_weights *w, const moe_bf16 *x, int T,
+                               const moe_bf16 *out);
+
 // A1: router GEMV for any T (SIMT, fp32 accumulate).
 cudaError_t launch_router_gemv(const moe_bf16 *x, int T, int H, const moe_bf16 *w_router,
                                const moe_bf16 *w_gate, float *logits, float *gate_logit,
@@ -123,7 +128,10 @@ cudaError_t launch_router_tc(const moe_bf16 *x, int T, int H, const moe_bf16 *w_
 // the tokens' scaled fp16 copies (xs16 [T*K][H] in list order, x16 [T][H],
 // xscale [T]), runs gate|up + SwiGLU (h in bf16), converts h in place to
 // per-row scaled fp16 (2^s of each row in hscale [T*K + T]), runs down + weighted combine into out_acc [T][H] (fp32, zeroed
-// here), then rounds out_acc to bf16.
+// here), then rounds out_acc to bf16.  With y_slots given (per-slot mode),
+// the down kernel instead stores each slot's unweighted fp32 output in
+// y_slots [T][K+1][H] (the shared expert in slot K); out_acc, out, weights
+// and sgate are then unused.
 cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                               const moe_weights &w, const int32_t *ids, const Lists &L,
                               const float *weights,
@@ -131,6 +139,11 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                               float *hscale,
                               moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
                               moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
-                              cudaStream_t s, StageRecorder &rec);
+                              cudaStream_t s, StageRecorder &rec, float *y_slots = nullptr);
+
+// Per-expert entry counts of ids [T][K] into counts [E] (zeroed here); ids
+// >= E set MOE_DEV_BAD_EXPERT.
+cudaError_t launch_expert_counts(const int32_t *ids, int T, int32_t *counts, uint32_t *status,
+                                 cudaStream_t s);
 
 }  // namespace moe

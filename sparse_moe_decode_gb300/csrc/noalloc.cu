@@ -12,6 +12,7 @@
 
 #include <mutex>
 
+#include "kernels.h"
 #include "moe_gb300.h"
 
 namespace {
@@ -46,14 +47,16 @@ moe_status scratch_address(void **out) {
 extern "C" moe_status moe_block_forward_noalloc(const moe_dims *dims, const moe_weights *w,
                                                 const moe_bf16 *x, int T, moe_bf16 *out,
                                                 void *stream) {
-  if (!dims) return MOE_ERR_INVALID_ARG;
+  // every host-side check comes before anything is enqueued: a rejected
+  // call has no side effect
+  moe_status st = moe::block_forward_check(dims, w, x, T, out);
+  if (st != MOE_OK) return st;
   if (T == 0) return MOE_OK;
-  const size_t need = moe_workspace_bytes(dims, T < 0 ? 0 : T);
-  if (T < 0 || need == 0) return T < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+  const size_t need = moe_workspace_bytes(dims, T);
+  if (need == 0) return MOE_ERR_UNSUPPORTED;
   if (need > kScratchBytes) return MOE_ERR_WORKSPACE;
   void *scratch = nullptr;
-  moe_status st = scratch_address(&scratch);
-  if (st != MOE_OK) return st;
+  if ((st = scratch_address(&scratch)) != MOE_OK) return st;
   // The array keeps the previous call's contents; only the device status
   // word (first 256 bytes) must start at zero.  Everything else the block
   // reads is written earlier in the same call.

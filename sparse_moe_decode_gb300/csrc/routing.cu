@@ -177,13 +177,14 @@ cudaError_t launch_select(const float *logits, int T, int ld, const float *gate_
 //
 // Deterministic counting sort of the T*K entries by (expert, t, j) in one
 // CTA.  Pass 1 counts per expert; an exclusive scan gives offsets.  Pass 2
-// walks tokens in chunks of 2048: a per-expert bitmap of the chunk's tokens
-// gives each entry its rank among earlier tokens of the same expert (a
-// token names an expert at most once, so (t) orders entries within an
-// expert), and a running per-expert base carries the count across chunks.
+// walks tokens in chunks of 256: a per-expert bitmap over the chunk's
+// entries (bit t * K + j) gives each entry its rank among earlier entries of
+// the same expert, so that a token naming one expert in two slots still
+// gets two distinct places, and a running per-expert base carries the count
+// across chunks.
 constexpr int kListThreads = 1024;
-constexpr int kListChunk = 2048;               // tokens per chunk
-constexpr int kListWords = kListChunk / 32;    // bitmap words per expert
+constexpr int kListChunk = 256;                     // tokens per chunk
+constexpr int kListWords = kListChunk * kK / 32;    // bitmap words per expert
 constexpr size_t kListSmem = sizeof(uint32_t) * kE * kListWords +   // bitmap
                              sizeof(uint16_t) * kE * kListWords +   // word prefixes
                              sizeof(int16_t) * kListChunk * kK;     // the chunk's ids
@@ -233,7 +234,7 @@ lists_kernel(const int32_t *__restrict__ ids, int T, Lists L, uint32_t *status) 
   __syncthreads();
   for (int t0 = 0; t0 < T; t0 += kListChunk) {
     const int tn = min(kListChunk, T - t0);
-    const int words = (tn + 31) / 32;
+    const int words = (tn * kK + 31) / 32;
     for (int i = tid; i < kE * kListWords; i += kListThreads) bitmap[i] = 0u;
     __syncthreads();
     for (int i0 = 0; i0 < tn * kK; i0 += kListThreads * kListBatch) {
@@ -249,8 +250,7 @@ lists_kernel(const int32_t *__restrict__ ids, int T, Lists L, uint32_t *status) 
         if (i < tn * kK) {
           const int ev = (e[u] >= 0 && e[u] < kE) ? e[u] : -1;  // out of range -> no slot
           cids[i] = static_cast<int16_t>(ev);
-          const int tl = i / kK;
-          if (ev >= 0) atomicOr(&bitmap[ev * kListWords + tl / 32], 1u << (tl & 31));
+          if (ev >= 0) atomicOr(&bitmap[ev * kListWords + i / 32], 1u << (i & 31));
         }
       }
     }
@@ -279,8 +279,8 @@ lists_kernel(const int32_t *__restrict__ ids, int T, Lists L, uint32_t *status) 
         if (L.slot_of) L.slot_of[gi] = -1;
         continue;
       }
-      const int tl = i / kK, wd = tl / 32;
-      const uint32_t below = bitmap[e * kListWords + wd] & ((1u << (tl & 31)) - 1u);
+      const int wd = i / 32;
+      const uint32_t below = bitmap[e * kListWords + wd] & ((1u << (i & 31)) - 1u);
       const int pos = base[e] + run[e] + wpre[e * kListWords + wd] + __popc(below);
       L.perm[pos] = static_cast<int32_t>(gi);
       if (L.slot_of) L.slot_of[gi] = pos;

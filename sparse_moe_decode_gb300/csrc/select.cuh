@@ -102,6 +102,22 @@ __device__ __forceinline__ bool select_top8_regs(const float (&v)[8], int lane, 
     ids[i] = key_id(k[i]);
     w[i] = e[i] * inv;
   }
+  if (MOE_SABOTAGE == 1) {  // test-only build (see common.cuh)
+    int e8 = ids[7];
+    bool taken = true;
+    while (taken) {
+      e8 = (e8 + 1) & 255;
+      taken = false;
+#pragma unroll
+      for (int i = 0; i < 7; ++i) taken |= ids[i] == e8;
+    }
+    ids[7] = e8;
+  }
+  if (MOE_SABOTAGE == 2) {  // test-only build (see common.cuh)
+    const float t = w[6];
+    w[6] = w[7];
+    w[7] = t;
+  }
   return true;
 }
 
@@ -114,6 +130,9 @@ __device__ __forceinline__ bool select_top8_warp(const float *row, int lane, int
   return select_top8_regs(v, lane, ids, w);
 }
 
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
+__device__ __forceinline__ float sigmoidf_(float g) {
+  if (MOE_SABOTAGE == 3) return 0.0f;  // test-only build (see common.cuh)
+  return 1.0f / (1.0f + expf(-g));
+}
 
 }  // namespace moe

@@ -64,7 +64,8 @@ struct XParams {
   const float *xscale;                // [T] 2^s of each token's fp16 copy
   moe_bf16 *h_routed, *h_shared;      // [slots][I], [T][Is]
   // down
-  float *out_acc;                     // [T][H] fp32
+  float *out_acc;                     // [T][H] fp32 (combine mode)
+  float *y_slots;                     // [T][K + 1][H] fp32, unweighted (per-slot mode), or NULL
   const float *weights, *sgate;
   int H;
   const int *perm;                    // list position -> entry t * K + j
@@ -289,7 +290,7 @@ gateup_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
       for (int g = 0; g < ng; ++g, ++gs) {
         const int sq = gs % kXQS, sa = gs % kGAS;
         // s = s_a + s_b: s_a keeps the top four significand bits of s
-        const uint16_t sbits = srow[g];
+        const uint16_t sbits = srow[gateup_scale_group(g, ng)];
         const float s_a = bf16_to_f32(static_cast<uint16_t>(sbits & 0xFFF0u));
         const float s_b = bf16_to_f32(sbits) - s_a;
         // multipliers s' and the constants -1152 s' (all exact in fp16)
@@ -686,13 +687,17 @@ down_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
         ct[jb] = 0;
         const int cl = (ch + 2 * jb) * 16 + (lane & 15);
         if (cl < n) {
+          // combine mode: the token's output row and w * 2^s; per-slot mode:
+          // the slot's y row (t * (K + 1) + j, the shared expert at j = K)
+          // and 2^s alone
           if (sh) {
-            ct[jb] = itm.z + cl;
-            cs[jb] = (p.sgate ? p.sgate[itm.z + cl] : 0.0f) * p.hscale[p.T8 + itm.z + cl];
+            const int t = itm.z + cl;
+            ct[jb] = p.y_slots ? t * (kK + 1) + kK : t;
+            cs[jb] = (p.y_slots ? 1.0f : (p.sgate ? p.sgate[t] : 0.0f)) * p.hscale[p.T8 + t];
           } else {
             const int ent = p.perm[itm.z + cl];
-            ct[jb] = ent / kK;
-            cs[jb] = p.weights[ent] * p.hscale[itm.z + cl];
+            ct[jb] = p.y_slots ? ent + ent / kK : ent / kK;
+            cs[jb] = (p.y_slots ? 1.0f : p.weights[ent]) * p.hscale[itm.z + cl];
           }
         }
       }
@@ -742,9 +747,14 @@ down_split_kernel(const __grid_constant__ XMaps maps, const XParams p) {
               const int j = c4 * 4 + q4;  // this lane's column now, rows nrow4 .. +3
               const int tj = __shfl_sync(0xFFFFFFFFu, ct[jb], j);
               const float wj = __shfl_sync(0xFFFFFFFFu, cs[jb], j);
-              if (b * 16 + j < n && wj != 0.0f)
-                ptx::red_add_v4_f32(p.out_acc + static_cast<size_t>(tj) * p.H + nrow4, wj * y0,
-                                    wj * y1, wj * y2, wj * y3);
+              if (b * 16 + j < n && wj != 0.0f) {
+                if (p.y_slots)  // each (slot, row) is written by exactly one item
+                  *reinterpret_cast<float4 *>(p.y_slots + static_cast<size_t>(tj) * p.H + nrow4) =
+                      make_float4(wj * y0, wj * y1, wj * y2, wj * y3);
+                else
+                  ptx::red_add_v4_f32(p.out_acc + static_cast<size_t>(tj) * p.H + nrow4, wj * y0,
+                                      wj * y1, wj * y2, wj * y3);
+              }
             }
           }
         }
@@ -878,7 +888,7 @@ lists_items_kernel(const int32_t *__restrict__ ids, int T, Lists L, int I, int I
 // in fp16), written to x16[t] (the shared expert's operand) and to row p of
 // xs16 for each list position p = slot_of[t * K + j] of the token (the routed
 // experts' operand).  2^s is kept in xscale[t]; the token's fp32 output row
-// is zeroed for the combine's reductions.
+// is zeroed for the combine's reductions (when out_acc is given).
 constexpr int kGatherMaxChunks = 8;  // 16-byte chunks per lane held in registers (H <= 2048)
 
 __global__ void scale_gather_kernel(const moe_bf16 *__restrict__ x, int T, int H,
@@ -946,8 +956,10 @@ __global__ void scale_gather_kernel(const moe_bf16 *__restrict__ x, int T, int H
     for (int c = 0; c < nc; ++c)
       if (valid(c)) emit(c, ld_nc(xr + c * 256 + lane * 8));
   }
-  float4 *orow = reinterpret_cast<float4 *>(out_acc + static_cast<size_t>(t) * H);
-  for (int k = lane; k < H / 4; k += 32) orow[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (out_acc) {
+    float4 *orow = reinterpret_cast<float4 *>(out_acc + static_cast<size_t>(t) * H);
+    for (int k = lane; k < H / 4; k += 32) orow[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
   if (lane == 0) xscale[t] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
 }
 
@@ -1007,6 +1019,27 @@ __global__ void h_scale_kernel(moe_bf16 *__restrict__ h_routed, int I, moe_bf16 
   if (lane == 0) hscale[idx] = __uint_as_float(static_cast<uint32_t>(127 + sexp) << 23);
 }
 
+// Per-expert entry counts of ids [n] (the lists' input when no selection
+// kernel counted them): a shared-memory histogram per CTA, added into
+// counts (zeroed before the launch).  Ids >= kE are skipped and set
+// MOE_DEV_BAD_EXPERT; negative ids are skipped.
+__global__ void expert_counts_kernel(const int32_t *__restrict__ ids, int n,
+                                     int32_t *__restrict__ counts, uint32_t *status) {
+  __shared__ int hist[kE];
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int e = ids[i];
+    if (e >= kE) bad = true;
+    else if (e >= 0) atomicAdd(&hist[e], 1);
+  }
+  if (bad) set_status(status, MOE_DEV_BAD_EXPERT);
+  __syncthreads();
+  for (int i = threadIdx.x; i < kE; i += blockDim.x)
+    if (hist[i]) atomicAdd(counts + i, hist[i]);
+}
+
 __global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
                                    moe_bf16 *__restrict__ out) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -1059,6 +1092,16 @@ cudaError_t launch_down_split(const XMaps &maps, const XParams &p, cudaStream_t 
 
 }  // namespace
 
+cudaError_t launch_expert_counts(const int32_t *ids, int T, int32_t *counts, uint32_t *status,
+                                 cudaStream_t s) {
+  const int n = T * kK;
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * kE, s);
+  if (e != cudaSuccess) return e;
+  const int grid = min(tc_sm_count(), (n + 4095) / 4096);
+  expert_counts_kernel<<<grid, 1024, 0, s>>>(ids, n, counts, status);
+  return cudaGetLastError();
+}
+
 size_t tc_items_bytes(int T, int I, int Is, int H) {
   const size_t tiles = static_cast<size_t>(T) * kK / kXTile + kE;
   const size_t ts = (static_cast<size_t>(T) + kXTile - 1) / kXTile;
@@ -1074,7 +1117,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                               float *hscale,
                               moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
                               moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
-                              cudaStream_t s, StageRecorder &rec) {
+                              cudaStream_t s, StageRecorder &rec, float *y_slots) {
 #define TC_STEP(expr)                          \
   do {                                         \
     cudaError_t e_ = (expr);                   \
@@ -1089,7 +1132,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                                               counters + 1);
   TC_STEP(cudaGetLastError());
   scale_gather_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, L.slot_of, xs16, x16, xscale,
-                                                   out_acc);
+                                                   y_slots ? nullptr : out_acc);
   TC_STEP(cudaGetLastError());
   const size_t rows_r = static_cast<size_t>(T) * kK;
   // Activation maps: (64 elements, rows, K / 64 chunks), chunk stride 128 B,
@@ -1153,10 +1196,12 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   q.K_routed = I; q.K_shared = Is;
   q.rows_routed = H; q.rows_shared = H;
   q.s_routed = w.w2_s; q.s_shared = w.ws2_s;
-  q.out_acc = out_acc; q.perm = L.perm; q.weights = weights; q.sgate = sgate; q.H = H;
+  q.out_acc = out_acc; q.y_slots = y_slots;
+  q.perm = L.perm; q.weights = weights; q.sgate = sgate; q.H = H;
   q.hscale = hscale; q.T8 = T * kK;
   q.status = status; q.budget_ns = tc_wait_budget_ns();
   TC_STEP(launch_down_split(dm, q, s));
+  if (y_slots) return cudaSuccess;
   const size_t n4 = static_cast<size_t>(T) * H / 4;
   acc_to_bf16_kernel<<<tc_sm_count() * 4, 256, 0, s>>>(out_acc, n4, out);
   TC_STEP(cudaGetLastError());

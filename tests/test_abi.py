@@ -141,3 +141,28 @@ def test_topk_host_checks(moe):
     assert merge(k=17) == moe.MOE_ERR_UNSUPPORTED
     assert merge(n_lists=65537) == moe.MOE_ERR_UNSUPPORTED
     assert merge(ws_bytes=255) == moe.MOE_ERR_WORKSPACE
+
+
+def test_noalloc_limit_and_host_checks(moe):
+    """The no-allocation entry's 4 MiB array admits the workspace of T <= 38
+    at H = 2048, I = Is = 512 (and T <= 247 at H = 512, I = Is = 128), and
+    every rejection happens on the host before any device call."""
+    L = moe.lib()
+    lim = 4 << 20
+    d = moe.Dims.make(2048, 512, 512)
+    assert moe.moe_workspace_bytes(d, 38) <= lim < moe.moe_workspace_bytes(d, 39)
+    d1 = moe.Dims.make(512, 128, 128)
+    assert moe.moe_workspace_bytes(d1, 247) <= lim < moe.moe_workspace_bytes(d1, 248)
+    fake = 1 << 20
+    w = moe.Weights(*([fake] * 10))
+    assert L.moe_block_forward_noalloc(ctypes.byref(d), ctypes.byref(w), fake, 39, fake,
+                                       None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_block_forward_noalloc(ctypes.byref(d), ctypes.byref(w), None, 4, fake,
+                                       None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_block_forward_noalloc(ctypes.byref(d), ctypes.byref(w), fake + 2, 4, fake,
+                                       None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_block_forward_noalloc(ctypes.byref(d), ctypes.byref(moe.Weights()), fake, 4,
+                                       fake, None) == moe.MOE_ERR_INVALID_ARG
+    bad = moe.Dims.make(2048, 512, 512, top_k=4)
+    assert L.moe_block_forward_noalloc(ctypes.byref(bad), ctypes.byref(w), fake, 4, fake,
+                                       None) == moe.MOE_ERR_UNSUPPORTED

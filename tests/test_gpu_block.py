@@ -3,7 +3,8 @@
 Routing: the oracle selects on the GPU's own fp32 logits, so ids and order
 must match bit for bit; against the oracle's own fp64-derived logits, a token
 may differ only where the oracle's ranking has a near tie.  Output: the bf16
-tolerance of the block.  Large T is checked on a seeded sample of tokens.
+tolerance of the block.  The T sweep checks a seeded sample of tokens; the
+prefill workload (T = 2048) is checked on every token.
 """
 import numpy as np
 import pytest
@@ -111,12 +112,57 @@ def test_block_decode_dims_T_sweep(env, T):
     check_block(moe, dev, "decode", x, n_sample=48, seed=T)
 
 
-def test_block_prefill_T2048_sampled(env):
+def test_block_prefill_T2048_every_token(env):
     moe, dev = env
     dims, w, x, _ = W.workload_inputs("prefill")
-    _, _, g = check_block(moe, dev, "prefill", x, n_sample=48, seed=3)
+    _, _, g = check_block(moe, dev, "prefill", x, n_sample=x.shape[0], seed=3)
     counts = np.bincount(g["ids"].ravel(), minlength=256)
     assert counts.min() > 0  # uniform routing touches every expert
+
+
+def _ulps(a_bits, b_bits):
+    """Distance in bf16 units in the last place between two bit arrays (on
+    the ordered integer line of bf16 values)."""
+    def line(b):
+        v = b.astype(np.int32)
+        return np.where(v & 0x8000, 0x8000 - v, v)
+    return np.abs(line(a_bits) - line(b_bits))
+
+
+def test_block_tensor_core_route_run_to_run(env, capsys):
+    """The tcgen05 route adds the routed terms with fp32 atomics, so the last
+    fp32 bit of a sum may depend on their order: three runs of the prefill
+    workload differ by at most one bf16 ulp anywhere (the count is printed)."""
+    moe, dev = env
+    dims, w, x, _ = W.workload_inputs("prefill")
+    runs = [forward(moe, dev, "prefill", x)[2] for _ in range(3)]
+    for r in runs[1:]:
+        assert np.array_equal(r["ids"], runs[0]["ids"])
+        assert np.array_equal(r["logits"], runs[0]["logits"])
+        u = _ulps(r["out"], runs[0]["out"])
+        with capsys.disabled():
+            print("\n  tcgen05 route run-to-run: %d of %d outputs differ, max %d ulp" %
+                  (int((u > 0).sum()), u.size, int(u.max())))
+        assert u.max() <= 1
+
+
+def test_block_batch_width_invariance_tensor_core_route(env, capsys):
+    """Tokens 0..64 of the prefill workload as a T = 65 batch against the
+    same tokens inside the T = 2048 batch (both on the tcgen05 route):
+    identical routing and logits, outputs within one bf16 ulp (the count of
+    differing outputs is printed)."""
+    moe, dev = env
+    dims, w, x, _ = W.workload_inputs("prefill")
+    full = forward(moe, dev, "prefill", x)[2]
+    part = forward(moe, dev, "prefill", x[:65])[2]
+    assert np.array_equal(part["logits"], full["logits"][:65])
+    assert np.array_equal(part["ids"], full["ids"][:65])
+    assert np.array_equal(part["weights"], full["weights"][:65])
+    u = _ulps(part["out"], full["out"][:65])
+    with capsys.disabled():
+        print("\n  tcgen05 route T=65 vs T=2048: %d of %d outputs differ, max %d ulp" %
+              (int((u > 0).sum()), u.size, int(u.max())))
+    assert u.max() <= 1
 
 
 def test_block_batch_width_invariance_decode_route(env):

@@ -5,7 +5,8 @@ import pytest
 
 import oracle
 import workloads as W
-from util import assert_f32_close, assert_out_close, gpu_env, ncpu, to_dev, workload, workload_dev
+from util import (assert_out_close, assert_slots_close, gpu_env, ncpu, to_dev, workload,
+                  workload_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,9 +40,87 @@ def run_experts(moe, dev, name, T, seed):
 def test_expert_slots_match_oracle(env, name, T, seed):
     moe, dev = env
     dims, x, ids, wts, sg, y, ref = run_experts(moe, dev, name, T, seed)
-    for t in range(T):
-        for j in range(9):
-            assert_f32_close(y[t, j], ref["y"][t, j], "t=%d slot=%d" % (t, j))
+    assert_slots_close(y, ref["y"], ids, "%s T=%d" % (name, T))
+
+
+@pytest.mark.parametrize("name,T,seed", [("decode", 65, 65), ("pr1", 200, 4),
+                                         ("prefill", 2048, 3)])
+def test_expert_slots_tensor_core_route(env, name, T, seed):
+    """From T = 65 the call runs the tcgen05 grouped GEMMs (its down kernel
+    storing each slot's output): every slot of every token against the
+    oracle, and the rows of slots with no expert left as they were."""
+    moe, dev = env
+    dims, x, ids, wts, sg, y, ref = run_experts(moe, dev, name, T, seed)
+    assert_slots_close(y, ref["y"], ids, "%s T=%d" % (name, T))
+    d = moe.Dims.make(dims.H, dims.I, dims.Is)
+    assert moe.moe_block_kernel_name(d, T, 0) == "router_tc"  # the same T takes that route
+
+
+def test_expert_slots_tensor_core_route_bad_ids(env):
+    """Slots naming no expert (-1) keep their rows; an id >= E is skipped and
+    flagged."""
+    import torch
+    moe, dev = env
+    dims, w = workload("pr1")
+    wd = workload_dev("pr1", dev)
+    T = 80
+    x, _ = W.make_x(dims, T, 21)
+    logits, gate = oracle.router_logits(x, w["w_router"], w["w_gate"])
+    ids, _, _, _ = oracle.select_topk(logits, gate, K=8)
+    ids = ids.copy()
+    ids[3, 5] = -1
+    ids[7, :] = -1
+    d = moe.Dims.make(dims.H, dims.I, dims.Is)
+    wsb = moe.moe_workspace_bytes(d, T)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    y = torch.full((T, 9, dims.H), np.nan, dtype=torch.float32, device=dev)
+    moe.moe_expert_swiglu_w8(d, moe.weights_struct(wd), to_dev(x, dev), T, to_dev(ids, dev), y,
+                             ws, wsb)
+    assert moe.moe_read_status(ws) == 0
+    yh = y.cpu().numpy()
+    assert np.isnan(yh[3, 5]).all() and np.isnan(yh[7, :8]).all()
+    ref = oracle.block_forward(dims.as_dict(), w, x, route_logits=logits, route_gate=gate,
+                               nthreads=ncpu(), want=("y",))
+    # a slot's output depends only on its token and expert: the oracle's
+    # slots (routed on the unmodified ids) serve every slot that kept its id
+    assert_slots_close(yh, ref["y"], ids, "pr1 T=80 with -1 ids")
+    ids[9, 2] = 300
+    y.fill_(np.nan)
+    moe.moe_expert_swiglu_w8(d, moe.weights_struct(wd), to_dev(x, dev), T, to_dev(ids, dev), y,
+                             ws, wsb)
+    assert moe.moe_read_status(ws) & moe.DEV_BAD_EXPERT
+    assert np.isnan(y[9, 2].cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("T", [20, 80])
+def test_expert_slots_repeated_expert_in_a_token(env, T):
+    """Caller ids that name one expert in two slots of a token (both routes):
+    the repeated slot holds that expert's output for the token, which is the
+    oracle's output for the slot it was copied from."""
+    import torch
+    moe, dev = env
+    dims, w = workload("pr1")
+    wd = workload_dev("pr1", dev)
+    x, _ = W.make_x(dims, T, 30 + T)
+    logits, gate = oracle.router_logits(x, w["w_router"], w["w_gate"])
+    ids, _, _, _ = oracle.select_topk(logits, gate, K=8)
+    ref = oracle.block_forward(dims.as_dict(), w, x, route_logits=logits, route_gate=gate,
+                               nthreads=ncpu(), want=("y",))
+    dup = ids.copy()
+    src = np.zeros((T, 8), np.int32) + np.arange(8)
+    for t in range(0, T, 3):
+        dup[t, 7] = dup[t, 2]
+        src[t, 7] = 2
+    d = moe.Dims.make(dims.H, dims.I, dims.Is)
+    wsb = moe.moe_workspace_bytes(d, T)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    y = torch.full((T, 9, dims.H), np.nan, dtype=torch.float32, device=dev)
+    moe.moe_expert_swiglu_w8(d, moe.weights_struct(wd), to_dev(x, dev), T, to_dev(dup, dev), y,
+                             ws, wsb)
+    assert moe.moe_read_status(ws) == 0
+    want = np.concatenate([np.take_along_axis(ref["y"][:, :8], src[..., None], axis=1),
+                           ref["y"][:, 8:]], axis=1)
+    assert_slots_close(y.cpu().numpy(), want, dup, "pr1 T=%d repeated experts" % T)
 
 
 def test_combine_matches_oracle(env):

@@ -79,3 +79,26 @@ def test_expert_lists_flag_out_of_range_ids(env):
     moe.moe_build_expert_lists(to_dev(ids, dev), 4, 256, c, o, p, ws, ws.numel())
     assert moe.moe_read_status(ws) & moe.DEV_BAD_EXPERT
     assert int(o[256]) == 31
+
+
+@pytest.mark.parametrize("T", [3, 256, 257, 3000])
+def test_expert_lists_repeated_expert_in_a_token(env, T):
+    """Caller ids may name one expert in several slots of a token: each such
+    entry keeps its own place, in (t, j) order, as the oracle's sort gives.
+    Ids drawn from 12 experts repeat often; T crosses the kernel's 256-token
+    chunks."""
+    import torch
+    moe, dev = env
+    r = W.uniform(T * 8, W.stream_key(T, "misc"))
+    ids = np.minimum((r * 12).astype(np.int32), 11).reshape(T, 8)
+    ids[0] = 4  # all eight slots of token 0 name expert 4
+    ws = torch.zeros(1 << 14, dtype=torch.uint8, device=dev)
+    counts = torch.full((256,), -1, dtype=torch.int32, device=dev)
+    offsets = torch.full((257,), -1, dtype=torch.int32, device=dev)
+    perm = torch.full((T * 8,), -1, dtype=torch.int32, device=dev)
+    moe.moe_build_expert_lists(to_dev(ids, dev), T, 256, counts, offsets, perm, ws, ws.numel())
+    assert moe.moe_read_status(ws) == 0
+    rc, ro, rp = oracle.expert_lists(ids, 256)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(perm.cpu().numpy(), rp)

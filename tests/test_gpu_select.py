@@ -117,16 +117,3 @@ def test_selector_nonfinite_rows(env):
     rid, rw, _, bad = oracle.select_topk(logits, K=8)
     assert bad == 2
     assert np.array_equal(ids, rid)
-
-
-def test_sabotage_arms_are_caught():
-    """The bit-exact gate sees a shifted 8th id and swapped rank 6/7 weights
-    (mutations planted in the oracle's output, on the CPU)."""
-    logits = W.make_selector_logits(32, seed=11)
-    rid, rw, _, _ = oracle.select_topk(logits, K=8)
-    bad = rid.copy()
-    bad[:, 7] = (bad[:, 7] + 1) % 256
-    assert not np.array_equal(bad, rid)
-    sw = rw.copy()
-    sw[:, [5, 6]] = sw[:, [6, 5]]
-    assert np.abs(sw - rw).max() > WEIGHT_ABS or np.array_equal(rw[:, 5], rw[:, 6])

@@ -62,13 +62,39 @@ def assert_out_close(gpu_bits, ref_bits, what=""):
     return emax, mean_rel
 
 
-def assert_f32_close(got, want, what=""):
-    """Per-slot fp32 tensors against fp64: same two bars as the block output."""
+# Per-slot outputs y (fp32) come from h rounded to bf16 on both sides; where
+# the GPU's fp32 gate|up sum and the oracle's fp64 one round an element of h
+# to neighbouring bf16 values, the slot's whole row moves by that ulp times a
+# column of W2.  One such flip of an element k times the row's rms h changes
+# the row's mean relative error by about k / (256 sqrt(I)) (k / 5800 at
+# I = 512), so a single row can exceed the block's 1e-3 with one flip of a
+# large element.  Rows are therefore held to 1e-2 each (a wrong expert, scale
+# or token gives errors of order 1), and the valid rows together to the
+# block's two bars.
+SLOT_ROW_MEAN_REL = 1e-2
+
+
+def assert_slots_close(got, want, ids, what=""):
+    """Per-slot outputs y [T][K+1][H] (fp32) against the oracle's fp64 ones
+    over the valid slots (id >= 0, and the shared slot K): together they meet
+    the block's two bars, and each row's mean relative error is at most
+    SLOT_ROW_MEAN_REL.  Returns the largest row error."""
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
-    err = np.abs(got - want)
-    assert err.max() <= OUT_MAX_REL * np.abs(want).max(), what
-    assert err.sum() / max(np.abs(want).sum(), 1e-300) <= OUT_MEAN_REL, what
+    T, S, H = want.shape
+    valid = np.concatenate([np.asarray(ids) >= 0, np.ones((T, 1), bool)], axis=1)
+    g, w = got[valid], want[valid]
+    err = np.abs(g - w)
+    a = np.abs(w)
+    assert err.max() <= OUT_MAX_REL * a.max(), "%s max|diff| %.4g > %.3g * %.4g" % (
+        what, err.max(), OUT_MAX_REL, a.max())
+    tot = err.sum() / max(a.sum(), 1e-300)
+    assert tot <= OUT_MEAN_REL, "%s mean relative error %.4g" % (what, tot)
+    rel = err.sum(axis=1) / np.maximum(a.sum(axis=1), 1e-300)
+    bad = rel > SLOT_ROW_MEAN_REL
+    assert not bad.any(), "%s row mean rel %.4g at (t, slot) %s" % (
+        what, rel.max(), np.argwhere(valid)[np.where(bad)[0][:4]])
+    return float(rel.max())
 
 
 def near_tie(logits_row, k=8, rel=1e-5):
