@@ -79,10 +79,11 @@ __device__ __forceinline__ int consumer_tid() {
   return consumer_warp(threadIdx.x >> 5) * 32 + (threadIdx.x & 31);
 }
 constexpr int kFStages = 6;
-constexpr int kFRedBufs = 1;  // buffers of each quad's reduction exchange
+constexpr int kFRedBufs = 2;  // buffers of each quad's reduction exchange
 constexpr int kFStageBytes = 16 * kFusedMaxH;  // one gate|up unit, or packed down units
 constexpr int kFScaleBytes = 512;              // the group scales of a stage's rows
-constexpr int kFPass = 16;                   // tokens per pass (two n8 tiles)
+constexpr int kFPass = 8;                    // gate|up tokens per pass (one n8 tile)
+constexpr int kFDownPass = 16;               // down tokens per pass (two n8 tiles)
 constexpr int kRP = 260;                     // router partial row: 257 used, 16-byte rows
 constexpr int kFLocalSelT = kFConsumerWarps;  // tokens selected by every CTA itself
 constexpr int kFClaim = 4;  // routed gate|up units per claim when there are many
@@ -126,7 +127,7 @@ struct FusedSmem {
   uint8_t ring[kFStages][kFStageBytes];
   uint8_t ring_s[kFStages][kFScaleBytes];  // bf16 scales of each stage's rows
   union {
-    float red[kFQuads][kFRedBufs][4][2][32][4];  // gate|up: quad reduction exchange
+    float red[kFQuads][kFRedBufs][4][32][4];     // gate|up: quad reduction exchange
     float ys[16][kFRowOwnerT * (kK + 1)];      // row-owner down: y of this CTA's 16 rows
   } u;
   int32_t ids[kFusedMaxT][kK];
@@ -138,11 +139,10 @@ struct FusedSmem {
   int32_t counts[kE];
   int32_t offsets[kE + 1];
   int32_t active[kE + 1];
-  unsigned long long mask[kE];
-  int scan_tmp[8];
   uint64_t full[kFStages], empty[kFStages], routed;
   int2 stage_unit[kFStages];  // (expert, first row pair | first output row); x < 0: end
-  uint64_t red_full[kFQuads][kFRedBufs], red_empty[kFQuads][kFRedBufs];
+  uint64_t red_empty[kFQuads][kFRedBufs];
+  int red_cnt[kFQuads][kFRedBufs];  // warps that have stored their pass's quarter
   int abort;
 };
 
@@ -217,24 +217,31 @@ __device__ __forceinline__ void fwait(uint64_t *bar, uint32_t parity, FusedSmem 
 
 // Grid-wide barrier of the consumer threads of every CTA.  Self-resetting:
 // CTA 0 adds 2^31 - (G - 1), the others 1, so each barrier flips bit 31 of the
-// counter and leaves its low bits unchanged.  Bounded by the wait budget.
-__device__ __forceinline__ void grid_sync(unsigned *bar, FusedSmem &S, uint64_t budget,
-                                          uint32_t *status) {
+// counter and leaves its low bits unchanged.  The arrival is a release
+// reduction (no round trip to wait for); `phase` (consumer thread 0 only) is
+// the value bit 31 takes when the barrier completes: the bit read at the
+// start of the launch, which every CTA reads alike (no barrier completes
+// before every CTA has arrived), flipped at each barrier.  The polling
+// thread's acquire load and the CTA barrier after it order the reads that
+// follow after every CTA's writes before its arrival.  Bounded by the wait
+// budget.
+__device__ __forceinline__ void grid_sync(unsigned *bar, unsigned &phase, FusedSmem &S,
+                                          uint64_t budget, uint32_t *status) {
   ptx::named_barrier(1, kFConsumers);
   if (consumer_tid() == 0) {
-    __threadfence();
+    phase ^= 0x80000000u;
     const unsigned inc = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1) : 1u;
-    const unsigned old = atomicAdd(bar, inc);
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(bar), "r"(inc) : "memory");
     const uint64_t t0 = ptx::globaltimer();
-    while (((ld_acquire_u32(bar) ^ old) & 0x80000000u) == 0u) {
+    unsigned v;
+    while (((v = ld_acquire_u32(bar)) & 0x80000000u) != phase) {
       if (aborted(S) || ptx::globaltimer() - t0 > budget) {
-        if (!aborted(S)) record_give_up(status, 2u, old & 0x7FFFFFFFu);
+        if (!aborted(S)) record_give_up(status, 2u, v & 0x7FFFFFFFu);
         *reinterpret_cast<volatile int *>(&S.abort) = 1;
         break;
       }
-      __nanosleep(64);
+      __nanosleep(32);
     }
-    __threadfence();
   }
   ptx::named_barrier(1, kFConsumers);
 }
@@ -575,22 +582,18 @@ __device__ __forceinline__ void select_token(FusedSmem &S, const FusedParams &p,
 // barrier, and every CTA reads all selections.  Then every CTA builds the
 // token -> expert lists in shared memory.
 __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedParams &p, int cwarp,
-                                                   int lane, uint64_t budget) {
+                                                   int lane, unsigned &phase, uint64_t budget) {
   const int tid = consumer_tid();
   // independent of the selection, so done first, by the last warps (idle
   // during a local selection of T < 12 tokens)
   for (int t2 = kFConsumers - 1 - tid; t2 < p.T; t2 += kFConsumers)
     S.xs[t2] = __ldcg(p.xscale + t2);
-  if (tid < kE) {
-    S.counts[tid] = 0;
-    S.mask[tid] = 0ull;
-  }
   if (p.T <= kFLocalSelT) {
     if (cwarp < p.T) select_token(S, p, cwarp, lane, true);
   } else {
     const int t = blockIdx.x * kFConsumerWarps + cwarp;
     if (t < p.T) select_token(S, p, t, lane, false);
-    grid_sync(p.grid_bar, S, budget, p.status);
+    grid_sync(p.grid_bar, phase, S, budget, p.status);
     for (int i = tid; i < p.T * kK; i += kFConsumers) {
       S.ids[i / kK][i % kK] = __ldcg(p.sel_ids + i);
       S.wts[i / kK][i % kK] = __ldcg(p.sel_w + i);
@@ -598,99 +601,66 @@ __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedPara
     for (int t2 = tid; t2 < p.T; t2 += kFConsumers) S.sg[t2] = __ldcg(p.sel_sg + t2);
   }
   ptx::named_barrier(1, kFConsumers);
-  if (p.T * kK <= 32) {
-    // Up to 32 (token, slot) entries: one warp sorts the keys (expert, entry)
-    // with a bitonic network over its lanes; the sorted order is the list
-    // order (experts ascending, tokens ascending within an expert, as the
-    // general path below builds it), and each run of one expert gives its
-    // count, offset and place in the active list.
-    if (cwarp == 0) {
-      const int n = p.T * kK;
-      int e0 = kE;  // entries naming no expert (and padding lanes) sort last
-      if (lane < n) {
-        const int v = S.ids[lane / kK][lane % kK];
-        if (v >= 0) e0 = v;
+  // Lists, in (expert, t, j) order.  Warp 0 walks the entries in batches of
+  // 32 in entry order: the lanes naming one expert (__match_any_sync) take
+  // consecutive places after that expert's earlier entries, so each entry
+  // learns its rank within its expert (kept in slot_of for now); warp 0 then
+  // scans the counts into offsets and the active list, and every thread
+  // places its entries.
+  const int n = p.T * kK;
+  if (cwarp == 0) {
+    for (int e = lane; e < kE; e += 32) S.counts[e] = 0;
+    __syncwarp();
+    for (int b = 0; b < n; b += 32) {
+      const int i = b + lane;
+      const int e = i < n ? S.ids[i / kK][i % kK] : -1;
+      const unsigned same = __match_any_sync(0xFFFFFFFFu, e);
+      const int lead = __ffs(same) - 1;
+      int before = 0;
+      if (lane == lead && e >= 0) {
+        before = S.counts[e];
+        S.counts[e] = before + __popc(same);
       }
-      unsigned key = (static_cast<unsigned>(e0) << 8) | static_cast<unsigned>(lane);
-#pragma unroll
-      for (int k = 2; k <= 32; k <<= 1)
-#pragma unroll
-        for (int jj = k >> 1; jj > 0; jj >>= 1) {
-          const unsigned other = __shfl_xor_sync(0xFFFFFFFFu, key, jj);
-          const bool keep_min = ((lane & jj) == 0) == ((lane & k) == 0);
-          key = keep_min ? min(key, other) : max(key, other);
-        }
-      const int e = static_cast<int>(key >> 8), i = static_cast<int>(key & 0xFFu);
-      const bool valid = e < kE;
-      const unsigned valid_mask = __ballot_sync(0xFFFFFFFFu, valid);
-      const int n_valid = __popc(valid_mask);
-      const int prev = __shfl_up_sync(0xFFFFFFFFu, e, 1);
-      const bool start = valid && (lane == 0 || prev != e);
-      const unsigned starts = __ballot_sync(0xFFFFFFFFu, start);
-      if (valid) {
-        S.perm[lane] = i;
-        S.slot_of[i / kK][i % kK] = lane;
-      } else if (i < n) {
-        S.slot_of[i / kK][i % kK] = -1;
-      }
-      if (start) {
-        const unsigned above = lane == 31 ? 0u : starts & ~((2u << lane) - 1u);
-        const int next = above ? __ffs(above) - 1 : n_valid;
-        S.counts[e] = next - lane;
-        S.offsets[e] = lane;
-        S.active[1 + __popc(starts & ((1u << lane) - 1u))] = e;
-      }
-      if (lane == 0) {
-        S.active[0] = __popc(starts);
-        S.offsets[kE] = n_valid;
-      }
+      before = __shfl_sync(0xFFFFFFFFu, before, lead);
+      if (i < n) S.slot_of[i / kK][i % kK] = e >= 0 ? before + __popc(same & ((1u << lane) - 1u)) : -1;
+      __syncwarp();
     }
-    ptx::named_barrier(1, kFConsumers);
-    return;
-  }
-  for (int i = tid; i < p.T * kK; i += kFConsumers) {
-    const int t = i / kK, e = S.ids[t][i % kK];
-    if (e >= 0) {
-      atomicAdd(&S.counts[e], 1);
-      atomicOr(&S.mask[e], 1ull << t);
+    // offsets: exclusive scan of the counts (8 experts per lane), and the
+    // active list (experts with entries, ascending)
+    int c[kE / 32], run = 0, act = 0;
+#pragma unroll
+    for (int k = 0; k < kE / 32; ++k) {
+      c[k] = S.counts[8 * lane + k];
+      run += c[k];
+      act += c[k] > 0 ? 1 : 0;
     }
-  }
-  ptx::named_barrier(1, kFConsumers);
-  // exclusive scans of counts (offsets) and of (counts > 0) (active list)
-  if (tid < kE) {
-    const int c = S.counts[tid];
-    int incl = c, act = c > 0 ? 1 : 0;
+    int incl = run, aincl = act;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int n1 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      const int n2 = __shfl_up_sync(0xFFFFFFFFu, act, o);
-      if (lane >= o) { incl += n1; act += n2; }
+      const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      const int y = __shfl_up_sync(0xFFFFFFFFu, aincl, o);
+      if (lane >= o) { incl += x; aincl += y; }
     }
-    if (lane == 31) S.scan_tmp[cwarp] = incl | (act << 20);
-    ptx::named_barrier(6, kE);  // ids 2..4 belong to the quads
-    int base = 0, abase = 0;
-    for (int w2 = 0; w2 < cwarp; ++w2) {
-      base += S.scan_tmp[w2] & 0xFFFFF;
-      abase += S.scan_tmp[w2] >> 20;
+    int off = incl - run, a = aincl - act;
+#pragma unroll
+    for (int k = 0; k < kE / 32; ++k) {
+      S.offsets[8 * lane + k] = off;
+      off += c[k];
+      if (c[k] > 0) S.active[1 + a++] = 8 * lane + k;
     }
-    const int off = base + incl - c;
-    const int a_idx = abase + act - (c > 0 ? 1 : 0);
-    S.offsets[tid] = off;
-    if (c > 0) S.active[1 + a_idx] = tid;
-    if (tid == kE - 1) {
-      S.offsets[kE] = off + c;
-      S.active[0] = a_idx + (c > 0 ? 1 : 0);
+    if (lane == 31) {
+      S.offsets[kE] = incl;
+      S.active[0] = aincl;
     }
   }
   ptx::named_barrier(1, kFConsumers);
-  for (int i = tid; i < p.T * kK; i += kFConsumers) {
-    const int t = i / kK, j = i % kK, e = S.ids[t][j];
-    int pos = -1;
+  for (int i = tid; i < n; i += kFConsumers) {
+    const int t = i / kK, jj = i % kK, e = S.ids[t][jj];
     if (e >= 0) {
-      pos = S.offsets[e] + __popcll(S.mask[e] & ((1ull << t) - 1ull));
+      const int pos = S.offsets[e] + S.slot_of[t][jj];
       S.perm[pos] = i;
+      S.slot_of[t][jj] = pos;
     }
-    S.slot_of[t][j] = pos;
   }
   ptx::named_barrier(1, kFConsumers);
 }
@@ -805,102 +775,99 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
   const uint8_t *rows = S.ring[s];
   const int stride = p.H;
   for (int tb = 0; tb < n_tok; tb += kFPass) {
-    const int ntiles = min(2, (n_tok - tb + 7) / 8);
-    const moe_bf16 *brow[2];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int idx = tb + 8 * nt + g;
-      brow[nt] = nullptr;
-      if (idx < n_tok) {
-        const int t = sh ? idx : S.perm[p0 + idx] / kK;
-        brow[nt] = reinterpret_cast<const moe_bf16 *>(p.x16) + static_cast<size_t>(t) * p.H;
-      }
+    const moe_bf16 *brow = nullptr;  // this lane's B column (token) of the n8 tile
+    if (tb + g < n_tok) {
+      const int t = sh ? tb + g : S.perm[p0 + tb + g] / kK;
+      brow = reinterpret_cast<const moe_bf16 *>(p.x16) + static_cast<size_t>(t) * p.H;
     }
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    for (int nt = 0; nt < ntiles; ++nt) {
-      for (int kk = kb; kk < kb + kq; kk += 256) {  // batches of 4 slices (2 groups)
-        const int ns4 = min(4, (kb + kq - kk) / 64);
-        uint32_t xw[4][8];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kk = kb; kk < kb + kq; kk += 256) {  // batches of 4 slices (2 groups)
+      const int ns4 = min(4, (kb + kq - kk) / 64);
+      uint32_t xw[4][8];
 #pragma unroll
-        for (int sl = 0; sl < 4; ++sl) {
-          if (brow[nt] && sl < ns4) {
-            // fp16 rows written before grid barrier 1 of this launch: no SM
-            // reads them earlier, so L1 holds no stale copy, and caching
-            // them in L1 serves this CTA's many units of the same expert
-            const moe_bf16 *src = brow[nt] + kk + 64 * sl + 16 * c;
-            const uint4 x0 = ld_ca16(src), x1 = ld_ca16(src + 8);
-            xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
-            xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
-          } else {
+      for (int sl = 0; sl < 4; ++sl) {
+        if (brow && sl < ns4) {
+          // fp16 rows written before grid barrier 1 of this launch: no SM
+          // reads them earlier, so L1 holds no stale copy, and caching
+          // them in L1 serves this CTA's many units of the same expert
+          const moe_bf16 *src = brow + kk + 64 * sl + 16 * c;
+          const uint4 x0 = ld_ca16(src), x1 = ld_ca16(src + 8);
+          xw[sl][0] = x0.x; xw[sl][1] = x0.y; xw[sl][2] = x0.z; xw[sl][3] = x0.w;
+          xw[sl][4] = x1.x; xw[sl][5] = x1.y; xw[sl][6] = x1.z; xw[sl][7] = x1.w;
+        } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
-          }
+          for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
         }
-        const int g0 = gateup_scale_group(kk / kG, ng), g1 = gateup_scale_group(kk / kG + 1, ng);
-        const float slo0 = bf16_to_f32(s_gate[g0]), shi0 = bf16_to_f32(s_up[g0]);
-        const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[g1]) : 0.0f;
-        const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[g1]) : 0.0f;
+      }
+      const int g0 = gateup_scale_group(kk / kG, ng), g1 = gateup_scale_group(kk / kG + 1, ng);
+      const float slo0 = bf16_to_f32(s_gate[g0]), shi0 = bf16_to_f32(s_up[g0]);
+      const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[g1]) : 0.0f;
+      const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[g1]) : 0.0f;
 #pragma unroll
-        for (int sl = 0; sl < 4; ++sl) {
-          if (sl >= ns4) break;
-          float part[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part);
-          const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
-          acc[nt][0] = fmaf(slo, part[0], acc[nt][0]);
-          acc[nt][1] = fmaf(slo, part[1], acc[nt][1]);
-          acc[nt][2] = fmaf(shi, part[2], acc[nt][2]);
-          acc[nt][3] = fmaf(shi, part[3], acc[nt][3]);
-        }
+      for (int sl = 0; sl < 4; ++sl) {
+        if (sl >= ns4) break;
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part);
+        const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
+        acc[0] = fmaf(slo, part[0], acc[0]);
+        acc[1] = fmaf(slo, part[1], acc[1]);
+        acc[2] = fmaf(shi, part[2], acc[2]);
+        acc[3] = fmaf(shi, part[3], acc[3]);
       }
     }
     if (tb + kFPass >= n_tok) {  // the stage's rows are no longer needed
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
     }
-    // Hand the four K quarters to this pass's reducing warp (it rotates over
-    // the quad) through an exchange of kFRedBufs buffers; only the reducer
-    // waits.
+    // Hand the K quarter to the last of the quad's four warps to finish this
+    // pass (an arrival count in shared memory), through kFRedBufs buffers:
+    // no warp waits for the others; the last one sums the four quarters in
+    // a fixed order, applies SwiGLU and writes h.
     const uint32_t u = npass++;
     const int b = u % kFRedBufs;
     const uint32_t rpar = (u / kFRedBufs) & 1;
     fwait(&S.red_empty[q][b], rpar ^ 1, S, budget, p.status);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) S.u.red[q][b][wq][nt][lane][i] = acc[nt][i];
+    for (int i = 0; i < 4; ++i) S.u.red[q][b][wq][lane][i] = acc[i];
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&S.red_full[q][b]);
-    if (wq == static_cast<int>(u & 3)) {
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&S.red_cnt[q][b], 1) == 3 ? 1 : 0;
+      __threadfence_block();
+    }
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+      __syncwarp();
       bool wide = false;
-      fwait(&S.red_full[q][b], rpar, S, budget, p.status);
-      for (int nt = 0; nt < ntiles; ++nt) {
-        float r4[4] = {0.f, 0.f, 0.f, 0.f};
+      float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w2 = 0; w2 < 4; ++w2)  // fixed order
+      for (int w2 = 0; w2 < 4; ++w2)  // fixed order
 #pragma unroll
-          for (int i = 0; i < 4; ++i) r4[i] += S.u.red[q][b][w2][nt][lane][i];
+        for (int i = 0; i < 4; ++i) r4[i] += S.u.red[q][b][w2][lane][i];
 #pragma unroll
-        for (int col = 0; col < 2; ++col) {
-          const int idx = tb + 8 * nt + 2 * c + col;
-          if (idx < n_tok) {
-            const float xsv = S.xs[sh ? idx : S.perm[p0 + idx] / kK];  // undo 2^-s
-            const uint16_t hv = f32_to_bf16(silu_mul(r4[col] * xsv, r4[2 + col] * xsv));
-            // h in fp16 as well: a bf16 value (8 significant bits) below
-            // 2^15 in magnitude is exact in fp16 down to 2^-17; smaller
-            // ones land on fp16's subnormal grid (error < 2^-25).
-            const float hf = __uint_as_float(static_cast<uint32_t>(hv) << 16);
-            const uint16_t h16 = __half_as_ushort(__float2half_rn(hf));
-            wide |= !(fabsf(hf) < 32768.0f);
-            const size_t o = sh ? static_cast<size_t>(idx) * p.Is + i0 + g
-                                : static_cast<size_t>(p0 + idx) * p.I + i0 + g;
-            (sh ? p.h_shared : p.h_routed)[o] = hv;
-            (sh ? p.h16_shared : p.h16_routed)[o] = h16;
-          }
+      for (int col = 0; col < 2; ++col) {
+        const int idx = tb + 2 * c + col;
+        if (idx < n_tok) {
+          const float xsv = S.xs[sh ? idx : S.perm[p0 + idx] / kK];  // undo 2^-s
+          const uint16_t hv = f32_to_bf16(silu_mul(r4[col] * xsv, r4[2 + col] * xsv));
+          // h in fp16 as well: a bf16 value (8 significant bits) below
+          // 2^15 in magnitude is exact in fp16 down to 2^-17; smaller
+          // ones land on fp16's subnormal grid (error < 2^-25).
+          const float hf = __uint_as_float(static_cast<uint32_t>(hv) << 16);
+          const uint16_t h16 = __half_as_ushort(__float2half_rn(hf));
+          wide |= !(fabsf(hf) < 32768.0f);
+          const size_t o = sh ? static_cast<size_t>(idx) * p.Is + i0 + g
+                              : static_cast<size_t>(p0 + idx) * p.I + i0 + g;
+          (sh ? p.h_shared : p.h_routed)[o] = hv;
+          (sh ? p.h16_shared : p.h16_routed)[o] = h16;
         }
       }
       if (__any_sync(0xFFFFFFFFu, wide) && lane == 0) atomicOr(p.h_wide, 1u);
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.red_empty[q][b]);
+      if (lane == 0) {
+        S.red_cnt[q][b] = 0;
+        ptx::mbar_arrive(&S.red_empty[q][b]);
+      }
     }
   }
   if (n_tok == 0) {
@@ -926,7 +893,7 @@ __device__ __forceinline__ void down_unit_gemm(const FusedSmem &S, const FusedPa
   const int g = lane >> 2, c = lane & 3;
   const moe_bf16 *s_lo = sbase + g * ng;
   const moe_bf16 *s_hi = sbase + (g + 8) * ng;
-  for (int tb = 0; tb < n_tok; tb += kFPass) {
+  for (int tb = 0; tb < n_tok; tb += kFDownPass) {
     const int ntiles = min(2, (n_tok - tb + 7) / 8);
     const uint16_t *brow[2];
 #pragma unroll
@@ -1056,8 +1023,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     ptx::mbar_init(&S.routed, 1);
     for (int q = 0; q < kFQuads; ++q)
       for (int b = 0; b < kFRedBufs; ++b) {
-        ptx::mbar_init(&S.red_full[q][b], 4);   // the quad's four warps
         ptx::mbar_init(&S.red_empty[q][b], 1);  // the pass's reducing warp
+        S.red_cnt[q][b] = 0;
       }
     S.abort = 0;
     ptx::fence_mbar_init();
@@ -1090,22 +1057,44 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     // that the counter's round trip overlaps the issue of the units already
     // claimed; when there are few, single units keep the split even.
     const unsigned n_routed = static_cast<unsigned>(S.active[0] * wk.nIb);
-    const unsigned gu_claim = n_routed >= 24u * gridDim.x ? static_cast<unsigned>(kFClaim) : 1u;
-    // the first claim of CTA c is c itself (no round trip to the counter);
-    // the counter numbers the claims after the first G
-    const unsigned gu_base = gridDim.x * gu_claim;
-    unsigned claim = blockIdx.x * gu_claim;
+    const unsigned G = gridDim.x;
     int j = early ? 1 : 0;  // ring index of the next stage
+    // Few units (few tokens, so nearly equal costs): a static round-robin
+    // split with no claims, in which the shared units of the first Is / 8
+    // CTAs count as the first slots, so every CTA streams its units at once.
+    const bool static_gu = n_routed < 24u * G;
+    if (static_gu) {
+      const unsigned nS = static_cast<unsigned>(wk.nSb);
+      for (unsigned b = (blockIdx.x + G - nS % G) % G; b < n_routed && !aborted(S); b += G) {
+        const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
+        if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
+        ++j;
+      }
+    }
+    const unsigned gu_claim = static_cast<unsigned>(kFClaim);
+    // the first claim of CTA c is c itself (no round trip to the counter);
+    // the counter numbers the claims after the first G.  Two claims are
+    // requested ahead, so that the counter's round trip stays hidden even
+    // when the ring has room and a claim's units issue at once.  A CTA uses
+    // its claims in the order it requested them, which is increasing, so
+    // every claim below the total is used by the CTA that took it.
+    const unsigned gu_base = G * gu_claim;
+    unsigned claim = static_gu ? n_routed : blockIdx.x * gu_claim;
+    unsigned ahead0 = n_routed, ahead1 = n_routed;  // lane 0's requested claims
+    if (lane == 0 && claim < n_routed) {
+      ahead0 = gu_base + atomicAdd(p.unit_claims, gu_claim);
+      ahead1 = gu_base + atomicAdd(p.unit_claims, gu_claim);
+    }
     while (claim < n_routed && !aborted(S)) {
-      unsigned nx = 0;
-      if (lane == 0) nx = gu_base + atomicAdd(p.unit_claims, gu_claim);
       const unsigned end = min(claim + gu_claim, n_routed);
       for (unsigned b = claim; b < end && !aborted(S); ++b) {
         const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
         if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
         ++j;
       }
-      claim = __shfl_sync(0xFFFFFFFFu, nx, 0);
+      claim = __shfl_sync(0xFFFFFFFFu, ahead0, 0);
+      ahead0 = ahead1;
+      if (lane == 0 && claim < n_routed) ahead1 = gu_base + atomicAdd(p.unit_claims, gu_claim);
     }
     // one end marker per quad (each quad takes every kFQuads-th stage, so
     // kFQuads consecutive markers reach every quad once)
@@ -1134,20 +1123,29 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     // the CTAs that reach this point first would take several items per quad
     // when there are few (decode).
     const unsigned n_down = wk.row_owner ? 0u : static_cast<unsigned>(wk.n_exp * wk.nrb);
-    const unsigned G = gridDim.x;
     const unsigned per_claim = n_down >= 8u * G ? 2u : 1u;
     const unsigned cap = max(static_cast<unsigned>(kFQuads), (4u * n_down / 3u + G - 1u) / G);
-    unsigned taken = per_claim;
     const unsigned dn_base = G * per_claim;  // first claims static, as for gate|up
     claim = blockIdx.x * per_claim;
+    // requested ahead as for gate|up, up to cap items per CTA
+    unsigned taken = per_claim;
+    ahead0 = n_down;
+    ahead1 = n_down;
+    if (lane == 0 && claim < n_down) {
+      if (taken < cap) { ahead0 = dn_base + atomicAdd(p.down_claims, per_claim); taken += per_claim; }
+      if (taken < cap) { ahead1 = dn_base + atomicAdd(p.down_claims, per_claim); taken += per_claim; }
+    }
     while (claim < n_down && !aborted(S)) {
-      unsigned nx = n_down;
-      if (lane == 0 && taken < cap) nx = dn_base + atomicAdd(p.down_claims, per_claim);
-      taken += per_claim;
       const unsigned end = min(claim + per_claim, n_down);
       for (unsigned b = claim; b < end && !aborted(S); ++b, ++j)
         if (produce_down(S, p, wk, j, down_item(S, p, wk, b), pol, budget, lane)) issued_at(j);
-      claim = __shfl_sync(0xFFFFFFFFu, nx, 0);
+      claim = __shfl_sync(0xFFFFFFFFu, ahead0, 0);
+      ahead0 = ahead1;
+      ahead1 = n_down;
+      if (lane == 0 && claim < n_down && taken < cap) {
+        ahead1 = dn_base + atomicAdd(p.down_claims, per_claim);
+        taken += per_claim;
+      }
     }
     end_markers();
     // after an abort, let the copies already in flight land before exiting
@@ -1162,9 +1160,11 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     // ----------------------------------------------------------- consumers
     const int cw = consumer_warp(warp);
     const int q = cw >> 2, wq = cw & 3;
+    // bit 31 of the grid-barrier counter (used by consumer thread 0 only)
+    unsigned bar_phase = consumer_tid() == 0 ? ld_acquire_u32(p.grid_bar) & 0x80000000u : 0u;
     phase_router(S, p, cw, lane);
-    grid_sync(p.grid_bar, S, budget, p.status);
-    phase_select_lists(S, p, cw, lane, budget);
+    grid_sync(p.grid_bar, bar_phase, S, budget, p.status);
+    phase_select_lists(S, p, cw, lane, bar_phase, budget);
     if (consumer_tid() == 0) ptx::mbar_arrive(&S.routed);
     const Work wk = make_work(S, p);
     uint32_t npass = 0;
@@ -1174,7 +1174,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     // phases ahead of a slot's barrier)
     int j = q;
     while (consume_gu(S, p, j, q, wq, lane, budget, npass)) j += kFQuads;
-    grid_sync(p.grid_bar, S, budget, p.status);
+    grid_sync(p.grid_bar, bar_phase, S, budget, p.status);
     // every h is written: the down MMAs take the fp16 copies unless some h
     // is outside fp16's range
     const bool f16 = __ldcg(p.h_wide) == 0u;
@@ -1184,7 +1184,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       ptx::named_barrier(1, kFConsumers);
       combine_rows(S, p, wk);
     } else {
-      grid_sync(p.grid_bar, S, budget, p.status);
+      grid_sync(p.grid_bar, bar_phase, S, budget, p.status);
       phase_combine(S, p);
     }
   }

@@ -67,58 +67,78 @@ __device__ __forceinline__ void merge_level(uint64_t (&k)[8], int mask) {
   cx(k[0], k[1]); cx(k[2], k[3]); cx(k[4], k[5]); cx(k[6], k[7]);
 }
 
-// Select for one token with the whole warp, lane l holding the logits of
-// experts 8l .. 8l+7 in v.  On return every lane holds the token's ids (rank
-// order) and softmax weights; returns false for a non-finite row (ids -1,
-// weights 0).
+// Select for N tokens with the whole warp, lane l holding the logits of
+// experts 8l .. 8l+7 of token n in v[n].  The N merge networks are
+// independent, so their shuffles and compare-exchanges interleave.  On
+// return every lane holds each token's ids (rank order) and softmax weights;
+// ok[n] is false for a non-finite row (ids -1, weights 0).
+template <int N>
+__device__ __forceinline__ void select_top8_multi(const float (&v)[N][8], int lane,
+                                                  int (&ids)[N][8], float (&w)[N][8],
+                                                  bool (&ok)[N]) {
+  uint64_t k[N][8];
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    bool finite = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      finite &= isfinite(v[n][i]);
+      k[n][i] = rank_key(v[n][i], 8 * lane + i);
+    }
+    ok[n] = __all_sync(0xFFFFFFFFu, finite);
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) sort8(k[n]);
+  // the five levels run as a loop: the selection runs once per token and
+  // launch, so a compact body (fetched once) beats straight-line code
+#pragma unroll 1
+  for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+    for (int n = 0; n < N; ++n) merge_level(k[n], m);
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    // softmax over the 8 selected logits, max-subtracted (rank 0 is the max)
+    const float z0 = key_value(k[n][0]);
+    float e[8], s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      e[i] = expf(key_value(k[n][i]) - z0);
+      s += e[i];
+    }
+    const float inv = 1.0f / s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ids[n][i] = ok[n] ? key_id(k[n][i]) : -1;
+      w[n][i] = ok[n] ? e[i] * inv : 0.0f;
+    }
+    if (MOE_SABOTAGE == 1 && ok[n]) {  // test-only build (see common.cuh)
+      int e8 = ids[n][7];
+      bool taken = true;
+      while (taken) {
+        e8 = (e8 + 1) & 255;
+        taken = false;
+#pragma unroll
+        for (int i = 0; i < 7; ++i) taken |= ids[n][i] == e8;
+      }
+      ids[n][7] = e8;
+    }
+    if (MOE_SABOTAGE == 2) {  // test-only build (see common.cuh)
+      const float t = w[n][6];
+      w[n][6] = w[n][7];
+      w[n][7] = t;
+    }
+  }
+}
+
+// One token (see select_top8_multi); returns false for a non-finite row.
 __device__ __forceinline__ bool select_top8_regs(const float (&v)[8], int lane, int (&ids)[8],
                                                  float (&w)[8]) {
-  bool finite = true;
-  uint64_t k[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    finite &= isfinite(v[i]);
-    k[i] = rank_key(v[i], 8 * lane + i);
-  }
-  if (!__all_sync(0xFFFFFFFFu, finite)) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { ids[i] = -1; w[i] = 0.0f; }
-    return false;
-  }
-  sort8(k);
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) merge_level(k, m);
-  // softmax over the 8 selected logits, max-subtracted (rank 0 is the max)
-  const float z0 = key_value(k[0]);
-  float e[8], s = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    e[i] = expf(key_value(k[i]) - z0);
-    s += e[i];
-  }
-  const float inv = 1.0f / s;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    ids[i] = key_id(k[i]);
-    w[i] = e[i] * inv;
-  }
-  if (MOE_SABOTAGE == 1) {  // test-only build (see common.cuh)
-    int e8 = ids[7];
-    bool taken = true;
-    while (taken) {
-      e8 = (e8 + 1) & 255;
-      taken = false;
-#pragma unroll
-      for (int i = 0; i < 7; ++i) taken |= ids[i] == e8;
-    }
-    ids[7] = e8;
-  }
-  if (MOE_SABOTAGE == 2) {  // test-only build (see common.cuh)
-    const float t = w[6];
-    w[6] = w[7];
-    w[7] = t;
-  }
-  return true;
+  const float(&vv)[1][8] = reinterpret_cast<const float(&)[1][8]>(v);
+  int(&ii)[1][8] = reinterpret_cast<int(&)[1][8]>(ids);
+  float(&ww)[1][8] = reinterpret_cast<float(&)[1][8]>(w);
+  bool ok[1];
+  select_top8_multi<1>(vv, lane, ii, ww, ok);
+  return ok[0];
 }
 
 // As select_top8_regs, reading the 256 fp32 logits of `row` (16-byte aligned).
