@@ -24,8 +24,11 @@ Timing protocol:
   * cpu_baseline: the fp64 oracle on this host's cores, on a bounded sample.
 Multi-GPU: replicas only (the block has no exchange step); each rank runs
 the same workload on its own GPU and `value` sums the ranks' tokens.
-Unless --only is given, `workloads` also times the wide-row top-16 candidate
-selector (T = 8 and 64 rows of a 151,936-wide vocabulary, L2-cold).
+Unless --only is given, `workloads` also times a stack of eight decoder-layer
+blocks at T = 1 in one CUDA graph (moe_block_forward_residual: the block, the
+residual add and the next layer's RMS norm; per-layer time, L2-cold) and the
+wide-row top-16 candidate selector (T = 8 and 64 rows of a 151,936-wide
+vocabulary, L2-cold).
 """
 from __future__ import annotations
 
@@ -389,6 +392,86 @@ class Bench:
         return t / steps, 2 * self.T * self.d.H, 2 * self.T * self.d.H
 
 
+def bench_layers(moe, torch, dev, T: int, n_layers: int, steps: int, warmup: int,
+                 barrier=lambda: None, max_all=lambda v: v):
+    """A stack of decoder-layer blocks at decode size, as a serving loop runs
+    them: each layer is moe_block_forward_residual (the block, the residual
+    added in its combine, the next layer's RMS-normed input) on its own
+    weight bank (an expert-permuted copy of the seeded weights), x and the
+    residual carried in place from layer to layer, all layers captured in
+    one CUDA graph.  Two such stacks on distinct banks alternate between
+    replays, so L2 holds none of a replay's weights.  The same stacks of
+    plain moe_block_forward calls are timed beside them."""
+    name = "decode"
+    wl = W.WORKLOADS[name]
+    d = wl.dims
+    host_w = W.make_weights(d, wl.seed)
+    base = {k: (torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16
+                                                      else v)).to(dev) if v is not None else None)
+            for k, v in host_w.items()}
+    keep, banks = [], []
+    for r in range(2 * n_layers):
+        perm = torch.from_numpy(W.expert_permutation(256, wl.seed, 100 + r)).to(dev)
+        w = dict(base)
+        for k in ("w_router", "w13_q", "w13_s", "w2_q", "w2_s"):
+            w[k] = base[k].index_select(0, perm).contiguous()
+        keep.append(w)
+        banks.append(moe.weights_struct(w))
+    dims = moe.Dims.make(d.H, d.I, d.Is)
+    wsb = moe.moe_workspace_bytes(dims, T)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    x0 = torch.from_numpy(W.make_x(d, T, 4242)[0].view(np.int16)).to(dev)
+    r0 = torch.from_numpy(W.bf16_normal((T, d.H), W.stream_key(4243, "misc"), 4.0)
+                          .view(np.int16)).to(dev)
+    gammas = [torch.from_numpy(W.bf16_normal((d.H,), W.stream_key(4244, "misc", l), 1.0)
+                               .view(np.int16)).to(dev) for l in range(n_layers)]
+    x = x0.clone()
+    resid = r0.clone()
+    out = torch.empty_like(x0)
+    s = torch.cuda.Stream(device=dev)
+
+    def stack(k, residual):
+        for l in range(n_layers):
+            wb = banks[k * n_layers + l]
+            if residual:
+                moe.moe_block_forward_residual(dims, wb, x, T, resid, gammas[l], 1e-6, resid, x,
+                                               ws, wsb, s)
+            else:
+                moe.moe_block_forward(dims, wb, x, T, out, None, None, None, None, ws, wsb, s)
+
+    res = {}
+    for residual in (True, False):
+        with torch.cuda.stream(s):
+            for k in range(2):  # eager pass first (checks the calls)
+                stack(k, residual)
+            graphs = []
+            for k in range(2):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    stack(k, residual)
+                graphs.append(g)
+            for i in range(warmup):
+                graphs[i % 2].replay()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for i in range(steps):
+                graphs[i % 2].replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        barrier()
+        us = max_all(e0.elapsed_time(e1) * 1e3 / (steps * n_layers))
+        res["us_per_layer" if residual else "us_per_layer_block_only"] = us
+    assert moe.moe_read_status(ws) == 0
+    res.update({"T": T, "layers": n_layers, "kernels_per_layer": 2,
+                "tokens_per_s_per_layer": T / (res["us_per_layer"] * 1e-6),
+                "l2": "cold: two stacks of %d layers on distinct weight banks alternate" %
+                      n_layers})
+    return res
+
+
 def bench_candidates(moe, torch, dev, T: int, steps: int, warmup: int, peak_gbs: float,
                      barrier=lambda: None, max_all=lambda v: v, world: int = 1):
     """Wide-row top-16 candidates (the drafter's lm_head candidate selector):
@@ -687,6 +770,8 @@ def main():
         torch.cuda.empty_cache()
 
     if not args.only:
+        results["decode_T1_layers8"] = bench_layers(moe, torch, dev, 1, 8, args.steps,
+                                                    args.warmup, barrier, max_all)
         for Tc in (W.CANDIDATES_T, 64):
             results["candidates_T%d_N%d_k%d" % (Tc, W.CANDIDATES_N, W.CANDIDATES_K)] = \
                 bench_candidates(moe, torch, dev, Tc, args.steps, args.warmup, pk["hbm_gbs"],

@@ -179,6 +179,26 @@ moe_status moe_block_forward(const moe_dims *dims, const moe_weights *w,
                              float *logits_out, float *gate_logit_out,
                              void *workspace, size_t ws_bytes, void *stream);
 
+/* The block and the steps either side of it in a decoder layer (lucebox
+ * commit list: the residual add, RMS norm and weight multiply fused, with
+ * the residual sum kept beside the normalised output):
+ *   resid_out[t] = bf16(resid_in[t] + block(x)[t])   (the block's fp32 sum
+ *                  plus the residual, one round to nearest even), and
+ *   x_next[t]    = bf16(resid_out[t] / sqrt(mean(resid_out[t]^2) + eps)
+ *                  * gamma)                           (the next layer's input).
+ * x, resid_in, resid_out, x_next [T][H] bf16; gamma [H] bf16; eps >= 0 and
+ * finite.  resid_out may be resid_in (in place) and x_next may be x;
+ * x_next must not overlap either residual buffer, and the two residual
+ * buffers are the same or disjoint (otherwise MOE_ERR_INVALID_ARG).  Same
+ * routes, tolerance and workspace as moe_block_forward; one more kernel (the
+ * norm, one warp per token, its sum of squares in a fixed order, so the
+ * result does not depend on the batch). */
+moe_status moe_block_forward_residual(const moe_dims *dims, const moe_weights *w,
+                                      const moe_bf16 *x, int T, const moe_bf16 *resid_in,
+                                      const moe_bf16 *gamma, float eps, moe_bf16 *resid_out,
+                                      moe_bf16 *x_next, void *workspace, size_t ws_bytes,
+                                      void *stream);
+
 /* moe_block_forward with HOST x and out (ordinary or pinned host memory):
  * copies x in, runs the block, copies out back, then synchronises the stream
  * so that out is valid on return.  The staging buffers live in the workspace

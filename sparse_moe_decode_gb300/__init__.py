@@ -28,7 +28,7 @@ __all__ = [
     "DEV_NONFINITE", "DEV_BAD_EXPERT", "DEV_TIMEOUT", "EXPORTS",
     "moe_block_forward_profiled", "moe_block_kernel_count", "moe_block_kernel_name",
     "moe_block_forward_noalloc", "moe_topk_workspace_bytes", "moe_topk_candidates",
-    "moe_topk_merge",
+    "moe_topk_merge", "moe_block_forward_residual",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -45,7 +45,7 @@ EXPORTS = (
     "moe_clear_status", "moe_status_string", "moe_abi_version",
     "moe_block_forward_profiled", "moe_block_kernel_count", "moe_block_kernel_name",
     "moe_block_forward_noalloc", "moe_topk_workspace_bytes", "moe_topk_candidates",
-    "moe_topk_merge",
+    "moe_topk_merge", "moe_block_forward_residual",
 )
 
 
@@ -110,6 +110,8 @@ def lib() -> ctypes.CDLL:
                 "moe_topk_workspace_bytes": (Z, [I, I]),
                 "moe_topk_candidates": (I, [P, I, I, I, I, P, P, P, Z, P]),
                 "moe_topk_merge": (I, [P, P, I, I, I, P, P, P, Z, P]),
+                "moe_block_forward_residual": (I, [DP, WP, P, I, P, P, ctypes.c_float, P, P,
+                                                   P, Z, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -196,6 +198,15 @@ def moe_block_forward(dims, weights: Weights, x, T, out, ids_out=None, weights_o
                                    _a(out), _a(ids_out), _a(weights_out), _a(logits_out),
                                    _a(gate_logit_out), _a(workspace), int(ws_bytes), _s(stream)),
            "moe_block_forward")
+
+
+def moe_block_forward_residual(dims, weights: Weights, x, T, resid_in, gamma, eps, resid_out,
+                               x_next, workspace, ws_bytes, stream=None):
+    _check(lib().moe_block_forward_residual(ctypes.byref(dims), ctypes.byref(weights), _a(x),
+                                            int(T), _a(resid_in), _a(gamma), float(eps),
+                                            _a(resid_out), _a(x_next), _a(workspace),
+                                            int(ws_bytes), _s(stream)),
+           "moe_block_forward_residual")
 
 
 def moe_block_forward_host(dims, weights: Weights, x_host, T, out_host, workspace, ws_bytes,

@@ -185,12 +185,22 @@ struct Rec : StageRecorder {
   cudaError_t operator()() override { return ev ? cudaEventRecord(ev[i++], s) : cudaSuccess; }
 };
 
+// The steps after the block in a decoder layer (moe_block_forward_residual):
+// the residual added in the combine epilogue, then the next layer's input.
+struct Residual {
+  const moe_bf16 *resid;  // [T][H], added to the block's output before its rounding
+  const moe_bf16 *gamma;  // [H]
+  float eps;
+  moe_bf16 *x_next;       // [T][H]
+};
+
 // The decode/verify path: router -> select -> lists -> gate|up -> down -> combine.
 moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const moe_bf16 *x,
                                 int T, moe_bf16 *out, int32_t *ids_out, float *weights_out,
                                 float *logits_out, float *gate_logit_out, void *ws,
                                 const Layout &L, cudaStream_t s,
-                                cudaEvent_t const *events = nullptr) {
+                                cudaEvent_t const *events = nullptr,
+                                const Residual *res = nullptr) {
   const int H = d->hidden, I = d->expert_inter, Is = d->shared_inter;
   Rec rec{events, s};
   uint32_t *status = at<uint32_t>(ws, L.status);
@@ -214,8 +224,9 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
                                 at<float>(ws, L.sgate), hr, hs, out, ids_out, weights_out,
                                 logits_out, gate_logit_out, status, grid_bar, grid_bar + 1,
                                 grid_bar + 2, at<float>(ws, L.y), at<uint16_t>(ws, L.h16),
-                                grid_bar + 3, s));
+                                grid_bar + 3, res ? res->resid : nullptr, s));
     MOE_TRY(rec());
+    if (res) MOE_TRY(launch_rmsnorm(out, T, H, res->gamma, res->eps, res->x_next, s));
     return MOE_OK;
   }
   if (route == kRouteGemv) {
@@ -231,8 +242,9 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
     MOE_TRY(rec());
     MOE_TRY(launch_down_simt(T, H, I, Is, *w, lists, hr, hs, y, s));
     MOE_TRY(rec());
-    MOE_TRY(launch_combine(T, H, y, wts, wg ? sg : nullptr, out, s));
+    MOE_TRY(launch_combine(T, H, y, wts, wg ? sg : nullptr, out, s, res ? res->resid : nullptr));
     MOE_TRY(rec());
+    if (res) MOE_TRY(launch_rmsnorm(out, T, H, res->gamma, res->eps, res->x_next, s));
     return MOE_OK;
   }
   int4 *items = at<int4>(ws, L.items);
@@ -245,7 +257,8 @@ moe_status block_forward_device(const moe_dims *d, const moe_weights *w, const m
   MOE_TRY(launch_experts_tc(x, T, H, I, Is, *w, ids, lists, wts, wg ? sg : nullptr,
                             at<uint16_t>(ws, L.xs), at<uint16_t>(ws, L.x16),
                             at<float>(ws, L.xscale), at<float>(ws, L.hscale), hr, hs, at<float>(ws, L.acc), out, items,
-                            counters, status, s, rec));
+                            counters, status, s, rec, nullptr, res ? res->resid : nullptr));
+  if (res) MOE_TRY(launch_rmsnorm(out, T, H, res->gamma, res->eps, res->x_next, s));
   return MOE_OK;
 }
 
@@ -417,6 +430,33 @@ moe_status moe_block_forward(const moe_dims *dims, const moe_weights *w, const m
     return MOE_ERR_INVALID_ARG;
   return block_forward_device(dims, w, x, T, out, ids_out, weights_out, logits_out,
                               gate_logit_out, workspace, L, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_block_forward_residual(const moe_dims *dims, const moe_weights *w,
+                                      const moe_bf16 *x, int T, const moe_bf16 *resid_in,
+                                      const moe_bf16 *gamma, float eps, moe_bf16 *resid_out,
+                                      moe_bf16 *x_next, void *workspace, size_t ws_bytes,
+                                      void *stream) {
+  moe_status st = block_forward_check(dims, w, x, T, resid_out);
+  if (st != MOE_OK) return st;
+  Layout L;
+  if ((st = check_ws(dims, T, workspace, ws_bytes, L)) != MOE_OK) return st;
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return MOE_ERR_INVALID_ARG;  // also NaN
+  if (T == 0) return MOE_OK;
+  if (!ptr_ok(resid_in) || !ptr_ok(gamma) || !ptr_ok(x_next)) return MOE_ERR_INVALID_ARG;
+  // x_next is written after everything else has read the buffers, but it
+  // must not overlap the residual rows it is computed from
+  const uintptr_t bytes = sizeof(moe_bf16) * static_cast<uintptr_t>(T) * dims->hidden;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(x_next), b = reinterpret_cast<uintptr_t>(resid_out);
+  const uintptr_t c = reinterpret_cast<uintptr_t>(resid_in);
+  if ((a < b + bytes && b < a + bytes) || (a < c + bytes && c < a + bytes))
+    return MOE_ERR_INVALID_ARG;
+  // in place (resid_out == resid_in) or disjoint; a partial overlap would
+  // let one row's sum read another row's result
+  if (b != c && b < c + bytes && c < b + bytes) return MOE_ERR_INVALID_ARG;
+  const Residual res{resid_in, gamma, eps, x_next};
+  return block_forward_device(dims, w, x, T, resid_out, nullptr, nullptr, nullptr, nullptr,
+                              workspace, L, static_cast<cudaStream_t>(stream), nullptr, &res);
 }
 
 moe_status moe_block_forward_host(const moe_dims *dims, const moe_weights *w,

@@ -114,6 +114,7 @@ struct FusedParams {
   unsigned *h_wide;      // nonzero: some |h| >= 2^15 (or not finite); zeroed in phase R
   float *y;            // [T*K + T][H] down outputs: routed slots in list order, then shared
   moe_bf16 *out;       // [T][H]
+  const moe_bf16 *resid;  // [T][H] residual added before the rounding of out, or NULL
   int32_t *ids_out;
   float *weights_out, *logits_out, *gate_logit_out;
   uint32_t *status;
@@ -974,7 +975,9 @@ __device__ __forceinline__ void combine_rows(FusedSmem &S, const FusedParams &p,
       if (slot >= 0 && w != 0.0f) acc = fmaf(w, S.u.ys[r][slot], acc);
     }
     if (p.Is > 0 && S.sg[t] != 0.0f) acc = fmaf(S.sg[t], S.u.ys[r][p.T * kK + t], acc);
-    p.out[static_cast<size_t>(t) * p.H + wk.n0 + r] = f32_to_bf16(acc);
+    const size_t o = static_cast<size_t>(t) * p.H + wk.n0 + r;
+    if (p.resid) acc += bf16_to_f32(p.resid[o]);
+    p.out[o] = f32_to_bf16(acc);
   }
 }
 
@@ -1003,6 +1006,12 @@ __device__ __forceinline__ void phase_combine(FusedSmem &S, const FusedParams &p
           p.y + static_cast<size_t>(p.T * kK + t) * p.H + n));
       a0 = fmaf(S.sg[t], v.x, a0);
       a1 = fmaf(S.sg[t], v.y, a1);
+    }
+    if (p.resid) {
+      const uint32_t r2 =
+          *reinterpret_cast<const uint32_t *>(p.resid + static_cast<size_t>(t) * p.H + n);
+      a0 += bf16_lo(r2);
+      a1 += bf16_hi(r2);
     }
     const uint32_t o = static_cast<uint32_t>(f32_to_bf16(a0)) |
                        (static_cast<uint32_t>(f32_to_bf16(a1)) << 16);
@@ -1246,7 +1255,7 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, unsigned *unit_claims,
                                 unsigned *down_claims, float *y, uint16_t *h16,
-                                unsigned *h_wide, cudaStream_t s) {
+                                unsigned *h_wide, const moe_bf16 *resid, cudaStream_t s) {
   FusedParams p{};
   p.x = x; p.x16 = x16; p.xscale = xscale;
   p.T = T; p.H = H; p.I = I; p.Is = Is; p.KS = H / 512;
@@ -1257,7 +1266,7 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
   p.unit_claims = unit_claims;
   p.down_claims = down_claims;
   p.y = y;
-  p.h_routed = h_routed; p.h_shared = h_shared; p.out = out;
+  p.h_routed = h_routed; p.h_shared = h_shared; p.out = out; p.resid = resid;
   p.h16_routed = h16;
   p.h16_shared = h16 + static_cast<size_t>(T) * kK * I;
   p.h_wide = h_wide;

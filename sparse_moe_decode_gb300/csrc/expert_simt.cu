@@ -264,7 +264,8 @@ cudaError_t launch_down_simt(int T, int H, int I, int Is, const moe_weights &w, 
 
 __global__ void combine_kernel(int T, int H, const float *__restrict__ y,
                                const float *__restrict__ weights,
-                               const float *__restrict__ sgate, moe_bf16 *__restrict__ out) {
+                               const float *__restrict__ sgate, const moe_bf16 *resid,
+                               moe_bf16 *out) {
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int H4 = H / 4;
   if (idx >= static_cast<size_t>(T) * H4) return;
@@ -288,6 +289,11 @@ __global__ void combine_kernel(int T, int H, const float *__restrict__ y,
       acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);
     }
   }
+  if (resid) {  // the residual, added before the one rounding (in place allowed)
+    const uint2 r = *reinterpret_cast<const uint2 *>(resid + static_cast<size_t>(t) * H + n);
+    acc.x += bf16_lo(r.x); acc.y += bf16_hi(r.x);
+    acc.z += bf16_lo(r.y); acc.w += bf16_hi(r.y);
+  }
   uint2 o;
   o.x = pack_bf16x2(acc.x, acc.y);
   o.y = pack_bf16x2(acc.z, acc.w);
@@ -295,11 +301,12 @@ __global__ void combine_kernel(int T, int H, const float *__restrict__ y,
 }
 
 cudaError_t launch_combine(int T, int H, const float *y, const float *weights,
-                           const float *sgate, moe_bf16 *out, cudaStream_t s) {
+                           const float *sgate, moe_bf16 *out, cudaStream_t s,
+                           const moe_bf16 *resid) {
   const size_t n = static_cast<size_t>(T) * (H / 4);
   const int threads = 256;
   combine_kernel<<<static_cast<unsigned>((n + threads - 1) / threads), threads, 0, s>>>(
-      T, H, y, weights, sgate, out);
+      T, H, y, weights, sgate, resid, out);
   return cudaGetLastError();
 }
 

@@ -66,9 +66,16 @@ cudaError_t launch_down_simt(int T, int H, int I, int Is, const moe_weights &w, 
                              const moe_bf16 *h_routed, const moe_bf16 *h_shared, float *y,
                              cudaStream_t s);
 
-// A7: out[t] = bf16(sum_j w[t][j] y[t][j] + sg[t] y[t][K]).
+// A7: out[t] = bf16(sum_j w[t][j] y[t][j] + sg[t] y[t][K] (+ resid[t])).
 cudaError_t launch_combine(int T, int H, const float *y, const float *weights,
-                           const float *sgate, moe_bf16 *out, cudaStream_t s);
+                           const float *sgate, moe_bf16 *out, cudaStream_t s,
+                           const moe_bf16 *resid = nullptr);
+
+// The next layer's input from the residual sum r [T][H] (bf16): x_next =
+// bf16(r / sqrt(mean(r^2) + eps) * gamma), one warp per token, the sum of
+// squares in a fixed order.
+cudaError_t launch_rmsnorm(const moe_bf16 *r, int T, int H, const moe_bf16 *gamma, float eps,
+                           moe_bf16 *x_next, cudaStream_t s);
 
 // ---- decode-size T: the fused persistent kernel (decode_fused.cu)
 
@@ -82,7 +89,8 @@ constexpr int kFusedMaxI = 2048;  // expert / shared intermediate
 bool fused_decode_supported(int T, int H, int I, int Is);
 size_t fused_smem_bytes();
 
-// A1..A7 in one cooperative launch.  x16 [T][H] fp16 and xscale [T] (the
+// A1..A7 in one cooperative launch (resid, nullable: a residual [T][H] added
+// to out before its rounding).  x16 [T][H] fp16 and xscale [T] (the
 // tokens' scaled fp16 copies), rpart [T][H/512][260] fp32, sel_ids [T][K],
 // sel_w [T][K], sel_sg [T], h_routed [T*K][I], h_shared [T][Is],
 // y [T*K + T][H] fp32, h16 [T*K*I + T*Is] fp16, unit_claims, down_claims
@@ -96,7 +104,7 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
                                 float *weights_out, float *logits_out, float *gate_logit_out,
                                 uint32_t *status, unsigned *grid_bar, unsigned *unit_claims,
                                 unsigned *down_claims, float *y, uint16_t *h16,
-                                unsigned *h_wide, cudaStream_t s);
+                                unsigned *h_wide, const moe_bf16 *resid, cudaStream_t s);
 
 // ---- prefill-size T: tcgen05 GEMMs (tc_gemm.cu: router; tc_expert.cu: experts)
 
@@ -139,7 +147,8 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                               float *hscale,
                               moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
                               moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
-                              cudaStream_t s, StageRecorder &rec, float *y_slots = nullptr);
+                              cudaStream_t s, StageRecorder &rec, float *y_slots = nullptr,
+                              const moe_bf16 *resid = nullptr);
 
 // Per-expert entry counts of ids [T][K] into counts [E] (zeroed here); ids
 // >= E set MOE_DEV_BAD_EXPERT.

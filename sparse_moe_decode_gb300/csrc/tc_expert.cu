@@ -1040,8 +1040,11 @@ __global__ void expert_counts_kernel(const int32_t *__restrict__ ids, int n,
     if (hist[i]) atomicAdd(counts + i, hist[i]);
 }
 
+// out = bf16(acc (+ resid)), four elements per thread and step; resid (the
+// residual, bf16, may be the same buffer as out) is added before the one
+// rounding.
 __global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
-                                   moe_bf16 *__restrict__ out) {
+                                   const moe_bf16 *resid, moe_bf16 *out) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n4;
        i0 += 4 * stride) {
@@ -1052,6 +1055,11 @@ __global__ void acc_to_bf16_kernel(const float *__restrict__ acc, size_t n4,
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       if (i0 + u * stride < n4) {
+        if (resid) {
+          const uint2 r = reinterpret_cast<const uint2 *>(resid)[i0 + u * stride];
+          v[u].x += bf16_lo(r.x); v[u].y += bf16_hi(r.x);
+          v[u].z += bf16_lo(r.y); v[u].w += bf16_hi(r.y);
+        }
         uint2 o;
         o.x = pack_bf16x2(v[u].x, v[u].y);
         o.y = pack_bf16x2(v[u].z, v[u].w);
@@ -1117,7 +1125,8 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
                               float *hscale,
                               moe_bf16 *h_routed, moe_bf16 *h_shared, float *out_acc,
                               moe_bf16 *out, int4 *items, int *counters, uint32_t *status,
-                              cudaStream_t s, StageRecorder &rec, float *y_slots) {
+                              cudaStream_t s, StageRecorder &rec, float *y_slots,
+                              const moe_bf16 *resid) {
 #define TC_STEP(expr)                          \
   do {                                         \
     cudaError_t e_ = (expr);                   \
@@ -1203,7 +1212,7 @@ cudaError_t launch_experts_tc(const moe_bf16 *x, int T, int H, int I, int Is,
   TC_STEP(launch_down_split(dm, q, s));
   if (y_slots) return cudaSuccess;
   const size_t n4 = static_cast<size_t>(T) * H / 4;
-  acc_to_bf16_kernel<<<tc_sm_count() * 4, 256, 0, s>>>(out_acc, n4, out);
+  acc_to_bf16_kernel<<<tc_sm_count() * 4, 256, 0, s>>>(out_acc, n4, resid, out);
   TC_STEP(cudaGetLastError());
   return cudaSuccess;
 #undef TC_STEP

@@ -166,3 +166,29 @@ def test_noalloc_limit_and_host_checks(moe):
     bad = moe.Dims.make(2048, 512, 512, top_k=4)
     assert L.moe_block_forward_noalloc(ctypes.byref(bad), ctypes.byref(w), fake, 4, fake,
                                        None) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_residual_entry_host_checks(moe):
+    """moe_block_forward_residual rejects bad eps and overlapping buffers on
+    the host, before anything is enqueued."""
+    L = moe.lib()
+    d = moe.Dims.make(512, 128, 128)
+    fake = 1 << 20
+    w = moe.Weights(*([fake] * 10))
+    T, row = 4, 512 * 2
+    ws = fake * 64
+    wsb = moe.moe_workspace_bytes(d, T)
+
+    def call(r_in, r_out, x_next, eps=1e-6, x=fake):
+        return L.moe_block_forward_residual(ctypes.byref(d), ctypes.byref(w), x, T, r_in, fake,
+                                            eps, r_out, x_next, ws, wsb, None)
+
+    a, b, c = fake * 2, fake * 4, fake * 6
+    assert call(a, b, c, eps=-1.0) == moe.MOE_ERR_INVALID_ARG
+    assert call(a, b, c, eps=float("nan")) == moe.MOE_ERR_INVALID_ARG
+    assert call(a, b, b + row) == moe.MOE_ERR_INVALID_ARG       # x_next inside resid_out
+    assert call(a, b, a) == moe.MOE_ERR_INVALID_ARG             # x_next over resid_in
+    assert call(a, a + row, c) == moe.MOE_ERR_INVALID_ARG       # residuals partly overlap
+    assert call(None, b, c) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_block_forward_residual(ctypes.byref(d), ctypes.byref(w), fake, T, a, fake,
+                                        1e-6, b, c, ws, 16, None) == moe.MOE_ERR_WORKSPACE

@@ -11,7 +11,8 @@ import pytest
 
 import oracle
 import workloads as W
-from util import assert_out_close, bits, gpu_env, ncpu, near_tie, to_dev, workload, workload_dev
+from util import (assert_out_close, bf16_f64, bits, gpu_env, ncpu, near_tie, to_dev, workload,
+                  workload_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -120,37 +121,60 @@ def test_block_prefill_T2048_every_token(env):
     assert counts.min() > 0  # uniform routing touches every expert
 
 
-def _ulps(a_bits, b_bits):
-    """Distance in bf16 units in the last place between two bit arrays (on
-    the ordered integer line of bf16 values)."""
-    def line(b):
-        v = b.astype(np.int32)
-        return np.where(v & 0x8000, 0x8000 - v, v)
-    return np.abs(line(a_bits) - line(b_bits))
+def _bf16_ulp(b):
+    """Spacing of bf16 values at each value (bits), from its magnitude up."""
+    m = (b.astype(np.int32) & 0x7FFF)
+    m = np.minimum(m, 0x7F7F)
+    return (W.bf16_bits_to_f32((m + 1).astype(np.uint16)).astype(np.float64) -
+            W.bf16_bits_to_f32(m.astype(np.uint16)).astype(np.float64))
+
+
+def _order_bound(moe, dev, x, g):
+    """Per output element, how far two fp32 summation orders of the block's
+    nine terms (w_j y_j, then sg y_s) may land apart before the bf16
+    rounding: each order is within 8 * 2^-24 * sum|terms| of the exact sum
+    (terms from the oracle's per-slot outputs on the GPU's routing)."""
+    dims, w = workload("prefill")
+    ref = oracle.block_forward(dims.as_dict(), w, x, route_logits=g["logits"],
+                               route_gate=g["gate"], nthreads=ncpu(), want=("y",))
+    terms = np.abs(ref["y"][:, :8] * ref["weights"][:, :, None]).sum(axis=1)
+    terms += np.abs(ref["y"][:, 8] * ref["sgate"][:, None])
+    return 16.0 * 2.0 ** -24 * terms
+
+
+def _check_reordered(a_bits, b_bits, bound, what, capsys):
+    """a and b differ at most by the summation-order bound plus one bf16 ulp
+    of the larger of the two (its rounding); the counts are printed."""
+    da = np.abs(bf16_f64(a_bits) - bf16_f64(b_bits))
+    ulp = np.maximum(_bf16_ulp(a_bits), _bf16_ulp(b_bits))
+    n_diff = int((da > 0).sum())
+    in_ulps = da / ulp
+    with capsys.disabled():
+        print("\n  %s: %d of %d outputs differ, max %.0f ulp, max |diff| / bound %.3g" %
+              (what, n_diff, da.size, in_ulps.max(), (np.maximum(da - ulp, 0) / bound).max()))
+    assert (da <= bound + ulp).all(), what
 
 
 def test_block_tensor_core_route_run_to_run(env, capsys):
-    """The tcgen05 route adds the routed terms with fp32 atomics, so the last
-    fp32 bit of a sum may depend on their order: three runs of the prefill
-    workload differ by at most one bf16 ulp anywhere (the count is printed)."""
+    """The tcgen05 route adds the routed terms with fp32 atomics in the order
+    they arrive, so runs of the prefill workload may differ by a reordered
+    fp32 sum of nine terms (at most 16 * 2^-24 * sum|terms|) plus one bf16
+    ulp of rounding; routing and logits do not differ at all."""
     moe, dev = env
     dims, w, x, _ = W.workload_inputs("prefill")
     runs = [forward(moe, dev, "prefill", x)[2] for _ in range(3)]
+    bound = _order_bound(moe, dev, x, runs[0])
     for r in runs[1:]:
         assert np.array_equal(r["ids"], runs[0]["ids"])
         assert np.array_equal(r["logits"], runs[0]["logits"])
-        u = _ulps(r["out"], runs[0]["out"])
-        with capsys.disabled():
-            print("\n  tcgen05 route run-to-run: %d of %d outputs differ, max %d ulp" %
-                  (int((u > 0).sum()), u.size, int(u.max())))
-        assert u.max() <= 1
+        _check_reordered(r["out"], runs[0]["out"], bound, "tcgen05 route run-to-run", capsys)
 
 
 def test_block_batch_width_invariance_tensor_core_route(env, capsys):
     """Tokens 0..64 of the prefill workload as a T = 65 batch against the
     same tokens inside the T = 2048 batch (both on the tcgen05 route):
-    identical routing and logits, outputs within one bf16 ulp (the count of
-    differing outputs is printed)."""
+    identical routing and logits, outputs within the summation-order bound
+    of the run-to-run test."""
     moe, dev = env
     dims, w, x, _ = W.workload_inputs("prefill")
     full = forward(moe, dev, "prefill", x)[2]
@@ -158,11 +182,10 @@ def test_block_batch_width_invariance_tensor_core_route(env, capsys):
     assert np.array_equal(part["logits"], full["logits"][:65])
     assert np.array_equal(part["ids"], full["ids"][:65])
     assert np.array_equal(part["weights"], full["weights"][:65])
-    u = _ulps(part["out"], full["out"][:65])
-    with capsys.disabled():
-        print("\n  tcgen05 route T=65 vs T=2048: %d of %d outputs differ, max %d ulp" %
-              (int((u > 0).sum()), u.size, int(u.max())))
-    assert u.max() <= 1
+    g65 = {k: v[:65] for k, v in full.items()}
+    bound = _order_bound(moe, dev, x[:65], g65)
+    _check_reordered(part["out"], full["out"][:65], bound, "tcgen05 route T=65 vs T=2048",
+                     capsys)
 
 
 def test_block_batch_width_invariance_decode_route(env):
