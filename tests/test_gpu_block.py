@@ -279,3 +279,80 @@ def test_block_fused_wide_h_takes_bf16_down(env, T):
         _, _, _, blk = forward(moe, dev, "decode", xs)
         assert int(blk.workspace[16:20].view(torch.int32).item()) == wide
         check_block(moe, dev, "decode", xs)
+
+
+def _check_custom(moe, dev, dims, w, x, n_sample=None, seed=0, what=""):
+    """Block forward at any dims against the oracle on the GPU's routing
+    (every token, or a seeded sample of n_sample tokens)."""
+    import torch
+    T = x.shape[0]
+    wd = {k: to_dev(v, dev) for k, v in w.items()}
+    blk = moe.MoEBlock(dims.H, dims.I, dims.Is, wd, T_max=T, device=dev)
+    out = torch.empty((T, dims.H), dtype=torch.int16, device=dev)
+    logits = torch.empty((T, 256), dtype=torch.float32, device=dev)
+    gate = torch.empty((T,), dtype=torch.float32, device=dev) if dims.Is else None
+    ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
+    blk.forward(to_dev(x, dev), out=out, ids=ids, logits=logits, gate_logit=gate)
+    torch.cuda.synchronize()
+    assert blk.status() == 0
+    toks = None if n_sample is None else sample_tokens(T, n_sample, seed)
+    rows = np.arange(T) if toks is None else toks
+    ref = oracle.block_forward(dims.as_dict(), w, x, tokens=toks, route_logits=logits.cpu().numpy(),
+                               route_gate=None if gate is None else gate.cpu().numpy(),
+                               nthreads=ncpu(), want=("out",))
+    assert np.array_equal(ids.cpu().numpy()[rows], ref["ids"][rows])
+    assert_out_close(bits(out)[rows], ref["out"][rows], what)
+    return bits(out), ids.cpu().numpy()
+
+
+@pytest.mark.parametrize("T", [4, 33, 100])
+def test_block_without_shared_expert(env, T):
+    """shared_inter = 0: no gate row, no shared term, on every route."""
+    moe, dev = env
+    dims = W.Dims(H=512, I=128, Is=0)
+    w = W.make_weights(dims, 31)
+    x, _ = W.make_x(dims, T, 32 + T)
+    _check_custom(moe, dev, dims, w, x, what="Is=0 T=%d" % T)
+
+
+@pytest.mark.parametrize("T", [8, 40, 100])
+def test_block_expert_and_shared_sizes_differ(env, T):
+    """I = 256, Is = 128 (the fused kernel's stages hold the larger size)."""
+    moe, dev = env
+    dims = W.Dims(H=1024, I=256, Is=128)
+    w = W.make_weights(dims, 41)
+    x, _ = W.make_x(dims, T, 42 + T)
+    _check_custom(moe, dev, dims, w, x, what="I=256 Is=128 T=%d" % T)
+
+
+@pytest.mark.parametrize("T", [1, 12, 33, 100])
+def test_block_all_zero_input(env, T):
+    """x = 0: every logit is 0, so the total order picks experts 0..7 (the
+    lower id wins a tie), the softmax weights are all 1/8, and the output is
+    exactly zero on every route."""
+    import torch
+    moe, dev = env
+    dims, _ = workload("pr1")
+    wd = workload_dev("pr1", dev)
+    x = np.zeros((T, dims.H), np.uint16)
+    blk = moe.MoEBlock(dims.H, dims.I, dims.Is, wd, T_max=T, device=dev)
+    out = torch.full((T, dims.H), -1, dtype=torch.int16, device=dev)
+    ids = torch.empty((T, 8), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, 8), dtype=torch.float32, device=dev)
+    blk.forward(to_dev(x, dev), out=out, ids=ids, weights=wts)
+    torch.cuda.synchronize()
+    assert blk.status() == 0
+    assert (ids.cpu().numpy() == np.arange(8)).all()
+    assert (wts.cpu().numpy() == np.float32(0.125)).all()
+    o = bits(out)
+    assert ((o == 0) | (o == 0x8000)).all()  # +0 or -0
+
+
+def test_block_largest_T(env):
+    """T = 65536, the largest supported batch (tcgen05 route, PR1 dims), on a
+    seeded sample of tokens including the first and the last."""
+    moe, dev = env
+    dims, w = workload("pr1")
+    T = 65536
+    x, _ = W.make_x(dims, T, 65)
+    _check_custom(moe, dev, dims, w, x, n_sample=24, seed=5, what="T=65536")
