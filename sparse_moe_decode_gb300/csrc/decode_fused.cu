@@ -68,9 +68,10 @@ namespace {
 constexpr int kFQuads = 3;
 constexpr int kFConsumerWarps = 4 * kFQuads;
 constexpr int kFConsumers = kFConsumerWarps * 32;
-// 16 warps, 128 registers: warp 0 is the producer, alone on its SM
-// sub-partition (warps 4, 8 and 12 idle), so that the consumers' issue does
-// not delay its copies; warps w with w mod 4 != 0 are consumer warps.
+// 16 warps, 128 registers: warp 0 is the producer, on an SM sub-partition
+// with no consumer warp, so that the consumers' issue does not delay its
+// copies; warps w with w mod 4 != 0 are consumer warps; warps 4, 8 and 12
+// (the producer's sub-partition) reduce the gate|up passes of quads 0, 1, 2.
 constexpr int kFThreads = 512;
 
 // consumer warp index (0 .. 11) of warp w (w mod 4 != 0)
@@ -142,8 +143,10 @@ struct FusedSmem {
   int32_t active[kE + 1];
   uint64_t full[kFStages], empty[kFStages], routed;
   int2 stage_unit[kFStages];  // (expert, first row pair | first output row); x < 0: end
-  uint64_t red_empty[kFQuads][kFRedBufs];
-  int red_cnt[kFQuads][kFRedBufs];  // warps that have stored their pass's quarter
+  uint64_t red_full[kFQuads][kFRedBufs];   // the quad's four quarters are stored
+  uint64_t red_empty[kFQuads][kFRedBufs];  // the reducer has read them
+  uint64_t red_done[kFQuads];              // the reducer wrote its last h
+  int4 red_meta[kFQuads][kFRedBufs];       // the pass: (expert | -1 = end, i0, tb, 0)
   int abort;
 };
 
@@ -592,7 +595,9 @@ __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedPara
   if (p.T <= kFLocalSelT) {
     if (cwarp < p.T) select_token(S, p, cwarp, lane, true);
   } else {
-    const int t = blockIdx.x * kFConsumerWarps + cwarp;
+    // one token per CTA (consumer warp 0): the merge network is bound by
+    // issue, so tokens that share an SM sub-partition take turns
+    const int t = blockIdx.x + gridDim.x * cwarp;
     if (t < p.T) select_token(S, p, t, lane, false);
     grid_sync(p.grid_bar, phase, S, budget, p.status);
     for (int i = tid; i < p.T * kK; i += kFConsumers) {
@@ -732,20 +737,107 @@ __device__ __forceinline__ void unit_gemm(const uint8_t *rows, int stride, int k
         for (int i = 0; i < 8; ++i) xw[sl][i] = 0u;
       }
     }
+    if (ns == 4) {
+      // a full batch with no branch between its slices, so that their
+      // independent MMA chains interleave
+      float part[4][4];
 #pragma unroll
-    for (int sl = 0; sl < 4; ++sl) {
-      if (sl >= ns) break;
-      const int k0 = kk + 64 * sl;
-      const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
-      if (F16) mma_slice_f16(rows, stride, k0, g, c, xw[sl], part);
-      else mma_slice(rows, stride, k0, g, c, xw[sl], part);
-      acc[0] = fmaf(slo, part[0], acc[0]);
-      acc[1] = fmaf(slo, part[1], acc[1]);
-      acc[2] = fmaf(shi, part[2], acc[2]);
-      acc[3] = fmaf(shi, part[3], acc[3]);
+      for (int sl = 0; sl < 4; ++sl) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) part[sl][i] = 0.0f;
+        if (F16) mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part[sl]);
+        else mma_slice(rows, stride, kk + 64 * sl, g, c, xw[sl], part[sl]);
+      }
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        const int k0 = kk + 64 * sl;
+        const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
+        acc[0] = fmaf(slo, part[sl][0], acc[0]);
+        acc[1] = fmaf(slo, part[sl][1], acc[1]);
+        acc[2] = fmaf(shi, part[sl][2], acc[2]);
+        acc[3] = fmaf(shi, part[sl][3], acc[3]);
+      }
+    } else {
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl) {
+        if (sl >= ns) break;
+        const int k0 = kk + 64 * sl;
+        const float slo = bf16_to_f32(s_lo[k0 / kG]), shi = bf16_to_f32(s_hi[k0 / kG]);
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        if (F16) mma_slice_f16(rows, stride, k0, g, c, xw[sl], part);
+        else mma_slice(rows, stride, k0, g, c, xw[sl], part);
+        acc[0] = fmaf(slo, part[0], acc[0]);
+        acc[1] = fmaf(slo, part[1], acc[1]);
+        acc[2] = fmaf(shi, part[2], acc[2]);
+        acc[3] = fmaf(shi, part[3], acc[3]);
+      }
     }
   }
+}
+
+// One consumer warp's K quarter of gate|up pass u of quad q into the quad's
+// exchange buffer; warp 0 of the quad also stores the pass (m.x = -1: the
+// quad's gate|up units are done).
+__device__ __forceinline__ void hand_off(FusedSmem &S, const FusedParams &p, int q, int wq,
+                                         int lane, uint32_t u, int4 m, const float (&acc)[4],
+                                         uint64_t budget) {
+  const int b = u % kFRedBufs;
+  fwait(&S.red_empty[q][b], ((u / kFRedBufs) & 1) ^ 1, S, budget, p.status);
+  *reinterpret_cast<float4 *>(S.u.red[q][b][wq][lane]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  if (wq == 0 && lane == 0) S.red_meta[q][b] = m;
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(&S.red_full[q][b]);
+}
+
+// Reducer warp of quad q: for each gate|up pass, the four K quarters added in
+// a fixed order, 2^s undone, h = bf16(silu(gate) * up) and its fp16 copy
+// (r17) written.  A bf16 value (8 significant bits) below 2^15 in magnitude
+// is exact in fp16 down to 2^-17; smaller ones land on fp16's subnormal grid
+// (error < 2^-25); a larger one sets h_wide.
+__device__ __forceinline__ void reduce_gu(FusedSmem &S, const FusedParams &p, int q, int lane,
+                                          uint64_t budget) {
+  const int g = lane >> 2, c = lane & 3;
+  bool wide = false;
+  for (uint32_t u = 0;; ++u) {
+    const int b = u % kFRedBufs;
+    fwait(&S.red_full[q][b], (u / kFRedBufs) & 1, S, budget, p.status);
+    if (aborted(S)) break;
+    const int4 m = S.red_meta[q][b];
+    if (m.x < 0) break;
+    const int e = m.x, i0 = m.y, tb = m.z;
+    const bool sh = e == kE;
+    const int n_tok = sh ? p.T : S.counts[e];
+    const int p0 = sh ? 0 : S.offsets[e];
+    float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w2 = 0; w2 < 4; ++w2) {  // fixed order
+      const float4 v = *reinterpret_cast<const float4 *>(S.u.red[q][b][w2][lane]);
+      r4[0] += v.x; r4[1] += v.y; r4[2] += v.z; r4[3] += v.w;
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.red_empty[q][b]);
+#pragma unroll
+    for (int col = 0; col < 2; ++col) {
+      const int idx = tb + 2 * c + col;
+      if (idx < n_tok) {
+        const float xsv = S.xs[sh ? idx : S.perm[p0 + idx] / kK];  // undo 2^-s
+        const uint16_t hv = f32_to_bf16(silu_mul(r4[col] * xsv, r4[2 + col] * xsv));
+        const float hf = __uint_as_float(static_cast<uint32_t>(hv) << 16);
+        const uint16_t h16 = __half_as_ushort(__float2half_rn(hf));
+        wide |= !(fabsf(hf) < 32768.0f);
+        const size_t o = sh ? static_cast<size_t>(idx) * p.Is + i0 + g
+                            : static_cast<size_t>(p0 + idx) * p.I + i0 + g;
+        (sh ? p.h_shared : p.h_routed)[o] = hv;
+        (sh ? p.h16_shared : p.h16_routed)[o] = h16;
+      }
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, wide) && lane == 0) atomicOr(p.h_wide, 1u);
+  // every h of this quad (and the flag) ordered before the consumers' grid
+  // barrier, which follows their wait for red_done
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(&S.red_done[q]);
 }
 
 // Phase W consumer: gate|up unit j of this CTA, by quad q (warp wq of 4
@@ -761,6 +853,8 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
   if (un.x < 0) {
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
+    const float none[4] = {0.f, 0.f, 0.f, 0.f};
+    hand_off(S, p, q, wq, lane, npass++, make_int4(-1, 0, 0, 0), none, budget);
     return false;
   }
   const int e = un.x, i0 = un.y;
@@ -804,72 +898,45 @@ __device__ __forceinline__ bool consume_gu(FusedSmem &S, const FusedParams &p, i
       const float slo0 = bf16_to_f32(s_gate[g0]), shi0 = bf16_to_f32(s_up[g0]);
       const float slo1 = ns4 > 2 ? bf16_to_f32(s_gate[g1]) : 0.0f;
       const float shi1 = ns4 > 2 ? bf16_to_f32(s_up[g1]) : 0.0f;
+      if (ns4 == 4) {
+        // a full batch with no branch between its slices, so that their
+        // independent MMA chains interleave
+        float part[4][4];
 #pragma unroll
-      for (int sl = 0; sl < 4; ++sl) {
-        if (sl >= ns4) break;
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part);
-        const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
-        acc[0] = fmaf(slo, part[0], acc[0]);
-        acc[1] = fmaf(slo, part[1], acc[1]);
-        acc[2] = fmaf(shi, part[2], acc[2]);
-        acc[3] = fmaf(shi, part[3], acc[3]);
+        for (int sl = 0; sl < 4; ++sl) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) part[sl][i] = 0.0f;
+          mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part[sl]);
+        }
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+          const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
+          acc[0] = fmaf(slo, part[sl][0], acc[0]);
+          acc[1] = fmaf(slo, part[sl][1], acc[1]);
+          acc[2] = fmaf(shi, part[sl][2], acc[2]);
+          acc[3] = fmaf(shi, part[sl][3], acc[3]);
+        }
+      } else {
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+          if (sl >= ns4) break;
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_slice_f16(rows, stride, kk + 64 * sl, g, c, xw[sl], part);
+          const float slo = sl < 2 ? slo0 : slo1, shi = sl < 2 ? shi0 : shi1;
+          acc[0] = fmaf(slo, part[0], acc[0]);
+          acc[1] = fmaf(slo, part[1], acc[1]);
+          acc[2] = fmaf(shi, part[2], acc[2]);
+          acc[3] = fmaf(shi, part[3], acc[3]);
+        }
       }
     }
     if (tb + kFPass >= n_tok) {  // the stage's rows are no longer needed
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
     }
-    // Hand the K quarter to the last of the quad's four warps to finish this
-    // pass (an arrival count in shared memory), through kFRedBufs buffers:
-    // no warp waits for the others; the last one sums the four quarters in
-    // a fixed order, applies SwiGLU and writes h.
-    const uint32_t u = npass++;
-    const int b = u % kFRedBufs;
-    const uint32_t rpar = (u / kFRedBufs) & 1;
-    fwait(&S.red_empty[q][b], rpar ^ 1, S, budget, p.status);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) S.u.red[q][b][wq][lane][i] = acc[i];
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicAdd(&S.red_cnt[q][b], 1) == 3 ? 1 : 0;
-      __threadfence_block();
-    }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-      __syncwarp();
-      bool wide = false;
-      float r4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w2 = 0; w2 < 4; ++w2)  // fixed order
-#pragma unroll
-        for (int i = 0; i < 4; ++i) r4[i] += S.u.red[q][b][w2][lane][i];
-#pragma unroll
-      for (int col = 0; col < 2; ++col) {
-        const int idx = tb + 2 * c + col;
-        if (idx < n_tok) {
-          const float xsv = S.xs[sh ? idx : S.perm[p0 + idx] / kK];  // undo 2^-s
-          const uint16_t hv = f32_to_bf16(silu_mul(r4[col] * xsv, r4[2 + col] * xsv));
-          // h in fp16 as well: a bf16 value (8 significant bits) below
-          // 2^15 in magnitude is exact in fp16 down to 2^-17; smaller
-          // ones land on fp16's subnormal grid (error < 2^-25).
-          const float hf = __uint_as_float(static_cast<uint32_t>(hv) << 16);
-          const uint16_t h16 = __half_as_ushort(__float2half_rn(hf));
-          wide |= !(fabsf(hf) < 32768.0f);
-          const size_t o = sh ? static_cast<size_t>(idx) * p.Is + i0 + g
-                              : static_cast<size_t>(p0 + idx) * p.I + i0 + g;
-          (sh ? p.h_shared : p.h_routed)[o] = hv;
-          (sh ? p.h16_shared : p.h16_routed)[o] = h16;
-        }
-      }
-      if (__any_sync(0xFFFFFFFFu, wide) && lane == 0) atomicOr(p.h_wide, 1u);
-      __syncwarp();
-      if (lane == 0) {
-        S.red_cnt[q][b] = 0;
-        ptx::mbar_arrive(&S.red_empty[q][b]);
-      }
-    }
+    // Hand the K quarter to the quad's reducer warp (kFRedBufs buffers), which
+    // adds the four quarters in a fixed order, applies SwiGLU and writes h.
+    hand_off(S, p, q, wq, lane, npass++, make_int4(e, i0, tb, 0), acc, budget);
   }
   if (n_tok == 0) {
     __syncwarp();
@@ -1030,11 +1097,13 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       ptx::mbar_init(&S.empty[s], 4);  // the four warps of the consuming quad
     }
     ptx::mbar_init(&S.routed, 1);
-    for (int q = 0; q < kFQuads; ++q)
+    for (int q = 0; q < kFQuads; ++q) {
       for (int b = 0; b < kFRedBufs; ++b) {
-        ptx::mbar_init(&S.red_empty[q][b], 1);  // the pass's reducing warp
-        S.red_cnt[q][b] = 0;
+        ptx::mbar_init(&S.red_full[q][b], 4);   // the quad's four warps
+        ptx::mbar_init(&S.red_empty[q][b], 1);  // the reducer
       }
+      ptx::mbar_init(&S.red_done[q], 1);
+    }
     S.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -1183,6 +1252,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
     // phases ahead of a slot's barrier)
     int j = q;
     while (consume_gu(S, p, j, q, wq, lane, budget, npass)) j += kFQuads;
+    fwait(&S.red_done[q], 0, S, budget, p.status);
     grid_sync(p.grid_bar, bar_phase, S, budget, p.status);
     // every h is written: the down MMAs take the fp16 copies unless some h
     // is outside fp16's range
@@ -1196,6 +1266,9 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       grid_sync(p.grid_bar, bar_phase, S, budget, p.status);
       phase_combine(S, p);
     }
+  } else {
+    // ------------------------------------------------------------ reducers
+    reduce_gu(S, p, (warp >> 2) - 1, lane, budget);
   }
   __syncthreads();
   if (threadIdx.x == 0 && aborted(S)) set_status(p.status, MOE_DEV_TIMEOUT);
