@@ -125,6 +125,18 @@ struct FusedParams {
   unsigned long long budget_ns;
 };
 
+// Tensor maps of the gate|up rows and their scales ([0] routed, [1] shared):
+// one copy fetches a unit's 8 gate and 8 up rows (two blocks I rows apart),
+// another their scales, so a stage costs the copy engine two operations
+// rather than four.  Rows: (256 bytes, H/256 chunks, row, gate|up, expert),
+// box (256, H/256, 8, 2, 1).  Scales: (the 8 * H/128 scales of 8 rows, row
+// block, gate|up, expert), box (8 * H/128, 1, 2, 1).  ok = 0: bulk copies.
+struct FusedMaps {
+  CUtensorMap w[2];
+  CUtensorMap s[2];
+  int ok;
+};
+
 struct FusedSmem {
   uint8_t ring[kFStages][kFStageBytes];
   uint8_t ring_s[kFStages][kFScaleBytes];  // bf16 scales of each stage's rows
@@ -301,8 +313,9 @@ __device__ __forceinline__ int2 down_item(const FusedSmem &S, const FusedParams 
 
 // Producer: issue gate|up unit j (expert e, row pairs i0..i0+7) into ring
 // stage j % kFStages; false if the stage was not issued (abort).
-__device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p, int j, int e,
-                                           int i0, uint64_t pol, uint64_t budget, int lane) {
+__device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p,
+                                           const FusedMaps &maps, int j, int e, int i0,
+                                           uint64_t pol, uint64_t budget, int lane) {
   const int s = j % kFStages;
   int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
   if (lane == 0) {
@@ -314,7 +327,13 @@ __device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p, i
     }
   }
   if (!__shfl_sync(0xFFFFFFFFu, go, 0)) return false;
-  if (lane < 4) {
+  if (maps.ok) {
+    if (lane == 0) {
+      const int sh = e == kE ? 1 : 0;
+      ptx::tma_load_5d(S.ring[s], &maps.w[sh], 0, 0, i0, 0, sh ? 0 : e, &S.full[s], pol);
+      ptx::tma_load_4d(S.ring_s[s], &maps.s[sh], 0, i0 / 8, 0, sh ? 0 : e, &S.full[s], pol);
+    }
+  } else if (lane < 4) {
     // lanes 0/1: 8 consecutive gate / up rows, one contiguous copy of 8 * H
     // bytes each (bulk copies of >= 8 KB stream at full rate); lanes 2/3:
     // the bf16 group scales of those rows (8 * H/128 each)
@@ -1086,7 +1105,8 @@ __device__ __forceinline__ void phase_combine(FusedSmem &S, const FusedParams &p
   }
 }
 
-__global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedParams p) {
+__global__ void __launch_bounds__(kFThreads, 1)
+    decode_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedParams p) {
   extern __shared__ __align__(128) uint8_t fsmem_raw[];
   FusedSmem &S = *reinterpret_cast<FusedSmem *>(fsmem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1125,7 +1145,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       for (int i = 0; i < kFStages; ++i)
         if (jj % kFStages == i) last_use[i] = jj;
     };
-    if (early && produce_gu(S, p, 0, kE, 8 * blockIdx.x, pol, budget, lane)) issued_at(0);
+    if (early && produce_gu(S, p, maps, 0, kE, 8 * blockIdx.x, pol, budget, lane)) issued_at(0);
     if (lane == 0) fwait(&S.routed, 0, S, budget, p.status);
     __syncwarp();
     const Work wk = make_work(S, p);
@@ -1145,7 +1165,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       const unsigned nS = static_cast<unsigned>(wk.nSb);
       for (unsigned b = (blockIdx.x + G - nS % G) % G; b < n_routed && !aborted(S); b += G) {
         const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
-        if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
+        if (produce_gu(S, p, maps, j, e, i0, pol, budget, lane)) issued_at(j);
         ++j;
       }
     }
@@ -1167,7 +1187,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(const FusedP
       const unsigned end = min(claim + gu_claim, n_routed);
       for (unsigned b = claim; b < end && !aborted(S); ++b) {
         const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
-        if (produce_gu(S, p, j, e, i0, pol, budget, lane)) issued_at(j);
+        if (produce_gu(S, p, maps, j, e, i0, pol, budget, lane)) issued_at(j);
         ++j;
       }
       claim = __shfl_sync(0xFFFFFFFFu, ahead0, 0);
@@ -1346,6 +1366,47 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
   p.ids_out = ids_out; p.weights_out = weights_out; p.logits_out = logits_out;
   p.gate_logit_out = gate_logit_out; p.status = status; p.grid_bar = grid_bar;
   p.budget_ns = fused_wait_budget_ns();
+  // tensor maps of the gate|up rows and scales, kept per thread for the last
+  // weight set (encoding them takes host time on every call otherwise)
+  struct MapKey {
+    const void *w, *ws, *sc, *ssc;
+    int H, I, Is, dev;
+    bool operator==(const MapKey &o) const {
+      return w == o.w && ws == o.ws && sc == o.sc && ssc == o.ssc && H == o.H && I == o.I &&
+             Is == o.Is && dev == o.dev;
+    }
+  };
+  static thread_local MapKey mkey{};
+  static thread_local FusedMaps maps{};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const MapKey key{w.w13_q, w.ws13_q, w.w13_s, w.ws13_s, H, I, Is, dev};
+  if (!(key == mkey) || !maps.ok) {
+    FusedMaps m{};
+    const uint64_t ng = static_cast<uint64_t>(H) / kG;
+    auto rows_map = [&](CUtensorMap *t, const void *base, uint64_t half, uint64_t ne) {
+      const uint64_t dims[5] = {256, static_cast<uint64_t>(H) / 256, half, 2, ne};
+      const uint64_t str[4] = {256, static_cast<uint64_t>(H), half * H, 2 * half * H};
+      const uint32_t box[5] = {256, static_cast<uint32_t>(H / 256), 8, 2, 1};
+      return tc_make_map_nd(t, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, dims, str, box);
+    };
+    auto scale_map = [&](CUtensorMap *t, const void *base, uint64_t half, uint64_t ne) {
+      const uint64_t dims[4] = {8 * ng, half / 8, 2, ne};
+      const uint64_t str[3] = {16 * ng, half * ng * 2, 2 * half * ng * 2};
+      const uint32_t box[4] = {static_cast<uint32_t>(8 * ng), 1, 2, 1};
+      return tc_make_map_nd(t, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, str, box);
+    };
+    bool ok = rows_map(&m.w[0], w.w13_q, I, kE) && scale_map(&m.s[0], w.w13_s, I, kE);
+    if (Is > 0) {
+      ok = ok && rows_map(&m.w[1], w.ws13_q, Is, 1) && scale_map(&m.s[1], w.ws13_s, Is, 1);
+    } else {
+      m.w[1] = m.w[0];
+      m.s[1] = m.s[0];
+    }
+    m.ok = ok ? 1 : 0;
+    maps = m;
+    mkey = key;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(device_sms());
   cfg.blockDim = dim3(kFThreads);
@@ -1356,7 +1417,7 @@ cudaError_t launch_decode_fused(const moe_bf16 *x, int T, int H, int I, int Is,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_fused_kernel, p);
+  return cudaLaunchKernelEx(&cfg, decode_fused_kernel, maps, p);
 }
 
 }  // namespace moe

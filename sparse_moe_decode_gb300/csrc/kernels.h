@@ -116,6 +116,11 @@ bool tc_make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
 // of dims 1 and 2, box innermost first; 128-byte swizzle, zero fill.
 bool tc_make_map3(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
                   const uint64_t dims[3], const uint64_t strides[2], const uint32_t box[3]);
+// Tensor of rank 1..5, dims innermost first, byte strides of dims 1..rank-1,
+// box innermost first; no swizzle (rows land in shared memory as they lie in
+// global memory), no fill.
+bool tc_make_map_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int rank,
+                    const uint64_t *dims, const uint64_t *strides, const uint32_t *box);
 int tc_sm_count();
 // Budget of every bounded wait in the tcgen05 kernels (MOE_WAIT_BUDGET_NS, default 2 s).
 unsigned long long tc_wait_budget_ns();

@@ -230,6 +230,23 @@ bool tc_make_map3(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tc_make_map_nd(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int rank,
+                    const uint64_t *dims, const uint64_t *strides, const uint32_t *box) {
+  EncodeTiledFn enc = encoder();
+  if (!enc || !base || rank < 1 || rank > 5) return false;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bx[5], estr[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bx[i] = box[i];
+    estr[i] = 1;
+    if (i + 1 < rank) gstride[i] = strides[i];
+  }
+  return enc(m, dt, static_cast<cuuint32_t>(rank), const_cast<void *>(base), gdim, gstride, bx,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_sm_count() {
   static int n[64] = {0};
   int dev = 0;
