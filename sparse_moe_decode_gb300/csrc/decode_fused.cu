@@ -406,6 +406,40 @@ __device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p,
   return true;
 }
 
+// Producer, item mode: issue down item (e, n0) = rows n0 .. n0 + nr - 1 of
+// expert e's down matrix (nr * K contiguous bytes, lane 0) and their group
+// scales (lane 1) into ring stage j % kFStages.  The addresses are formed
+// before the wait and both copies go out in one instruction: the producer's
+// time per stage bounds the stream.  False if the stage was not issued.
+__device__ __forceinline__ bool produce_item(FusedSmem &S, const FusedParams &p, const Work &wk,
+                                             int j, int e, int n0, uint64_t pol,
+                                             uint64_t budget, int lane) {
+  const int s = j % kFStages;
+  const bool sh = e == kE;
+  const int Ii = sh ? p.Is : p.I;
+  const int ng = Ii / kG;
+  const int nr = min(wk.down_rows, p.H - n0);
+  const uint32_t wbytes = static_cast<uint32_t>(nr) * Ii, sbytes = 2u * nr * ng;
+  const size_t row0 = sh ? static_cast<size_t>(n0) : static_cast<size_t>(e) * p.H + n0;
+  const void *src = lane == 0 ? static_cast<const void *>((sh ? p.ws2_q : p.w2_q) + row0 * Ii)
+                              : static_cast<const void *>((sh ? p.ws2_s : p.w2_s) + row0 * ng);
+  void *dst = lane == 0 ? static_cast<void *>(S.ring[s]) : static_cast<void *>(S.ring_s[s]);
+  const uint32_t bytes = lane == 0 ? wbytes : sbytes;
+  int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
+  if (lane == 0) {
+    fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget, p.status);
+    go = aborted(S) ? 0 : 1;
+    if (go) {
+      S.stage_unit[s] = make_int2(e, n0);  // published by the arrival below
+      ptx::mbar_expect_tx(&S.full[s], wbytes + sbytes);
+    }
+  }
+  if (!__shfl_sync(0xFFFFFFFFu, go, 0)) return false;
+  if (lane < 2) bulk_g2s(dst, src, bytes, &S.full[s], pol);
+  __syncwarp();
+  return true;
+}
+
 // Token scaling for the fp16 tensor-core path: token t becomes x * 2^-s in
 // fp16 with s = exponent(max |x_t|) - 14, so the largest magnitude lands in
 // [2^14, 2^15).  A bf16 value (8 significant bits) is exact in fp16 whenever
@@ -1185,7 +1219,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     while (claim < n_routed && !aborted(S)) {
       const unsigned end = min(claim + gu_claim, n_routed);
-      for (unsigned b = claim; b < end && !aborted(S); ++b) {
+      for (unsigned b = claim; b < end; ++b) {
         const int e = S.active[1 + b / wk.nIb], i0 = 8 * static_cast<int>(b % wk.nIb);
         if (produce_gu(S, p, maps, j, e, i0, pol, budget, lane)) issued_at(j);
         ++j;
@@ -1235,8 +1269,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     while (claim < n_down && !aborted(S)) {
       const unsigned end = min(claim + per_claim, n_down);
-      for (unsigned b = claim; b < end && !aborted(S); ++b, ++j)
-        if (produce_down(S, p, wk, j, down_item(S, p, wk, b), pol, budget, lane)) issued_at(j);
+      for (unsigned b = claim; b < end; ++b, ++j) {
+        const int2 it = down_item(S, p, wk, b);
+        if (produce_item(S, p, wk, j, it.x, it.y, pol, budget, lane)) issued_at(j);
+      }
       claim = __shfl_sync(0xFFFFFFFFu, ahead0, 0);
       ahead0 = ahead1;
       ahead1 = n_down;
