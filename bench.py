@@ -172,17 +172,17 @@ def down_bytes(d: W.Dims, T: int, n_active: int):
 # one ncu capture of each kernel (summaries under profiles/), valid only while
 # the kernel's sources hash to the value recorded with the capture.
 MEASURED_TRAFFIC = {
-    "decode_fused": {"bytes": 529.9e6, "workload": "verify_T32",
+    "decode_fused": {"bytes": 530.1e6, "workload": "verify_T32",
                      "sources": ["decode_fused.cu", "common.cuh", "select.cuh", "sm100_ptx.cuh"],
-                     "sha256_16": "ece74c63b970a1fb",
+                     "sha256_16": "f3c341e56ddfe1bd",
                      "profile": "profiles/decode_fused_verify_T32.md"},
-    "gateup_swiglu_tc": {"bytes": 646.5e6, "workload": "prefill_T2048",
+    "gateup_swiglu_tc": {"bytes": 645.6e6, "workload": "prefill_T2048",
                          "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],
-                         "sha256_16": "15d66d1e5a1f6cff",
+                         "sha256_16": "fb7eb20b93e03113",
                          "profile": "profiles/split_kernels_prefill_T2048.md"},
-    "down_combine_tc": {"bytes": 315.8e6, "workload": "prefill_T2048",
+    "down_combine_tc": {"bytes": 312.8e6, "workload": "prefill_T2048",
                         "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],
-                        "sha256_16": "15d66d1e5a1f6cff",
+                        "sha256_16": "fb7eb20b93e03113",
                         "profile": "profiles/split_kernels_prefill_T2048.md"},
 }
 
