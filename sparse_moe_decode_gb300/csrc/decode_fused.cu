@@ -886,9 +886,12 @@ __device__ __forceinline__ void reduce_gu(FusedSmem &S, const FusedParams &p, in
     }
   }
   if (__any_sync(0xFFFFFFFFu, wide) && lane == 0) atomicOr(p.h_wide, 1u);
-  // every h of this quad (and the flag) ordered before the consumers' grid
-  // barrier, which follows their wait for red_done
-  __threadfence();
+  // Every h of this quad (and the flag) reaches the other CTAs through a
+  // chain that needs no fence here: this release arrival (after the warp
+  // barrier), the consumers' acquire wait for red_done, the CTA barrier of
+  // their grid barrier and its gpu-scope release reduction, whose acquire
+  // load in every other CTA precedes the reads of h (causality order is
+  // transitive across these scopes).
   __syncwarp();
   if (lane == 0) ptx::mbar_arrive(&S.red_done[q]);
 }
