@@ -601,7 +601,7 @@ __device__ __forceinline__ void select_token(FusedSmem &S, const FusedParams &p,
   }
   int id[8];
   float w[8];
-  const bool ok = select_top8_regs(v, lane, id, w);
+  const bool ok = select_top8_rounds(v, lane, id, w);
   if (lane < 8) {
     int myid = id[0];
     float myw = w[0];

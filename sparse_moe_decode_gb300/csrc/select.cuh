@@ -130,6 +130,75 @@ __device__ __forceinline__ void select_top8_multi(const float (&v)[N][8], int la
   }
 }
 
+// One token, fewest dependent steps (the fused decode kernel selects each
+// token once per launch, on the critical path of the whole block): each
+// lane sorts its 8 keys once; then 8 rounds each take the warp's best head.
+// A round reduces the heads' value halves with one warp max; among the lanes
+// holding that value the lowest holds the lowest expert ids (lane l owns
+// experts 8l .. 8l+7), and its head is its own best under the total order,
+// so it is the round's winner; it broadcasts its key and drops it.  The
+// selected (value, id) pairs and their rank order are those of the merge
+// network above (both are the selector's total order), and the softmax below
+// is the same arithmetic in the same order, so the results are identical.
+// Same contract as select_top8_regs.
+__device__ __forceinline__ bool select_top8_rounds(const float (&v)[8], int lane, int (&ids)[8],
+                                                   float (&w)[8]) {
+  uint64_t k[8];
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    finite &= isfinite(v[i]);
+    k[i] = rank_key(v[i], 8 * lane + i);
+  }
+  const bool ok = __all_sync(0xFFFFFFFFu, finite);
+  sort8(k);
+  uint64_t best[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    // every finite key's value half is at least 0x00800000, so a drained
+    // lane's zero head never ties a real one
+    const uint32_t hi = static_cast<uint32_t>(k[0] >> 32);
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const int win = __ffs(__ballot_sync(0xFFFFFFFFu, hi == m)) - 1;
+    best[r] = __shfl_sync(0xFFFFFFFFu, k[0], win);
+    if (lane == win) {
+#pragma unroll
+      for (int i = 0; i < 7; ++i) k[i] = k[i + 1];
+      k[7] = 0;
+    }
+  }
+  const float z0 = key_value(best[0]);
+  float e[8], s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    e[i] = expf(key_value(best[i]) - z0);
+    s += e[i];
+  }
+  const float inv = 1.0f / s;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ids[i] = ok ? key_id(best[i]) : -1;
+    w[i] = ok ? e[i] * inv : 0.0f;
+  }
+  if (MOE_SABOTAGE == 1 && ok) {  // test-only build (see common.cuh)
+    int e8 = ids[7];
+    bool taken = true;
+    while (taken) {
+      e8 = (e8 + 1) & 255;
+      taken = false;
+#pragma unroll
+      for (int i = 0; i < 7; ++i) taken |= ids[i] == e8;
+    }
+    ids[7] = e8;
+  }
+  if (MOE_SABOTAGE == 2) {  // test-only build (see common.cuh)
+    const float t = w[6];
+    w[6] = w[7];
+    w[7] = t;
+  }
+  return ok;
+}
+
 // One token (see select_top8_multi); returns false for a non-finite row.
 __device__ __forceinline__ bool select_top8_regs(const float (&v)[8], int lane, int (&ids)[8],
                                                  float (&w)[8]) {
