@@ -1,9 +1,9 @@
 // decode_fused.cu -- the whole block (A1..A7) for decode-size T in one
 // persistent cooperative kernel: one CTA per SM, 16 warps (the producer
-// warp alone on one SM sub-partition with three idle warps, twelve
-// consumer warps in three quads on the other three), phases separated by
-// bounded grid barriers (two, one more when T > 12 for the shared
-// selection, one more when T > 8 for the item-mode combine).
+// warp and three reducer warps on one SM sub-partition, twelve consumer
+// warps in three quads on the other three), phases separated by bounded
+// grid barriers (two, one more when T > 24 for the shared selection, one
+// more when T > 8 for the item-mode combine).
 //
 //   R  router: each CTA stages one 512-wide K-slice of every token and of
 //      up to 16 of the 257 rows (256 experts + the shared gate) in shared
@@ -12,24 +12,24 @@
 //      scales token t into fp16 for phase W;
 //   -- grid barrier 1 --
 //   S  one warp per token folds the partials in a fixed order and selects
-//      the top-8 with the warp merge network (softmax, shared sigmoid); for
-//      T <= 12 every CTA selects every token itself, so every CTA holds the
-//      same selection; for larger T the grid shares the tokens and a grid
-//      barrier publishes the selections;
+//      the top-8 (8 warp-max rounds over lane-sorted keys; softmax, shared
+//      sigmoid); for T <= 24 every CTA selects every token itself, so every
+//      CTA holds the same selection; for larger T each token is selected
+//      once in the grid and a grid barrier publishes the selections;
 //   L  every CTA builds the token -> expert lists in shared memory;
 //   W  gate|up + SwiGLU: work unit = 8 gate rows + their 8 up rows of one
 //      expert (16 rows x H int8); the first Is / 8 CTAs take one shared
 //      unit each before routing is known, and the routed units are claimed
 //      from a grid-wide counter, so that faster CTAs take more of them; the
-//      producer streams each unit's rows and group scales with bulk async
-//      copies into a 6-stage shared-memory ring; quad q consumes ring
-//      stages q, q + 3, ..., each warp a quarter of K, as m16n8k16 fp16
-//      tensor-core MMAs: the int8 weights become fp16 exactly in registers,
-//      the activations are each token's copy scaled by a power of two into
-//      fp16 (exact for every element within 2^29 of the token's largest),
-//      the group scales are promoted per 128-wide K group in fp32, a
-//      rotating reducer warp adds the four K quarters; h = bf16(silu(gate)
-//      * up) goes to global, with an fp16 copy of each value;
+//      producer streams each unit's rows and group scales with two
+//      tensor-map copies into a 6-stage shared-memory ring; quad q consumes
+//      ring stages q, q + 3, ..., each warp a quarter of K, as m16n8k16
+//      fp16 tensor-core MMAs: the int8 weights become fp16 exactly in
+//      registers, the activations are each token's copy scaled by a power
+//      of two into fp16 (exact for every element within 2^29 of the
+//      token's largest), the group scales are promoted per 128-wide K group
+//      in fp32; the quad's reducer warp adds the four K quarters in a fixed
+//      order and writes h = bf16(silu(gate) * up), with an fp16 copy;
 //   -- grid barrier 2 --
 //   D  down + combine, two modes chosen by T (the same in every CTA); each
 //      quad's down stages continue its own ring sequence past its gate|up
@@ -48,12 +48,15 @@
 //      rows itself.  Both combine the 8 routed y in rank order, then the
 //      shared expert's, with one bf16 rounding.
 //
-// The tensor cores here are the register-fragment form (mma.sync): at
-// decode sizes each weight meets 1..~10 tokens, the kernel is bound by HBM,
-// and register fragments avoid a shared-memory round trip for the converted
-// weights.  Every wait (mbarrier, grid barrier) is bounded by a %globaltimer
-// budget; a wait that gives up sets MOE_DEV_TIMEOUT and the kernel runs to
-// its end without waiting again.
+// The producer's time per stage bounds the stream once the consumers keep
+// up, so it issues as few copy operations per stage as the layout allows
+// and forms addresses before its waits.  The tensor cores here are the
+// register-fragment form (mma.sync): at decode sizes each weight meets
+// 1..~10 tokens, the kernel is bound by HBM, and register fragments avoid a
+// shared-memory round trip for the converted weights.  Every wait
+// (mbarrier, grid barrier) is bounded by a %globaltimer budget; a wait that
+// gives up sets MOE_DEV_TIMEOUT and the kernel runs to its end without
+// waiting again.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -86,7 +89,10 @@ constexpr int kFScaleBytes = 512;              // the group scales of a stage's 
 constexpr int kFPass = 8;                    // gate|up tokens per pass (one n8 tile)
 constexpr int kFDownPass = 16;               // down tokens per pass (two n8 tiles)
 constexpr int kRP = 260;                     // router partial row: 257 used, 16-byte rows
-constexpr int kFLocalSelT = kFConsumerWarps;  // tokens selected by every CTA itself
+// Up to this T every CTA selects every token itself (at most two per warp),
+// which costs less than a grid-shared selection's extra grid barrier and
+// read-back; above it each token is selected once in the grid.
+constexpr int kFLocalSelT = 2 * kFConsumerWarps;
 constexpr int kFClaim = 4;  // routed gate|up units per claim when there are many
 constexpr int kFRowOwnerT = 8;  // down phase in row-owner mode up to this T
 
@@ -633,20 +639,20 @@ __device__ __forceinline__ void select_token(FusedSmem &S, const FusedParams &p,
 }
 
 // Phases S and L.  T <= kFLocalSelT: every CTA selects all T tokens itself
-// (one warp per token, the same fold order and merge network in every CTA,
-// so every CTA holds the same selection), with no grid barrier between
-// selection and lists.  Larger T: one warp of the grid per token, a grid
-// barrier, and every CTA reads all selections.  Then every CTA builds the
-// token -> expert lists in shared memory.
+// (warp w takes tokens w, w + 12, ..., with the same fold order and
+// selection in every CTA, so every CTA holds the same selection), with no
+// grid barrier between selection and lists.  Larger T: one warp of the grid
+// per token (one token per CTA), a grid barrier, and every CTA reads all
+// selections.  Then every CTA builds the token -> expert lists in shared
+// memory.
 __device__ __forceinline__ void phase_select_lists(FusedSmem &S, const FusedParams &p, int cwarp,
                                                    int lane, unsigned &phase, uint64_t budget) {
   const int tid = consumer_tid();
-  // independent of the selection, so done first, by the last warps (idle
-  // during a local selection of T < 12 tokens)
+  // independent of the selection, so done first, by the last warps
   for (int t2 = kFConsumers - 1 - tid; t2 < p.T; t2 += kFConsumers)
     S.xs[t2] = __ldcg(p.xscale + t2);
   if (p.T <= kFLocalSelT) {
-    if (cwarp < p.T) select_token(S, p, cwarp, lane, true);
+    for (int t = cwarp; t < p.T; t += kFConsumerWarps) select_token(S, p, t, lane, true);
   } else {
     // one token per CTA (consumer warp 0): the merge network is bound by
     // issue, so tokens that share an SM sub-partition take turns
