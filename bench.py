@@ -189,8 +189,8 @@ MEASURED_TRAFFIC = {
 
 # The candidate selector's first kernel, captured at 64 rows (the runs it
 # writes stay in L2; the merge kernel reads them there): DRAM bytes per row.
-CANDIDATES_TRAFFIC = {"bytes_per_row": 38.92e6 / 64, "rows_captured": 64,
-                      "sources": ["topk.cu", "common.cuh"], "sha256_16": "976a791dcb403cf7",
+CANDIDATES_TRAFFIC = {"bytes_per_row": 38.93e6 / 64, "rows_captured": 64,
+                      "sources": ["topk.cu", "common.cuh"], "sha256_16": "382c56906eaa3e6e",
                       "profile": "profiles/topk_chunk_candidates_T64.md"}
 
 
