@@ -105,7 +105,7 @@ def test_block_verify_T32_skewed(env):
     assert len(np.unique(g["ids"])) > 100  # many distinct experts are active
 
 
-@pytest.mark.parametrize("T", [2, 12, 13, 19, 20, 46, 47, 64, 65, 100, 768, 4097])
+@pytest.mark.parametrize("T", [2, 12, 13, 19, 20, 24, 25, 46, 47, 64, 65, 100, 768, 4097])
 def test_block_decode_dims_T_sweep(env, T):
     moe, dev = env
     dims, _ = workload("decode")
