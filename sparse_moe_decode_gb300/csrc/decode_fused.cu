@@ -364,31 +364,27 @@ __device__ __forceinline__ bool produce_gu(FusedSmem &S, const FusedParams &p,
   return true;
 }
 
-// Producer: issue down stage j.  Item mode: item (e, n0) = rows n0 ..
-// n0 + nr - 1 of expert e's down matrix (nr * K contiguous bytes) and their
-// group scales.  Row-owner mode (item = (kE + 1, k)): this CTA's stage k,
-// the 16 rows n0 of down experts k * U .., one contiguous copy each, at a
-// fixed stride.  False if the stage was not issued (abort).
-__device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p, const Work &wk,
-                                             int j, int2 item, uint64_t pol, uint64_t budget,
+// Producer, row-owner mode: issue this CTA's down stage k into ring stage
+// j % kFStages: the 16 output rows n0 of down experts k * U .. k * U + U - 1
+// (one contiguous copy of 16 * K bytes each, at a fixed stride in the stage)
+// and their group scales.  False if the stage was not issued (abort).
+__device__ __forceinline__ bool produce_rows(FusedSmem &S, const FusedParams &p, const Work &wk,
+                                             int j, int k, uint64_t pol, uint64_t budget,
                                              int lane) {
   const int s = j % kFStages;
-  const bool rows = item.x > kE;
-  const int a0 = rows ? item.y * wk.units_per_stage : 0;
-  const int nu = rows ? min(wk.units_per_stage, wk.n_exp - a0) : 1;
+  const int a0 = k * wk.units_per_stage;
+  const int nu = min(wk.units_per_stage, wk.n_exp - a0);
   int go = 0;  // lane 0 decides for the whole warp (the flag may be set meanwhile)
   if (lane == 0) {
     fwait(&S.empty[s], ((j / kFStages) & 1) ^ 1, S, budget, p.status);
     uint32_t tx = 0;
     for (int u = 0; u < nu; ++u) {
-      const int e = rows ? down_expert(S, p, a0 + u) : item.x;
-      const int Ii = e == kE ? p.Is : p.I;
-      const int nr = rows ? 16 : min(wk.down_rows, p.H - item.y);
-      tx += static_cast<uint32_t>(nr) * Ii + 2u * nr * (Ii / kG);
+      const int Ii = down_expert(S, p, a0 + u) == kE ? p.Is : p.I;
+      tx += 16u * Ii + 2u * 16 * (Ii / kG);
     }
     go = aborted(S) ? 0 : 1;
     if (go) {
-      S.stage_unit[s] = item;  // published by the arrival below
+      S.stage_unit[s] = make_int2(kE + 1, k);  // published by the arrival below
       ptx::mbar_expect_tx(&S.full[s], tx);
     }
   }
@@ -396,20 +392,18 @@ __device__ __forceinline__ bool produce_down(FusedSmem &S, const FusedParams &p,
   if (lane < 2 * nu) {
     // lane u < nu: unit u's rows; lane nu + u: their group scales
     const int u = lane < nu ? lane : lane - nu;
-    const int e = rows ? down_expert(S, p, a0 + u) : item.x;
+    const int e = down_expert(S, p, a0 + u);
     const int Ii = e == kE ? p.Is : p.I;
     const int ng = Ii / kG;
-    const int n0 = rows ? wk.n0 : item.y;
-    const int nr = rows ? 16 : min(wk.down_rows, p.H - n0);
+    const int n0 = wk.n0;
     if (lane < nu) {
       const int8_t *src = e == kE ? p.ws2_q + static_cast<size_t>(n0) * p.Is
                                   : p.w2_q + (static_cast<size_t>(e) * p.H + n0) * p.I;
-      bulk_g2s(S.ring[s] + u * wk.unit_stride, src, static_cast<uint32_t>(nr) * Ii, &S.full[s],
-               pol);
+      bulk_g2s(S.ring[s] + u * wk.unit_stride, src, 16u * Ii, &S.full[s], pol);
     } else {
       const moe_bf16 *src = e == kE ? p.ws2_s + static_cast<size_t>(n0) * ng
                                     : p.w2_s + (static_cast<size_t>(e) * p.H + n0) * ng;
-      bulk_g2s(S.ring_s[s] + u * wk.scale_stride, src, 2u * nr * ng, &S.full[s], pol);
+      bulk_g2s(S.ring_s[s] + u * wk.scale_stride, src, 2u * 16 * ng, &S.full[s], pol);
     }
   }
   __syncwarp();
@@ -1258,7 +1252,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     end_markers();
     if (wk.row_owner) {
       for (int k = 0; k < wk.n_down_stages && !aborted(S); ++k, ++j)
-        if (produce_down(S, p, wk, j, make_int2(kE + 1, k), pol, budget, lane)) issued_at(j);
+        if (produce_rows(S, p, wk, j, k, pol, budget, lane)) issued_at(j);
     }
     // Down items, claimed from their own counter the same way (their costs
     // differ with the expert's token count, so a static split would not
