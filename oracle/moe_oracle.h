@@ -14,7 +14,8 @@
  *     (the down projections consume 16-bit activations);
  *   - the block output is rounded to bf16 (round to nearest, ties to even).
  *
- * Sources (ninfer-windows PR #8, "...in place of eight dependent rounds"):
+ * Sources (ninfer-windows PR #8, the commit that swaps eight dependent
+ * selection rounds for a warp merge network):
  *   router + 257th shared-gate row ......... the S1/S2 description and its
  *                                            roofline paragraph (T x 257 rows)
  *   total order "greater value, lower id" .. the bit-identity paragraph

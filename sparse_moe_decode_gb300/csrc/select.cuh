@@ -1,6 +1,7 @@
 // select.cuh -- warp-per-token top-8 selection (A2).
 //
-// Method (ninfer-windows PR #8, "...in place of eight dependent rounds"):
+// Method (ninfer-windows PR #8, the commit that swaps eight dependent
+// selection rounds for a warp merge network):
 // each lane holds 8 candidates sorted under the selector's total order; five
 // xor exchanges merge runs pairwise, each exchange being 8 independent
 // shuffles followed by three compare-exchange stages over static indices.
