@@ -174,7 +174,7 @@ def down_bytes(d: W.Dims, T: int, n_active: int):
 MEASURED_TRAFFIC = {
     "decode_fused": {"bytes": 529.7e6, "workload": "verify_T32",
                      "sources": ["decode_fused.cu", "common.cuh", "select.cuh", "sm100_ptx.cuh"],
-                     "sha256_16": "7f8a2cd6643551ad",
+                     "sha256_16": "9f47c0b17b71b145",
                      "profile": "profiles/decode_fused_verify_T32.md"},
     "gateup_swiglu_tc": {"bytes": 645.6e6, "workload": "prefill_T2048",
                          "sources": ["tc_expert.cu", "common.cuh", "sm100_ptx.cuh"],
